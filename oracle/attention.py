@@ -21,8 +21,9 @@ Backward of the loss sum(dO * O):
 dK_j / dV_j are scattered back onto the Kc/Vc and Kd/Vd rows they came from
 and summed over the query heads of the kv group.
 
-Every input is a float64 array holding exactly the values the device sees
-(the compute-dtype rounding happens before the upcast).
+Every input holds exactly the values the device sees (the compute-dtype
+rounding happens before); slices are upcast to float64 before any
+arithmetic, so float32 arrays of bf16-rounded values are accepted as well.
 """
 from __future__ import annotations
 
@@ -70,10 +71,10 @@ def forward(w, Q, Kc, Vc, Kd, Vd, blocks=None, heads=None):
         c0 = int(w.cu_ctx[s])
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0)
-            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0)
+            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0).astype(np.float64)
             for h in hlist:
-                S = scale * (Q[rows, h] @ keys.T)
+                S = scale * (Q[rows, h].astype(np.float64) @ keys.T)
                 lse = _logsumexp_rows(S)
                 P = np.exp(S - lse[:, None])
                 O[rows, h] = P @ vals
@@ -101,13 +102,13 @@ def backward(w, Q, Kc, Vc, Kd, Vd, dO, blocks=None, heads=None):
         c0 = int(w.cu_ctx[s])
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0)
-            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0)
+            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0).astype(np.float64)
             dK = np.zeros_like(keys)
             dV = np.zeros_like(vals)
             for h in hlist:
-                q = Q[rows, h]
-                do = dO[rows, h]
+                q = Q[rows, h].astype(np.float64)
+                do = dO[rows, h].astype(np.float64)
                 S = scale * (q @ keys.T)
                 lse = _logsumexp_rows(S)
                 P = np.exp(S - lse[:, None])
@@ -150,10 +151,11 @@ def partial_forward(w, Q, Kc, Vc, Kd, Vd, lo: int, hi: int, draft: bool):
                 if k1 <= k0:
                     continue
                 keys, vals = Kc[c0 + k0:c0 + k1, g], Vc[c0 + k0:c0 + k1, g]
-            S = scale * (Q[rows, h] @ keys.T)
+            keys = keys.astype(np.float64)
+            S = scale * (Q[rows, h].astype(np.float64) @ keys.T)
             lse = _logsumexp_rows(S)
             lse_out[h, rows] = lse
-            O_out[rows, h] = np.exp(S - lse[:, None]) @ vals
+            O_out[rows, h] = np.exp(S - lse[:, None]) @ vals.astype(np.float64)
     return lse_out, O_out
 
 

@@ -257,7 +257,10 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     values ``torch.Tensor.to(torch.bfloat16)`` produces for finite inputs.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    bias = ((bits >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
-    out = ((bits + bias) & np.uint64(0xFFFF0000)).astype(np.uint32)
+    bits = x.view(np.uint32)
+    # finite inputs: bits + 0x8000 stays below 2**32, so uint32 arithmetic is exact
+    out = (bits >> np.uint32(16)) & np.uint32(1)
+    out += np.uint32(0x7FFF)
+    out += bits
+    out &= np.uint32(0xFFFF0000)
     return out.view(np.float32).reshape(x.shape)
