@@ -1,0 +1,270 @@
+"""Python binding of libsplitkv (include/splitkv.h): argument marshalling only.
+
+Every entry point of the C ABI is exposed under the same name and takes the
+same arguments (ctypes pointers/ints; torch tensors are accepted wherever the
+C function takes a device pointer). All arithmetic runs in the library's
+CUDA kernels; there is no CPU path. If the shared library is missing this
+module raises at import time.
+
+The ``SplitKV`` helper bundles a problem, its two workspaces and the three
+passes for callers that hold their tensors in torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Dict, Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsplitkv.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "splitkv.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python block_sparse_cross_gb300/build.py` "
+        "(no CPU fallback exists)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- constants (mirrors include/splitkv.h) ---------------------------------
+SPLITKV_OK = 0
+SPLITKV_EINVAL = 1
+SPLITKV_EUNSUPPORTED = 2
+SPLITKV_EWORKSPACE = 3
+SPLITKV_ECUDA = 4
+SPLITKV_EDEVICE = 5
+SPLITKV_ETIMEOUT = 6
+SPLITKV_EPLAN = 7
+SPLITKV_EMETA = 8
+SPLITKV_ECAPACITY = 9
+SPLITKV_BF16 = 0
+SPLITKV_FP32 = 1
+SPLITKV_FLAG_CUDA_CORE = 1
+SPLITKV_FLAG_CONTIGUOUS = 2
+
+
+class splitkv_problem(ctypes.Structure):
+    _fields_ = [
+        ("num_samples", ctypes.c_int32),
+        ("cu_ctx", ctypes.c_void_p),
+        ("cu_anchor", ctypes.c_void_p),
+        ("anchors", ctypes.c_void_p),
+        ("total_ctx", ctypes.c_int64),
+        ("total_anchors", ctypes.c_int64),
+        ("max_ctx", ctypes.c_int32),
+        ("B", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("chunk", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("dtype", ctypes.c_int32),
+        ("num_workers", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
+    ]
+
+
+class splitkv_stats(ctypes.Structure):
+    _fields_ = [
+        ("device_status", ctypes.c_int32),
+        ("workers", ctypes.c_int32),
+        ("fwd_items", ctypes.c_int64),
+        ("bwd_items", ctypes.c_int64),
+        ("fwd_slots", ctypes.c_int64),
+        ("fwd_total_cost", ctypes.c_int64),
+        ("bwd_total_cost", ctypes.c_int64),
+        ("fwd_lpt_max_load", ctypes.c_int64),
+        ("fwd_contig_max_load", ctypes.c_int64),
+        ("bwd_lpt_max_load", ctypes.c_int64),
+        ("bwd_contig_max_load", ctypes.c_int64),
+        ("fwd_lpt_imbalance", ctypes.c_double),
+        ("fwd_contig_imbalance", ctypes.c_double),
+        ("bwd_lpt_imbalance", ctypes.c_double),
+        ("bwd_contig_imbalance", ctypes.c_double),
+        ("fwd_tiles", ctypes.c_int64),
+        ("dense_tiles", ctypes.c_int64),
+        ("work_bytes_used", ctypes.c_size_t),
+    ]
+
+    def as_dict(self) -> Dict[str, object]:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_P = ctypes.POINTER(splitkv_problem)
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "splitkv_workspace_size": ([_P, ctypes.POINTER(_sz), ctypes.POINTER(_sz)], ctypes.c_int),
+    "splitkv_plan": ([_P, _vp, _sz, _vp], ctypes.c_int),
+    "splitkv_fwd": ([_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    "splitkv_bwd": ([_P, _vp] + [_vp] * 14 + [_sz, _vp], ctypes.c_int),
+    "splitkv_plan_stats": ([_P, _vp, ctypes.POINTER(splitkv_stats), _vp], ctypes.c_int),
+    "splitkv_plan_export": ([_P, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_int64,
+                             ctypes.POINTER(ctypes.c_int64), _vp], ctypes.c_int),
+    "splitkv_device_status": ([_P, _vp, ctypes.POINTER(ctypes.c_int), _vp], ctypes.c_int),
+    "splitkv_resolve_workers": ([_P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "splitkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+def header_functions() -> list:
+    """Names of every function declared in include/splitkv.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(splitkv_\w+)\(", text, re.M)))
+
+
+def _ptr(x) -> Optional[int]:
+    """Device pointer of a torch tensor, or an int / None passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class SplitKVError(RuntimeError):
+    def __init__(self, where: str, status: int):
+        super().__init__(f"{where}: {splitkv_status_string(status)} ({status})")
+        self.status = status
+
+
+def _check(where: str, st: int) -> None:
+    if st != SPLITKV_OK:
+        raise SplitKVError(where, st)
+
+
+# ---- same-name wrappers ----------------------------------------------------
+def splitkv_status_string(status: int) -> str:
+    return _lib.splitkv_status_string(int(status)).decode()
+
+
+def splitkv_workspace_size(prob: splitkv_problem):
+    """Returns (status, plan_bytes, work_bytes)."""
+    pb, wb = _sz(0), _sz(0)
+    st = _lib.splitkv_workspace_size(ctypes.byref(prob), ctypes.byref(pb), ctypes.byref(wb))
+    return st, pb.value, wb.value
+
+
+def splitkv_resolve_workers(prob: splitkv_problem):
+    w = ctypes.c_int(0)
+    st = _lib.splitkv_resolve_workers(ctypes.byref(prob), ctypes.byref(w))
+    return st, w.value
+
+
+def splitkv_plan(prob, plan_ws, plan_bytes: int, stream=None) -> int:
+    return _lib.splitkv_plan(ctypes.byref(prob), _ptr(plan_ws), plan_bytes, _stream(stream))
+
+
+def splitkv_fwd(prob, plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE, work, work_bytes: int,
+                stream=None) -> int:
+    return _lib.splitkv_fwd(ctypes.byref(prob), _ptr(plan_ws), _ptr(Q), _ptr(Kc), _ptr(Vc),
+                            _ptr(Kd), _ptr(Vd), _ptr(O), _ptr(LSE), _ptr(work), work_bytes,
+                            _stream(stream))
+
+
+def splitkv_bwd(prob, plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE, dO, dQ, dKc, dVc, dKd, dVd, work,
+                work_bytes: int, stream=None) -> int:
+    return _lib.splitkv_bwd(ctypes.byref(prob), _ptr(plan_ws), _ptr(Q), _ptr(Kc), _ptr(Vc),
+                            _ptr(Kd), _ptr(Vd), _ptr(O), _ptr(LSE), _ptr(dO), _ptr(dQ),
+                            _ptr(dKc), _ptr(dVc), _ptr(dKd), _ptr(dVd), _ptr(work),
+                            work_bytes, _stream(stream))
+
+
+def splitkv_plan_stats(prob, plan_ws, stream=None):
+    out = splitkv_stats()
+    st = _lib.splitkv_plan_stats(ctypes.byref(prob), _ptr(plan_ws), ctypes.byref(out),
+                                 _stream(stream))
+    return st, out
+
+
+def splitkv_device_status(prob, plan_ws, stream=None):
+    s = ctypes.c_int(0)
+    st = _lib.splitkv_device_status(ctypes.byref(prob), _ptr(plan_ws), ctypes.byref(s),
+                                    _stream(stream))
+    return st, s.value
+
+
+def splitkv_plan_export(prob, plan_ws, kind: int, capacity: int, stream=None):
+    """Returns (status, ids, costs, worker, pos) as numpy arrays."""
+    import numpy as np
+    ids = np.zeros(max(capacity, 1), np.int64)
+    costs = np.zeros(max(capacity, 1), np.int64)
+    worker = np.zeros(max(capacity, 1), np.int32)
+    pos = np.zeros(max(capacity, 1), np.int32)
+    count = ctypes.c_int64(0)
+    st = _lib.splitkv_plan_export(ctypes.byref(prob), _ptr(plan_ws), int(kind),
+                                  ids.ctypes.data, costs.ctypes.data, worker.ctypes.data,
+                                  pos.ctypes.data, capacity, ctypes.byref(count),
+                                  _stream(stream))
+    n = min(count.value, capacity)
+    return st, ids[:n], costs[:n], worker[:n], pos[:n]
+
+
+# ---- convenience wrapper over torch tensors --------------------------------
+class SplitKV:
+    """One problem (metadata resident on the device) plus its workspaces.
+
+    cu_ctx / cu_anchor / anchors: int32 CUDA tensors; the host scalars are
+    taken from the caller (no device read). Allocates the two workspaces with
+    torch once; ``plan()``, ``forward()`` and ``backward()`` then only enqueue
+    kernels on the current torch stream.
+    """
+
+    def __init__(self, cu_ctx, cu_anchor, anchors, total_ctx: int, total_anchors: int,
+                 max_ctx: int, B: int, Hq: int, Hkv: int, d: int, chunk: int,
+                 scale: float, dtype: int = SPLITKV_BF16, num_workers: int = 0,
+                 flags: int = 0):
+        import torch
+        self._keep = (cu_ctx, cu_anchor, anchors)
+        self.prob = splitkv_problem(
+            num_samples=int(cu_ctx.numel() - 1), cu_ctx=_ptr(cu_ctx), cu_anchor=_ptr(cu_anchor),
+            anchors=_ptr(anchors) if anchors.numel() else None, total_ctx=int(total_ctx),
+            total_anchors=int(total_anchors), max_ctx=int(max_ctx), B=B, Hq=Hq, Hkv=Hkv, d=d,
+            chunk=chunk, scale=float(scale), dtype=dtype, num_workers=num_workers, flags=flags)
+        st, self.plan_bytes, self.work_bytes = splitkv_workspace_size(self.prob)
+        _check("splitkv_workspace_size", st)
+        dev = cu_ctx.device
+        self.plan_ws = torch.empty(self.plan_bytes, dtype=torch.uint8, device=dev)
+        self.work = torch.empty(self.work_bytes, dtype=torch.uint8, device=dev)
+
+    def _stream(self):
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+
+    def plan(self) -> None:
+        _check("splitkv_plan", splitkv_plan(self.prob, self.plan_ws, self.plan_bytes,
+                                            self._stream()))
+
+    def forward(self, Q, Kc, Vc, Kd, Vd, O, LSE) -> None:
+        _check("splitkv_fwd", splitkv_fwd(self.prob, self.plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE,
+                                          self.work, self.work_bytes, self._stream()))
+
+    def backward(self, Q, Kc, Vc, Kd, Vd, O, LSE, dO, dQ, dKc, dVc, dKd, dVd) -> None:
+        _check("splitkv_bwd", splitkv_bwd(self.prob, self.plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE,
+                                          dO, dQ, dKc, dVc, dKd, dVd, self.work,
+                                          self.work_bytes, self._stream()))
+
+    def stats(self) -> splitkv_stats:
+        st, out = splitkv_plan_stats(self.prob, self.plan_ws, self._stream())
+        _check("splitkv_plan_stats", st)
+        return out
+
+    def device_status(self) -> int:
+        st, s = splitkv_device_status(self.prob, self.plan_ws, self._stream())
+        _check("splitkv_device_status", st)
+        return s

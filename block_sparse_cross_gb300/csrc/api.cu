@@ -1,0 +1,366 @@
+// C ABI of the library: argument validation, workspace carving and the
+// launch sequence of each pass. See include/splitkv.h for the contract.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "kernels.h"
+
+using namespace skv;
+
+namespace {
+
+constexpr int kKnownFlags = SPLITKV_FLAG_CUDA_CORE | SPLITKV_FLAG_CONTIGUOUS;
+
+int check_problem(const splitkv_problem* p) {
+  if (!p) return SPLITKV_EINVAL;
+  if (p->num_samples < 1 || !p->cu_ctx || !p->cu_anchor) return SPLITKV_EINVAL;
+  if (p->total_anchors > 0 && !p->anchors) return SPLITKV_EINVAL;
+  if (p->total_ctx < 0 || p->total_anchors < 0 || p->max_ctx < 0) return SPLITKV_EINVAL;
+  if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->chunk < 1 || p->num_workers < 0)
+    return SPLITKV_EINVAL;
+  if (!(p->scale > 0.f) || !isfinite(p->scale)) return SPLITKV_EINVAL;
+  if (p->flags & ~kKnownFlags) return SPLITKV_EINVAL;
+  if (p->Hq % p->Hkv) return SPLITKV_EUNSUPPORTED;
+  const int group = p->Hq / p->Hkv;
+  if ((int64_t)p->B * group > kRows || kRows % (p->B * group)) return SPLITKV_EUNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return SPLITKV_EUNSUPPORTED;
+  if (p->chunk % kKeyTile) return SPLITKV_EUNSUPPORTED;
+  if (p->dtype != SPLITKV_BF16 && p->dtype != SPLITKV_FP32) return SPLITKV_EUNSUPPORTED;
+  // int32 indexing of rows, keys and anchors on the device
+  if (p->total_ctx >= (1LL << 31) - kKeyTile || p->total_anchors * p->B >= (1LL << 31) ||
+      p->max_ctx >= (1 << 30))
+    return SPLITKV_EUNSUPPORTED;
+  if (p->num_workers > 0) {
+    if (p->num_workers % p->Hkv || p->num_workers > kMaxWorkers ||
+        p->num_workers / p->Hkv > 32 * kMaxGroupsPerLane)
+      return SPLITKV_EUNSUPPORTED;
+  }
+  return SPLITKV_OK;
+}
+
+int resolve_workers(const splitkv_problem* p, int* m) {
+  if (p->num_workers > 0) {
+    *m = p->num_workers;
+    return SPLITKV_OK;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPLITKV_EDEVICE;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPLITKV_EDEVICE;
+  int w = sms / p->Hkv * p->Hkv;
+  if (w < p->Hkv) w = p->Hkv;
+  const int cap = std::min(kMaxWorkers, 32 * kMaxGroupsPerLane * p->Hkv) / p->Hkv * p->Hkv;
+  *m = std::min(w, cap);
+  return SPLITKV_OK;
+}
+
+PlanCaps caps_of(const splitkv_problem* p, int m) {
+  PlanCaps c;
+  const int64_t group = p->Hq / p->Hkv;
+  const int64_t bps = kRows / (p->B * group);
+  c.S = p->num_samples;
+  c.NA = p->total_anchors;
+  c.NSL = p->total_anchors == 0 ? 0
+                                : std::min<int64_t>(p->total_anchors,
+                                                    (p->total_anchors + bps - 1) / bps + c.S);
+  const int64_t nch = ((int64_t)p->max_ctx + p->chunk - 1) / p->chunk;
+  c.NCF = nch * c.NSL;
+  c.NCB = (p->total_ctx + kKeyTile - 1) / kKeyTile + c.S;
+  c.M = m;
+  c.Hkv = p->Hkv;
+  return c;
+}
+
+uint64_t problem_hash(const splitkv_problem* p, int m) {
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&](int64_t v) {
+    for (int i = 0; i < 8; ++i) {
+      h ^= (uint64_t)((v >> (8 * i)) & 0xff);
+      h *= 1099511628211ull;
+    }
+  };
+  uint32_t sbits;
+  memcpy(&sbits, &p->scale, 4);
+  mix(p->num_samples); mix(p->total_ctx); mix(p->total_anchors); mix(p->max_ctx);
+  mix(p->B); mix(p->Hq); mix(p->Hkv); mix(p->d); mix(p->chunk); mix(p->dtype);
+  mix(m); mix(p->flags & SPLITKV_FLAG_CONTIGUOUS); mix(sbits);
+  return h;
+}
+
+ProbDev make_dev(const splitkv_problem* p, int m) {
+  ProbDev P;
+  P.S = p->num_samples;
+  P.B = p->B;
+  P.Hq = p->Hq;
+  P.Hkv = p->Hkv;
+  P.group = p->Hq / p->Hkv;
+  P.d = p->d;
+  P.chunk = p->chunk;
+  P.bps = kRows / (p->B * P.group);
+  P.workers = m;
+  P.flags = p->flags;
+  P.dtype = p->dtype;
+  P.T = p->total_ctx;
+  P.NA = p->total_anchors;
+  P.NQ = p->total_anchors * p->B;
+  P.max_ctx = p->max_ctx;
+  P.scale = p->scale;
+  P.scale_log2 = p->scale * 1.4426950408889634f;
+  P.hash = problem_hash(p, m);
+  P.cu_ctx = p->cu_ctx;
+  P.cu_anchor = p->cu_anchor;
+  P.anchors = p->anchors;
+  return P;
+}
+
+size_t plan_bytes_for(const splitkv_problem* p) {
+  // sized for the largest worker count so that the size needs no device query
+  return plan_layout(caps_of(p, kMaxWorkers), nullptr, nullptr);
+}
+
+size_t work_bytes_for(const splitkv_problem* p) {
+  const PlanCaps c = caps_of(p, kMaxWorkers);
+  return work_layout(c.NCF * p->Hkv, p->total_anchors * p->B, p->Hq, p->d, nullptr, nullptr);
+}
+
+struct Ctx {
+  ProbDev P;
+  PlanCaps caps;
+  PlanPtrs pp;
+};
+
+int setup(const splitkv_problem* p, const void* plan_ws, Ctx* c) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!plan_ws) return SPLITKV_EINVAL;
+  int m = 0;
+  st = resolve_workers(p, &m);
+  if (st) return st;
+  c->P = make_dev(p, m);
+  c->caps = caps_of(p, kMaxWorkers);
+  c->caps.M = kMaxWorkers;
+  plan_layout(c->caps, (char*)plan_ws, &c->pp);
+  return SPLITKV_OK;
+}
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPLITKV_OK : SPLITKV_ECUDA; }
+
+bool use_tensor_cores(const ProbDev& P) {
+  return P.dtype == SPLITKV_BF16 && !(P.flags & SPLITKV_FLAG_CUDA_CORE);
+}
+
+}  // namespace
+
+extern "C" {
+
+int splitkv_workspace_size(const splitkv_problem* prob, size_t* plan_bytes, size_t* work_bytes) {
+  const int st = check_problem(prob);
+  if (st) return st;
+  if (!plan_bytes || !work_bytes) return SPLITKV_EINVAL;
+  *plan_bytes = plan_bytes_for(prob);
+  *work_bytes = work_bytes_for(prob);
+  return SPLITKV_OK;
+}
+
+int splitkv_resolve_workers(const splitkv_problem* prob, int* workers) {
+  const int st = check_problem(prob);
+  if (st) return st;
+  if (!workers) return SPLITKV_EINVAL;
+  return resolve_workers(prob, workers);
+}
+
+int splitkv_plan(const splitkv_problem* prob, void* plan_ws, size_t plan_bytes,
+                 splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  if (plan_bytes < plan_bytes_for(prob)) return SPLITKV_EWORKSPACE;
+  return cuda_status(launch_plan(c.P, c.pp, c.caps, (cudaStream_t)stream));
+}
+
+int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q, const void* Kc,
+                const void* Vc, const void* Kd, const void* Vd, void* O, float* LSE, void* work,
+                size_t work_bytes, splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  const bool any_q = prob->total_anchors > 0;
+  if (any_q && (!Q || !Kd || !Vd || !O || !LSE || !work)) return SPLITKV_EINVAL;
+  if (prob->total_ctx > 0 && (!Kc || !Vc)) return SPLITKV_EINVAL;
+  const void* ptrs[] = {Q, Kc, Vc, Kd, Vd, O, LSE, work};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return SPLITKV_EINVAL;
+  if (work_bytes < work_bytes_for(prob)) return SPLITKV_EWORKSPACE;
+  if (!any_q) return SPLITKV_OK;
+  WorkPtrs wk;
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = use_tensor_cores(c.P) ? launch_fwd_tc(c.P, c.pp, wk, Q, Kc, Vc, s)
+                                        : launch_fwd_simt(c.P, c.pp, wk, Q, Kc, Vc, s);
+  if (e != cudaSuccess) return SPLITKV_ECUDA;
+  return cuda_status(launch_merge(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, s));
+}
+
+int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q, const void* Kc,
+                const void* Vc, const void* Kd, const void* Vd, const void* O, const float* LSE,
+                const void* dO, void* dQ, void* dKc, void* dVc, void* dKd, void* dVd, void* work,
+                size_t work_bytes, splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  const bool any_q = prob->total_anchors > 0;
+  if (any_q && (!Q || !Kd || !Vd || !O || !LSE || !dO || !dQ || !dKd || !dVd || !work))
+    return SPLITKV_EINVAL;
+  if (prob->total_ctx > 0 && (!Kc || !Vc || !dKc || !dVc)) return SPLITKV_EINVAL;
+  const void* ptrs[] = {Q, Kc, Vc, Kd, Vd, O, LSE, dO, dQ, dKc, dVc, dKd, dVd, work};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return SPLITKV_EINVAL;
+  if (work_bytes < work_bytes_for(prob)) return SPLITKV_EWORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  if (prob->total_ctx > 0) {
+    e = launch_zero_uncovered(c.P, c.pp, dKc, dVc, s);
+    if (e != cudaSuccess) return SPLITKV_ECUDA;
+  }
+  if (!any_q) return SPLITKV_OK;
+  WorkPtrs wk;
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
+  e = launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, s);
+  if (e != cudaSuccess) return SPLITKV_ECUDA;
+  const bool tc = use_tensor_cores(c.P);
+  e = tc ? launch_bwd_dq_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s)
+         : launch_bwd_dq_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s);
+  if (e != cudaSuccess) return SPLITKV_ECUDA;
+  if (prob->total_ctx > 0) {
+    e = tc ? launch_bwd_dkdv_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s)
+           : launch_bwd_dkdv_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s);
+    if (e != cudaSuccess) return SPLITKV_ECUDA;
+  }
+  return cuda_status(launch_dq_reduce(c.P, c.pp, wk, dQ, s));
+}
+
+int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int* status,
+                          splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  if (!status) return SPLITKV_EINVAL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
+  PlanHeader h;
+  if (cudaMemcpy(&h, c.pp.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPLITKV_ECUDA;
+  *status = h.magic == kPlanMagic ? h.status : SPLITKV_EPLAN;
+  return SPLITKV_OK;
+}
+
+int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv_stats* out,
+                       splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  if (!out) return SPLITKV_EINVAL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
+  PlanHeader h;
+  if (cudaMemcpy(&h, c.pp.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPLITKV_ECUDA;
+  memset(out, 0, sizeof(*out));
+  out->device_status = h.magic == kPlanMagic ? h.status : SPLITKV_EPLAN;
+  out->workers = c.P.workers;
+  if (out->device_status != SPLITKV_OK) return SPLITKV_OK;
+  const int m = c.P.workers;
+  std::vector<int64_t> buf(m);
+  auto stats = [&](const int64_t* dev, int64_t* mx, double* imb) -> int {
+    if (cudaMemcpy(buf.data(), dev, 8 * m, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return SPLITKV_ECUDA;
+    int64_t s = 0, x = 0;
+    for (int64_t v : buf) {
+      s += v;
+      x = std::max(x, v);
+    }
+    *mx = x;
+    *imb = s > 0 ? (double)x / ((double)s / m) - 1.0 : 0.0;
+    return SPLITKV_OK;
+  };
+  if ((st = stats(c.pp.f_load_lpt, &out->fwd_lpt_max_load, &out->fwd_lpt_imbalance))) return st;
+  if ((st = stats(c.pp.f_load_contig, &out->fwd_contig_max_load, &out->fwd_contig_imbalance)))
+    return st;
+  if ((st = stats(c.pp.b_load_lpt, &out->bwd_lpt_max_load, &out->bwd_lpt_imbalance))) return st;
+  if ((st = stats(c.pp.b_load_contig, &out->bwd_contig_max_load, &out->bwd_contig_imbalance)))
+    return st;
+  const int64_t Hkv = prob->Hkv;
+  out->fwd_items = (int64_t)h.n_fwd_items * Hkv;
+  out->bwd_items = (int64_t)h.n_bwd_items * Hkv;
+  out->fwd_slots = (int64_t)h.n_slot_base * Hkv;
+  out->fwd_total_cost = h.fwd_total_cost * Hkv;
+  out->bwd_total_cost = h.bwd_total_cost * Hkv;
+  out->fwd_tiles = h.fwd_tiles * Hkv;
+  out->dense_tiles = h.dense_tiles * Hkv;
+  out->work_bytes_used =
+      work_layout(out->fwd_slots, c.P.NQ, prob->Hq, prob->d, nullptr, nullptr);
+  return SPLITKV_OK;
+}
+
+int splitkv_plan_export(const splitkv_problem* prob, const void* plan_ws, int kind, int64_t* ids,
+                        int64_t* costs, int32_t* worker, int32_t* pos, int64_t capacity,
+                        int64_t* count, splitkv_stream stream) {
+  Ctx c;
+  int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  if ((kind != 0 && kind != 1) || !count || capacity < 0) return SPLITKV_EINVAL;
+  if (capacity > 0 && (!ids || !costs || !worker || !pos)) return SPLITKV_EINVAL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
+  PlanHeader h;
+  if (cudaMemcpy(&h, c.pp.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPLITKV_ECUDA;
+  if (h.magic != kPlanMagic || h.status != SPLITKV_OK) return SPLITKV_EINVAL;
+  const int n = kind == 0 ? h.n_fwd_items : h.n_bwd_items;
+  const int Hkv = prob->Hkv;
+  *count = (int64_t)n * Hkv;
+  if (n == 0) return SPLITKV_OK;
+  std::vector<int32_t> sorted(n), item(n), grp(n), ps(n);
+  std::vector<int64_t> sc(n);
+  const bool f = kind == 0;
+  cudaError_t e = cudaSuccess;
+  e = e ? e : cudaMemcpy(sorted.data(), f ? c.pp.f_sorted : c.pp.b_sorted, 4 * n, cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(item.data(), f ? c.pp.f_item : c.pp.b_item, 4 * n, cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(grp.data(), f ? c.pp.f_grp : c.pp.b_grp, 4 * n, cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(ps.data(), f ? c.pp.f_pos : c.pp.b_pos, 4 * n, cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(sc.data(), f ? c.pp.f_scost : c.pp.b_scost, 8 * n, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return SPLITKV_ECUDA;
+  int64_t k = 0;
+  for (int r = 0; r < n; ++r) {
+    const int64_t cand = item[sorted[r]];
+    for (int g = 0; g < Hkv; ++g, ++k) {
+      if (k >= capacity) return SPLITKV_OK;
+      ids[k] = cand * Hkv + g;
+      costs[k] = sc[r];
+      worker[k] = grp[r] * Hkv + g;
+      pos[k] = ps[r];
+    }
+  }
+  return SPLITKV_OK;
+}
+
+const char* splitkv_status_string(int status) {
+  switch (status) {
+    case SPLITKV_OK: return "ok";
+    case SPLITKV_EINVAL: return "invalid argument";
+    case SPLITKV_EUNSUPPORTED: return "unsupported shape or dtype";
+    case SPLITKV_EWORKSPACE: return "workspace too small";
+    case SPLITKV_ECUDA: return "CUDA runtime error";
+    case SPLITKV_EDEVICE: return "no usable device";
+    case SPLITKV_ETIMEOUT: return "device pipeline wait timed out";
+    case SPLITKV_EPLAN: return "plan does not match the problem";
+    case SPLITKV_EMETA: return "inconsistent cu_ctx / cu_anchor / anchors";
+    case SPLITKV_ECAPACITY: return "metadata exceeds the declared sizes";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

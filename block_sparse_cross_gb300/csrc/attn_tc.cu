@@ -1,0 +1,973 @@
+// Tensor-core (tcgen05 / TMEM / TMA) attention kernels of the split, bf16
+// inputs, fp32 accumulation. Same items and partial layout as the CUDA-core
+// kernels (attn_simt.cu):
+//
+//  fwd    item (sample, chunk, slab, kv head) = 128 (query, head) rows x the
+//         chunk's visible keys. Per 128-key tile: S = Q K^T (SS MMA into
+//         TMEM), online softmax in registers, P (bf16) written back over S,
+//         O += P V (TS MMA, A from TMEM). Emits the chunk partial
+//         (lse_c, O_c / l_c) of every row: the local part of attention that
+//         the rit.work article on Split-KV (section "Split-KV двигает
+//         запросы, а не ключи и значения") assigns to each KV shard.
+//  dq     same items: S = Q K^T, dP = dO V^T, dS = P (dP - D) with
+//         P = exp(S*scale - LSE), dQ_c += dS K (TS MMA). Emits the fp32 dQ
+//         partial of the chunk (the query gradient that moves).
+//  dkdv   item (sample, 128-key tile, kv head): the tile stays put (local
+//         K/V gradients) while every slab of rows that sees it streams by:
+//         S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q.
+//
+// Warp roles (192 threads): warp 0 issues TMA (one elected lane), warp 1
+// allocates TMEM and issues every MMA (one lane), warps 2..5 own TMEM lane
+// quadrants (warp % 4) and do the softmax and the epilogue, one row (fwd/dq)
+// or one key (dkdv) per thread. All waits are bounded (tc_common.cuh); on a
+// timeout the CTA winds down, drains its copies and MMAs, frees TMEM and
+// latches SPLITKV_ETIMEOUT.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace skv {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kNS = 2;               // pipeline stages
+constexpr int kThreads = 192;
+constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainNs = 100000000ull;
+
+struct FwdItem {
+  int n0, g, row0, cs, ntiles, first, nblk;
+  size_t slot;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
+  FwdItem I;
+  I.first = pp.sl_first[e.slab];
+  I.nblk = pp.sl_nblk[e.slab];
+  const int c0 = P.cu_ctx[e.s], L = P.cu_ctx[e.s + 1] - c0;
+  const int amax = P.anchors[I.first + I.nblk - 1];
+  I.cs = e.c * P.chunk;
+  const int ke = min(min(I.cs + P.chunk, L), amax);
+  I.ntiles = (ke - I.cs + kKeyTile - 1) / kKeyTile;
+  I.row0 = c0 + I.cs;
+  I.n0 = I.first * P.B;
+  I.g = e.g;
+  I.slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
+  return I;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool mine = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, mine);
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// ===========================================================================
+// Forward
+// ===========================================================================
+template <int D>
+struct FwdLayout {
+  static constexpr int kSub = D / 64;
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t stage0 = kSub * kSubBytes;
+  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes;  // K then V
+  static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
+  static constexpr uint32_t total = bars + 512 + 1024;  // + alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, ProbDev P, PlanPtrs pp, WorkPtrs wk) {
+  using Lay = FwdLayout<D>;
+  constexpr int kSub = Lay::kSub;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = (uint64_t*)(smem + Lay::bars);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + kNS;
+  uint64_t* kv_empty = v_full + kNS;
+  uint64_t* s_full = kv_empty + kNS;  // [2]
+  uint64_t* p_ready = s_full + 2;     // [2]
+  uint64_t* pv_done = p_ready + 2;
+  uint64_t* o_free = pv_done + 1;
+  uint64_t* mma_drain = o_free + 1;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 32);
+  volatile int* abort_flag = (volatile int*)(bars + 33);
+
+  if (!plan_ok_cta(P, pp.hdr)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_ready + b, 4);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(o_free, 4);
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 256;
+  const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t nq = 0, nkv = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(q_full, kSub * kSubBytes);
+        for (int i = 0; i < kSub; ++i)
+          tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+        ++nq;
+        for (int t = 0; t < I.ntiles; ++t) {
+          const uint32_t s = nkv % kNS, u = nkv / kNS;
+          if (u > 0 && !(ok = mbar_wait(kv_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* kb = smem + Lay::stage0 + s * Lay::stage_bytes;
+          uint8_t* vb = kb + kSub * kSubBytes;
+          const int row = I.row0 + t * kKeyTile;
+          mbar_expect_tx(k_full + s, kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, row);
+          mbar_expect_tx(v_full + s, kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, row);
+          ++nkv;
+        }
+      }
+      if (!ok) {  // let every copy in flight land before the CTA exits
+        if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, kDrainNs);
+        for (uint32_t j = nkv > (uint32_t)kNS ? nkv - kNS : 0; j < nkv; ++j) {
+          mbar_wait_drain(k_full + j % kNS, (j / kNS) & 1, kDrainNs);
+          mbar_wait_drain(v_full + j % kNS, (j / kNS) & 1, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr = smem_u32(smem + Lay::q);
+      uint32_t nkv = 0, ns = 0, nit = 0;
+      bool ok = true;
+      bool pend = false, pend_first = false;
+      uint32_t pend_s = 0, pend_stage = 0, pend_par = 0, pend_item = 0;
+      auto issue_pv = [&]() -> bool {
+        const uint32_t sb = pend_s & 1;
+        if (!mbar_wait(p_ready + sb, (pend_s >> 1) & 1, abort_flag)) return false;
+        if (pend_first && pend_item > 0 && !mbar_wait(o_free, (pend_item - 1) & 1, abort_flag))
+          return false;
+        if (!mbar_wait(v_full + pend_stage, pend_par, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t v_addr =
+            smem_u32(smem + Lay::stage0 + pend_stage * Lay::stage_bytes + kSub * kSubBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_ts(tO, tS + sb * 128 + kk * 8, desc_mnmajor(v_addr, kk), kIdPV,
+                 (pend_first && kk == 0) ? 0u : 1u);
+        mma_commit(kv_empty + pend_stage);
+        mma_commit(pv_done);
+        return true;
+      };
+      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int t = 0; t < I.ntiles; ++t, ++nkv, ++ns) {
+          const uint32_t s = nkv % kNS, par = (nkv / kNS) & 1;
+          if (!(ok = mbar_wait(k_full + s, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
+          const uint32_t sb = ns & 1;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS + sb * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(s_full + sb);
+          if (t == I.ntiles - 1) mma_commit(q_empty);
+          if (pend && !(ok = issue_pv())) break;
+          pend = true;
+          pend_s = ns;
+          pend_stage = s;
+          pend_par = par;
+          pend_first = (t == 0);
+          pend_item = nit;
+        }
+      }
+      if (ok && pend) ok = issue_pv();
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0, kDrainNs);
+    }
+  } else {
+    // ---------------- softmax + epilogue (warps 2..5) ----------------
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float sl2 = P.scale_log2;
+    uint32_t ns = 0, npv = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
+      float m_run = -INFINITY, l = 0.f;
+      for (int t = 0; t < I.ntiles; ++t, ++ns) {
+        const uint32_t sb = ns & 1;
+        if (!(ok = warp_wait(s_full + sb, (ns >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const int lim = min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
+        const uint32_t sa = tS + lane_base + sb * 128;
+        float x[128];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+          tmem_ld32(sa + 32 * j, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float xv = (32 * j + i < lim) ? __uint_as_float(v[i]) * sl2 : -INFINITY;
+            x[32 * j + i] = xv;
+            mt = fmaxf(mt, xv);
+          }
+        }
+        const float m_new = fmaxf(m_run, mt);
+        float fac = 1.f;
+        bool resc = false;
+        if (t == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + 8.f) {  // lazy rescale: keep exponents <= 2^8
+          fac = ex2(m_run - m_new);
+          resc = true;
+          m_run = m_new;
+        }
+        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        float ls = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = ex2(x[2 * i] - mu), p1 = ex2(x[2 * i + 1] - mu);
+          ls += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
+        l = (t == 0) ? ls : l * fac + ls;
+        tmem_st32(sa, *(const uint32_t(*)[32])(pk));
+        tmem_st32(sa + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st_wait();
+        if (t > 0) {
+          if (!(ok = warp_wait(pv_done, npv & 1, abort_flag))) break;
+          ++npv;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+              uint32_t v[32];
+              tmem_ld32(tO + lane_base + 32 * j, v);
+              tmem_ld_wait(v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac);
+              tmem_st32(tO + lane_base + 32 * j, v);
+            }
+            tmem_st_wait();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready + sb);
+      }
+      if (!ok) break;
+      if (!(ok = warp_wait(pv_done, npv & 1, abort_flag))) break;
+      ++npv;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* po = wk.part_o + (I.slot * kRows + r) * D;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld32(tO + lane_base + 32 * j, v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *(float4*)(po + 32 * j + i) =
+              make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                          __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+      }
+      wk.part_lse[I.slot * kRows + r] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+}
+
+// ===========================================================================
+// dQ (same items as the forward)
+// ===========================================================================
+template <int D>
+struct DqLayout {
+  static constexpr int kSub = D / 64;
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t dO = kSub * kSubBytes;
+  static constexpr uint32_t stage0 = 2 * kSub * kSubBytes;
+  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes;  // K then V
+  static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
+  static constexpr uint32_t total = bars + 512 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     ProbDev P, PlanPtrs pp, WorkPtrs wk, const float* __restrict__ LSE) {
+  using Lay = DqLayout<D>;
+  constexpr int kSub = Lay::kSub;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = (uint64_t*)(smem + Lay::bars);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + kNS;
+  uint64_t* kv_empty = v_full + kNS;
+  uint64_t* dp_full = kv_empty + kNS;
+  uint64_t* p_ready = dp_full + 1;
+  uint64_t* dq_done = p_ready + 1;
+  uint64_t* dq_free = dq_done + 1;
+  uint64_t* mma_drain = dq_free + 1;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 32);
+  volatile int* abort_flag = (volatile int*)(bars + 33);
+
+  if (!plan_ok_cta(P, pp.hdr)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(dq_done, 1);
+    mbar_init(dq_free, 4);
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tdQ = tmem + 384;  // regions 0..2 (128 cols each) rotate S / dP
+  const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t nq = 0, nkv = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(q_full, 2 * kSub * kSubBytes);
+        for (int i = 0; i < kSub; ++i) {
+          tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+          tma_load_3d(smem + Lay::dO + i * kSubBytes, &tmdO, q_full, 64 * i, I.g * P.group, I.n0);
+        }
+        ++nq;
+        for (int t = 0; t < I.ntiles; ++t) {
+          const uint32_t s = nkv % kNS, u = nkv / kNS;
+          if (u > 0 && !(ok = mbar_wait(kv_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* kb = smem + Lay::stage0 + s * Lay::stage_bytes;
+          uint8_t* vb = kb + kSub * kSubBytes;
+          const int row = I.row0 + t * kKeyTile;
+          mbar_expect_tx(k_full + s, kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, row);
+          mbar_expect_tx(v_full + s, kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, row);
+          ++nkv;
+        }
+      }
+      if (!ok) {
+        if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, kDrainNs);
+        for (uint32_t j = nkv > (uint32_t)kNS ? nkv - kNS : 0; j < nkv; ++j) {
+          mbar_wait_drain(k_full + j % kNS, (j / kNS) & 1, kDrainNs);
+          mbar_wait_drain(v_full + j % kNS, (j / kNS) & 1, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr = smem_u32(smem + Lay::q);
+      const uint32_t do_addr = smem_u32(smem + Lay::dO);
+      uint32_t nkv = 0, gt = 0, nit = 0;
+      bool ok = true;
+      bool pend = false, pend_first = false, pend_last = false;
+      uint32_t pend_t = 0, pend_stage = 0, pend_item = 0;
+      auto issue_dq = [&]() -> bool {
+        if (!mbar_wait(p_ready, pend_t & 1, abort_flag)) return false;
+        if (pend_first && pend_item > 0 && !mbar_wait(dq_free, (pend_item - 1) & 1, abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t rS = (2 * pend_t) % 3;
+        const uint32_t k_addr = smem_u32(smem + Lay::stage0 + pend_stage * Lay::stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_ts(tdQ, tmem + rS * 128 + kk * 8, desc_mnmajor(k_addr, kk), kIdQ,
+                 (pend_first && kk == 0) ? 0u : 1u);
+        mma_commit(kv_empty + pend_stage);
+        if (pend_last) mma_commit(dq_done);
+        return true;
+      };
+      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int t = 0; t < I.ntiles; ++t, ++nkv, ++gt) {
+          const uint32_t s = nkv % kNS, par = (nkv / kNS) & 1;
+          if (!(ok = mbar_wait(k_full + s, par, abort_flag))) break;
+          if (!(ok = mbar_wait(v_full + s, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
+          const uint32_t v_addr = k_addr + kSub * kSubBytes;
+          const uint32_t rS = (2 * gt) % 3, rP = (2 * gt + 1) % 3;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + rS * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
+                   kk > 0 ? 1u : 0u);
+          if (pend && !(ok = issue_dq())) break;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + rP * 128, desc_kmajor(do_addr, kk), desc_kmajor(v_addr, kk), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(dp_full);
+          if (t == I.ntiles - 1) mma_commit(q_empty);
+          pend = true;
+          pend_t = gt;
+          pend_stage = s;
+          pend_first = (t == 0);
+          pend_last = (t == I.ntiles - 1);
+          pend_item = nit;
+        }
+      }
+      if (ok && pend) ok = issue_dq();
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0, kDrainNs);
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float sl2 = P.scale_log2;
+    uint32_t gt = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
+      float lse2 = 0.f, Dr = 0.f;
+      if (ri.n >= 0) {
+        lse2 = LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
+        Dr = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
+      }
+      for (int t = 0; t < I.ntiles; ++t, ++gt) {
+        if (!(ok = warp_wait(dp_full, gt & 1, abort_flag))) break;
+        tc_fence_after();
+        const int lim = min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
+        const uint32_t sa = tmem + lane_base + ((2 * gt) % 3) * 128;
+        const uint32_t pa = tmem + lane_base + ((2 * gt + 1) % 3) * 128;
+        uint32_t pk[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(sa + 32 * j, sv);
+          tmem_ld_wait(sv);
+          tmem_ld32(pa + 32 * j, dv);
+          tmem_ld_wait(dv);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int c = 32 * j + i;
+            const float p0 = c < lim ? ex2(__uint_as_float(sv[i]) * sl2 - lse2) : 0.f;
+            const float p1 = c + 1 < lim ? ex2(__uint_as_float(sv[i + 1]) * sl2 - lse2) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dv[i]) - Dr);
+            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - Dr);
+            pk[16 * j + i / 2] = pack_bf16(d0, d1);
+          }
+        }
+        tmem_st32(sa, *(const uint32_t(*)[32])(pk));
+        tmem_st32(sa + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+      }
+      if (!ok) break;
+      if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
+      tc_fence_after();
+      float* po = wk.part_o + (I.slot * kRows + r) * D;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld32(tdQ + lane_base + 32 * j, v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *(float4*)(po + 32 * j + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                    __uint_as_float(v[i + 2]),
+                                                    __uint_as_float(v[i + 3]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+}
+
+// ===========================================================================
+// dK / dV (backward items: one 128-key tile, all slabs that see it)
+// ===========================================================================
+template <int D>
+struct KvLayout {
+  static constexpr int kSub = D / 64;
+  static constexpr uint32_t k = 0;
+  static constexpr uint32_t v = kSub * kSubBytes;
+  static constexpr uint32_t stage0 = 2 * kSub * kSubBytes;
+  static constexpr uint32_t info_off = 2 * kSub * kSubBytes;       // inside a stage
+  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes + 2048;  // Q, dO, row info
+  static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
+  static constexpr uint32_t total = bars + 512 + 1024;
+};
+
+struct KvItem {
+  int s, g, c0, L, ks0, sl_lo, sl_hi;
+};
+
+__device__ __forceinline__ KvItem kv_item(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
+  KvItem I;
+  I.s = e.s;
+  I.g = e.g;
+  I.c0 = P.cu_ctx[e.s];
+  I.L = P.cu_ctx[e.s + 1] - I.c0;
+  I.ks0 = e.c * kKeyTile;
+  const int sl0 = pp.s_slab_off[e.s], sl1 = pp.s_slab_off[e.s + 1];
+  int lo = sl0, hi = sl1;
+  while (lo < hi) {  // first slab whose last anchor exceeds the tile start
+    const int mid = (lo + hi) >> 1;
+    if (P.anchors[pp.sl_first[mid] + pp.sl_nblk[mid] - 1] > I.ks0) hi = mid; else lo = mid + 1;
+  }
+  I.sl_lo = lo;
+  I.sl_hi = sl1;
+  return I;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       ProbDev P, PlanPtrs pp, WorkPtrs wk, const float* __restrict__ LSE,
+                       __nv_bfloat16* __restrict__ dKc, __nv_bfloat16* __restrict__ dVc) {
+  using Lay = KvLayout<D>;
+  constexpr int kSub = Lay::kSub;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = (uint64_t*)(smem + Lay::bars);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* st_full = bars + 2;        // [kNS]
+  uint64_t* st_empty = st_full + kNS;  // [kNS]
+  uint64_t* sp_full = st_empty + kNS;
+  uint64_t* p_ready = sp_full + 1;
+  uint64_t* acc_done = p_ready + 1;
+  uint64_t* acc_free = acc_done + 1;
+  uint64_t* mma_drain = acc_free + 1;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 32);
+  volatile int* abort_flag = (volatile int*)(bars + 33);
+
+  if (!plan_ok_cta(P, pp.hdr)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(st_full + s, 33);  // 32 row-info lanes + the TMA transaction arrive
+      mbar_init(st_empty + s, 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(acc_done, 1);
+    mbar_init(acc_free, 4);
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+  const int q0 = pp.b_qoff[blockIdx.x], q1 = pp.b_qoff[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ---------------- producer: K/V per item, Q/dO/row info per slab --------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    uint32_t nkv = 0, nst = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi) {
+      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+      if (lane == 0) {
+        if (nkv > 0) ok = mbar_wait(kv_empty, (nkv - 1) & 1, abort_flag);
+        if (ok) {
+          mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) {
+            tma_load_3d(smem + Lay::k + i * kSubBytes, &tmK, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+            tma_load_3d(smem + Lay::v + i * kSubBytes, &tmV, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+          }
+          ++nkv;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      nkv = __shfl_sync(0xffffffffu, nkv, 0);
+      if (!ok) break;
+      for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
+        const uint32_t s = nst % kNS, u = nst / kNS;
+        if (u > 0 && !(ok = warp_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
+        uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
+        float* lse2 = (float*)(sb + Lay::info_off);
+        float* dvv = lse2 + kRows;
+        int* anc = (int*)(dvv + kRows);
+        const int first = pp.sl_first[sg], nblk = pp.sl_nblk[sg];
+        for (int rr = lane; rr < kRows; rr += 32) {
+          const RowInfo ri = row_info(P, first, nblk, I.g, rr);
+          float l2 = 0.f, dd = 0.f;
+          if (ri.n >= 0) {
+            l2 = LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
+            dd = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
+          }
+          lse2[rr] = l2;
+          dvv[rr] = dd;
+          anc[rr] = ri.anchor;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(st_full + s, 2 * kSub * kSubBytes);
+          const int n0 = first * P.B;
+          for (int i = 0; i < kSub; ++i) {
+            tma_load_3d(sb + i * kSubBytes, &tmQ, st_full + s, 64 * i, I.g * P.group, n0);
+            tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
+          }
+        }
+        mbar_arrive(st_full + s);
+        ++nst;
+      }
+    }
+    if (!ok && lane == 0) {
+      if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1, kDrainNs);
+      for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
+        mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
+      const uint32_t k_addr = smem_u32(smem + Lay::k);
+      const uint32_t v_addr = smem_u32(smem + Lay::v);
+      uint32_t nst = 0, nit = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+        if (!(ok = mbar_wait(kv_full, nit & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
+          const uint32_t s = nst % kNS;
+          if (!(ok = mbar_wait(st_full + s, (nst / kNS) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t q_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
+          const uint32_t do_addr = q_addr + kSub * kSubBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS, desc_kmajor(k_addr, kk), desc_kmajor(q_addr, kk), kIdS, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tP, desc_kmajor(v_addr, kk), desc_kmajor(do_addr, kk), kIdS, kk > 0 ? 1u : 0u);
+          mma_commit(sp_full);
+          const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
+          if (last) mma_commit(kv_empty);
+          if (!(ok = mbar_wait(p_ready, nst & 1, abort_flag))) break;
+          if (first && nit > 0 && !(ok = mbar_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts(tdV, tS + kk * 8, desc_mnmajor(do_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts(tdK, tP + kk * 8, desc_mnmajor(q_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
+          mma_commit(st_empty + s);
+          if (last) mma_commit(acc_done);
+        }
+      }
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0, kDrainNs);
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key of the tile owned by this thread
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const float sl2 = P.scale_log2;
+    uint32_t nst = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+      const int key = I.ks0 + r;
+      for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
+        const uint32_t s = nst % kNS;
+        // row info of the stage was written by the producer warp: acquire it
+        // through the stage barrier (already complete; it cannot advance before
+        // this slab's p_ready), then wait for S^T / dP^T.
+        if (!(ok = warp_wait(st_full + s, (nst / kNS) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(sp_full, nst & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
+        const float* lse2 = (const float*)(sb + Lay::info_off);
+        const float* dvv = lse2 + kRows;
+        const int* anc = (const int*)(dvv + kRows);
+        uint32_t pkP[64], pkS[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tS + lane_base + 32 * j, sv);
+          tmem_ld_wait(sv);
+          tmem_ld32(tP + lane_base + 32 * j, dv);
+          tmem_ld_wait(dv);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int c = 32 * j + i;
+            const float p0 = key < anc[c] ? ex2(__uint_as_float(sv[i]) * sl2 - lse2[c]) : 0.f;
+            const float p1 =
+                key < anc[c + 1] ? ex2(__uint_as_float(sv[i + 1]) * sl2 - lse2[c + 1]) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dv[i]) - dvv[c]);
+            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - dvv[c + 1]);
+            pkP[16 * j + i / 2] = pack_bf16(p0, p1);
+            pkS[16 * j + i / 2] = pack_bf16(d0, d1);
+          }
+        }
+        tmem_st32(tS + lane_base, *(const uint32_t(*)[32])(pkP));
+        tmem_st32(tS + lane_base + 32, *(const uint32_t(*)[32])(pkP + 32));
+        tmem_st32(tP + lane_base, *(const uint32_t(*)[32])(pkS));
+        tmem_st32(tP + lane_base + 32, *(const uint32_t(*)[32])(pkS + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+      }
+      if (!ok) break;
+      if (!(ok = warp_wait(acc_done, nit & 1, abort_flag))) break;
+      tc_fence_after();
+      const bool valid = key < I.L;
+      const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tdV + lane_base + 32 * j, a);
+        tmem_ld_wait(a);
+        tmem_ld32(tdK + lane_base + 32 * j, b);
+        tmem_ld_wait(b);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 pv, pkk;
+            pv.x = pack_bf16(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+            pv.y = pack_bf16(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3]));
+            pv.z = pack_bf16(__uint_as_float(a[i + 4]), __uint_as_float(a[i + 5]));
+            pv.w = pack_bf16(__uint_as_float(a[i + 6]), __uint_as_float(a[i + 7]));
+            pkk.x = pack_bf16(__uint_as_float(b[i]) * P.scale, __uint_as_float(b[i + 1]) * P.scale);
+            pkk.y = pack_bf16(__uint_as_float(b[i + 2]) * P.scale, __uint_as_float(b[i + 3]) * P.scale);
+            pkk.z = pack_bf16(__uint_as_float(b[i + 4]) * P.scale, __uint_as_float(b[i + 5]) * P.scale);
+            pkk.w = pack_bf16(__uint_as_float(b[i + 6]) * P.scale, __uint_as_float(b[i + 7]) * P.scale);
+            *(uint4*)(dVc + off + 32 * j + i) = pv;
+            *(uint4*)(dKc + off + 32 * j + i) = pkk;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+}
+
+// ===========================================================================
+// Host side: tensor maps and launches
+// ===========================================================================
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// 3-D bf16 map over [n2][n1][n0] (n0 contiguous) with a {64, b1, b2} box.
+cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t n0, uint64_t n1, uint64_t n2,
+                     uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {n0, n1, n2};
+  const cuuint64_t strides[2] = {n0 * 2, n0 * n1 * 2};
+  const cuuint32_t box[3] = {64, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+struct Maps {
+  CUtensorMap q, dO, k, v;
+};
+
+cudaError_t make_maps(const ProbDev& P, const void* Q, const void* dO, const void* Kc,
+                      const void* Vc, Maps* m) {
+  const uint32_t rows_q = (uint32_t)(P.bps * P.B);
+  cudaError_t e = make_map(&m->q, Q, P.d, P.Hq, P.NQ, P.group, rows_q);
+  if (e == cudaSuccess && dO) e = make_map(&m->dO, dO, P.d, P.Hq, P.NQ, P.group, rows_q);
+  if (e == cudaSuccess) e = make_map(&m->k, Kc, P.d, P.Hkv, P.T, 1, kKeyTile);
+  if (e == cudaSuccess) e = make_map(&m->v, Vc, P.d, P.Hkv, P.T, 1, kKeyTile);
+  return e;
+}
+
+template <typename K>
+cudaError_t prep(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                          const void* Q, const void* Kc, const void* Vc, cudaStream_t st) {
+  if (P.T == 0) return cudaErrorInvalidValue;
+  Maps m;
+  cudaError_t e = make_maps(P, Q, nullptr, Kc, Vc, &m);
+  if (e != cudaSuccess) return e;
+  if (P.d == 128) {
+    auto k = fwd_tc_kernel<128>;
+    if ((e = prep(k, FwdLayout<128>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, FwdLayout<128>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+  } else {
+    auto k = fwd_tc_kernel<64>;
+    if ((e = prep(k, FwdLayout<64>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, FwdLayout<64>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                             const void* Q, const void* Kc, const void* Vc, const void* dO,
+                             const float* LSE, cudaStream_t st) {
+  if (P.T == 0) return cudaErrorInvalidValue;
+  Maps m;
+  cudaError_t e = make_maps(P, Q, dO, Kc, Vc, &m);
+  if (e != cudaSuccess) return e;
+  if (P.d == 128) {
+    auto k = bwd_dq_tc_kernel<128>;
+    if ((e = prep(k, DqLayout<128>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, DqLayout<128>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE);
+  } else {
+    auto k = bwd_dq_tc_kernel<64>;
+    if ((e = prep(k, DqLayout<64>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, DqLayout<64>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                               const void* Q, const void* Kc, const void* Vc, const void* dO,
+                               const float* LSE, void* dKc, void* dVc, cudaStream_t st) {
+  Maps m;
+  cudaError_t e = make_maps(P, Q, dO, Kc, Vc, &m);
+  if (e != cudaSuccess) return e;
+  if (P.d == 128) {
+    auto k = bwd_dkdv_tc_kernel<128>;
+    if ((e = prep(k, KvLayout<128>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, KvLayout<128>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
+                                                          (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
+  } else {
+    auto k = bwd_dkdv_tc_kernel<64>;
+    if ((e = prep(k, KvLayout<64>::total)) != cudaSuccess) return e;
+    k<<<P.workers, kThreads, KvLayout<64>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
+                                                         (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,114 @@
+// Small device helpers shared by the kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.h"
+
+namespace skv {
+
+__device__ __forceinline__ void latch(PlanHeader* h, int code) {
+  atomicCAS(&h->status, 0, code);
+}
+
+__device__ __forceinline__ int read_status(const PlanHeader* h) {
+  return *(volatile const int32_t*)&h->status;
+}
+
+// True when the plan is valid and was built for this problem; otherwise
+// latches SPLITKV_EPLAN (mismatch) and the caller skips its work.
+__device__ __forceinline__ bool plan_ok(const ProbDev& P, const PlanHeader* H) {
+  if (read_status(H) != 0) return false;
+  if (H->problem_hash != P.hash || H->magic != kPlanMagic) {
+    if (threadIdx.x == 0) latch(const_cast<PlanHeader*>(H), SPLITKV_EPLAN);
+    return false;
+  }
+  return true;
+}
+
+// CTA-uniform version of plan_ok (one thread reads, all agree).
+__device__ __forceinline__ bool plan_ok_cta(const ProbDev& P, const PlanHeader* H) {
+  __shared__ int ok_flag;
+  if (threadIdx.x == 0) ok_flag = plan_ok(P, H) ? 1 : 0;
+  __syncthreads();
+  return ok_flag != 0;
+}
+
+// Last index s in [0, n) with off[s] <= x (off non-decreasing, off[0] <= x).
+__device__ __forceinline__ int seg_of(const int32_t* off, int n, int64_t x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if ((int64_t)off[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <typename T> __device__ __forceinline__ float ld_f(const T* p);
+template <> __device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T> __device__ __forceinline__ void st_f(T* p, float v);
+template <> __device__ __forceinline__ void st_f<float>(float* p, float v) { *p = v; }
+template <> __device__ __forceinline__ void st_f<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+// Block-wide exclusive scan (blockDim.x a multiple of 32, <= 1024).
+// `ws` is 32 shared slots. Returns the exclusive prefix; *total = block sum.
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* ws, T* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    T w = lane < nw ? ws[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    ws[lane] = w;
+  }
+  __syncthreads();
+  T pre = (wid > 0 ? ws[wid - 1] : T(0)) + x - v;
+  *total = ws[nw - 1];
+  __syncthreads();
+  return pre;
+}
+
+// Sample / slab / row geometry of a forward item's 128 rows.
+// Row r of an item = (draft block b of the slab, query qi in the block,
+// head-in-group hg) with r = (b * B + qi) * group + hg.
+struct RowInfo {
+  int n;        // global query index, or -1 if the row is padding
+  int h;        // query head
+  int anchor;   // anchor of the row's block (0 for padding rows)
+};
+
+__device__ __forceinline__ RowInfo row_info(const ProbDev& P, int first_block, int nblk, int g,
+                                            int r) {
+  RowInfo ri;
+  const int per_blk = P.B * P.group;
+  const int b = r / per_blk;
+  if (b >= nblk) {
+    ri.n = -1; ri.h = 0; ri.anchor = 0;
+    return ri;
+  }
+  const int qi = (r / P.group) % P.B;
+  const int hg = r % P.group;
+  ri.n = (first_block + b) * P.B + qi;
+  ri.h = g * P.group + hg;
+  ri.anchor = P.anchors[first_block + b];
+  return ri;
+}
+
+}  // namespace skv

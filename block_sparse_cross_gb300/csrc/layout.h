@@ -1,0 +1,188 @@
+// Workspace layouts shared by the host API and the kernels.
+//
+// Plan workspace: a header (status word, counts) followed by the per-sample,
+// per-slab, per-item and per-worker arrays the planner fills. Every offset is
+// a pure function of host-known scalars, so the host can rebuild the typed
+// pointers on every call without reading the device.
+//
+// Work workspace: fp32 partials of the split computation.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/splitkv.h"
+
+namespace skv {
+
+constexpr int kRows = 128;      // (query, head) rows per work item / MMA tile
+constexpr int kKeyTile = 128;   // keys per tile; backward items own one tile
+constexpr int kMaxGroupsPerLane = 8;   // LPT kernel: groups <= 32 * 8
+constexpr int kMaxWorkers = 4096;
+constexpr int32_t kPlanMagic = 0x53504b56;  // "SPKV"
+
+struct PlanHeader {
+  int32_t magic;
+  int32_t status;          // latched device status (first error wins)
+  int32_t workers;         // m persistent CTAs
+  int32_t groups;          // m / Hkv
+  int32_t n_slabs;
+  int32_t n_fwd_cand;      // (sample, chunk, slab) candidates
+  int32_t n_fwd_items;     // ... of positive cost
+  int32_t n_slot_base;     // sum over slabs of active chunks (slots / Hkv)
+  int32_t n_bwd_cand;      // (sample, key tile) candidates
+  int32_t n_bwd_items;
+  int32_t flags;
+  int32_t pad0;
+  int64_t fwd_total_cost;  // per kv head
+  int64_t bwd_total_cost;
+  int64_t fwd_tiles;       // per kv head
+  int64_t dense_tiles;     // per kv head
+  uint64_t problem_hash;
+  int64_t pad1[7];
+};
+static_assert(sizeof(PlanHeader) % 16 == 0, "header alignment");
+
+// A queue entry: one item for one worker.
+//   forward : {sample, chunk, global slab index, kv head}
+//   backward: {sample, key tile, unused, kv head}
+struct __align__(16) QEntry {
+  int32_t s, c, slab, g;
+};
+
+struct PlanCaps {
+  int64_t S, NA, NSL, NCF, NCB, M, Hkv;
+};
+
+struct PlanPtrs {
+  PlanHeader* hdr;
+  // per sample [S+1]
+  int32_t* s_nch;
+  int32_t* s_nsl;
+  int32_t* s_nkt;
+  int32_t* s_cand_off;
+  int32_t* s_slab_off;
+  int32_t* s_bcand_off;
+  // per slab [NSL+1]
+  int32_t* sl_sample;
+  int32_t* sl_first;       // first global draft block
+  int32_t* sl_nblk;
+  int32_t* sl_nact;        // active chunks: ceil(max anchor / C)
+  int32_t* sl_slot;        // exclusive prefix of sl_nact
+  // forward candidates / items
+  int64_t* f_cost;         // [NCF]   cost of candidate (0 = inactive)
+  int32_t* f_item;         // [NCF]   candidate id of item i
+  int64_t* f_prefix;       // [NCF+1] prefix of item costs in id order
+  int32_t* f_sorted;       // [NCF]   item at LPT rank r
+  int64_t* f_scost;        // [NCF]   cost of the item at rank r
+  int32_t* f_grp;          // [NCF]   worker group of rank r
+  int32_t* f_pos;          // [NCF]   queue position of rank r
+  int32_t* f_qoff;         // [M+1]
+  QEntry* f_queue;         // [NCF*Hkv]
+  int64_t* f_load_lpt;     // [M]
+  int64_t* f_load_contig;  // [M]
+  // backward
+  int64_t* b_cost;
+  int32_t* b_item;
+  int64_t* b_prefix;
+  int32_t* b_sorted;
+  int64_t* b_scost;
+  int32_t* b_grp;
+  int32_t* b_pos;
+  int32_t* b_qoff;
+  QEntry* b_queue;
+  int64_t* b_load_lpt;
+  int64_t* b_load_contig;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Computes offsets (base == nullptr: sizes only). Returns total bytes.
+inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    off = align_up(off, 256);
+    char* r = base ? base + off : nullptr;
+    off += bytes;
+    return r;
+  };
+  PlanPtrs q;
+  q.hdr = (PlanHeader*)take(sizeof(PlanHeader));
+  q.s_nch = (int32_t*)take(4 * (c.S + 1));
+  q.s_nsl = (int32_t*)take(4 * (c.S + 1));
+  q.s_nkt = (int32_t*)take(4 * (c.S + 1));
+  q.s_cand_off = (int32_t*)take(4 * (c.S + 1));
+  q.s_slab_off = (int32_t*)take(4 * (c.S + 1));
+  q.s_bcand_off = (int32_t*)take(4 * (c.S + 1));
+  q.sl_sample = (int32_t*)take(4 * (c.NSL + 1));
+  q.sl_first = (int32_t*)take(4 * (c.NSL + 1));
+  q.sl_nblk = (int32_t*)take(4 * (c.NSL + 1));
+  q.sl_nact = (int32_t*)take(4 * (c.NSL + 1));
+  q.sl_slot = (int32_t*)take(4 * (c.NSL + 1));
+  q.f_cost = (int64_t*)take(8 * (c.NCF + 1));
+  q.f_item = (int32_t*)take(4 * (c.NCF + 1));
+  q.f_prefix = (int64_t*)take(8 * (c.NCF + 1));
+  q.f_sorted = (int32_t*)take(4 * (c.NCF + 1));
+  q.f_scost = (int64_t*)take(8 * (c.NCF + 1));
+  q.f_grp = (int32_t*)take(4 * (c.NCF + 1));
+  q.f_pos = (int32_t*)take(4 * (c.NCF + 1));
+  q.f_qoff = (int32_t*)take(4 * (c.M + 1));
+  q.f_queue = (QEntry*)take(sizeof(QEntry) * (c.NCF * c.Hkv + 1));
+  q.f_load_lpt = (int64_t*)take(8 * c.M);
+  q.f_load_contig = (int64_t*)take(8 * c.M);
+  q.b_cost = (int64_t*)take(8 * (c.NCB + 1));
+  q.b_item = (int32_t*)take(4 * (c.NCB + 1));
+  q.b_prefix = (int64_t*)take(8 * (c.NCB + 1));
+  q.b_sorted = (int32_t*)take(4 * (c.NCB + 1));
+  q.b_scost = (int64_t*)take(8 * (c.NCB + 1));
+  q.b_grp = (int32_t*)take(4 * (c.NCB + 1));
+  q.b_pos = (int32_t*)take(4 * (c.NCB + 1));
+  q.b_qoff = (int32_t*)take(4 * (c.M + 1));
+  q.b_queue = (QEntry*)take(sizeof(QEntry) * (c.NCB * c.Hkv + 1));
+  q.b_load_lpt = (int64_t*)take(8 * c.M);
+  q.b_load_contig = (int64_t*)take(8 * c.M);
+  if (p) *p = q;
+  return align_up(off, 256);
+}
+
+// Work workspace: partial O (or dQ) [slots][128][d] fp32, partial lse
+// [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32 and the
+// backward row term D [Hq][N_q] fp32.
+struct WorkPtrs {
+  float* part_o;
+  float* part_lse;
+  float* dq_draft;
+  float* dvec;
+};
+
+inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, char* base,
+                          WorkPtrs* p) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    off = align_up(off, 256);
+    char* r = base ? base + off : nullptr;
+    off += bytes;
+    return r;
+  };
+  WorkPtrs q;
+  q.part_o = (float*)take(sizeof(float) * (size_t)slots * kRows * d);
+  q.part_lse = (float*)take(sizeof(float) * (size_t)slots * kRows);
+  q.dq_draft = (float*)take(sizeof(float) * (size_t)nq * Hq * d);
+  q.dvec = (float*)take(sizeof(float) * (size_t)Hq * nq);
+  if (p) *p = q;
+  return align_up(off, 256);
+}
+
+// Scalars every kernel needs (passed by value).
+struct ProbDev {
+  int32_t S, B, Hq, Hkv, group, d, chunk, bps, workers, flags, dtype;
+  int64_t T, NA, NQ;
+  int32_t max_ctx;
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  uint64_t hash;
+  const int32_t* cu_ctx;
+  const int32_t* cu_anchor;
+  const int32_t* anchors;
+};
+
+}  // namespace skv

@@ -1,0 +1,441 @@
+// Device planner: realized-attention costs and LPT assignment.
+//
+// Cost of a work item = the number of masked (query, key) pairs it covers,
+// sum over anchors a_j > start of min(len, a_j - start) * B — the "realized
+// attention cost" by which the Split-KV abstract (arXiv:2611.05926) balances
+// KV chunks; the rit.work article on Split-KV (paragraph on anchor sampling
+// and load imbalance) notes the planner can price every segment in advance
+// because it sees all queries, and gives the rule: sort segments from most to
+// least expensive, give each to the least-loaded accelerator.
+//
+// Items are priced per (sample, chunk, slab) — the cost does not depend on
+// the kv head — and LPT runs over m/Hkv worker groups. Because the Hkv
+// replicas of an item have equal cost and consecutive ids (kv head fastest),
+// per-head LPT over m workers puts replica g of every item on worker
+// Hkv*G + g, where G is the group that grouped LPT picks; the grouped run is
+// therefore bit-identical to the per-head rule, Hkv times cheaper.
+//
+// Three launches: (1) one CTA validates the metadata, computes per-sample
+// and per-slab tables and all candidate costs, and compacts positive-cost
+// items; (2) a grid ranks items by (cost desc, id asc) by counting; (3) one
+// CTA runs the greedy assignment (one warp per direction) and builds the
+// per-worker queues and load tables.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace skv {
+
+namespace {
+
+__device__ __forceinline__ int64_t fwd_item_cost(const ProbDev& P, int s, int c, int sigma,
+                                                 int* ke_out) {
+  const int c0 = P.cu_ctx[s];
+  const int L = P.cu_ctx[s + 1] - c0;
+  const int a0 = P.cu_anchor[s];
+  const int A = P.cu_anchor[s + 1] - a0;
+  const int cs = c * P.chunk;
+  const int cl = min(P.chunk, L - cs);
+  const int first = a0 + sigma * P.bps;
+  const int nblk = min(P.bps, A - sigma * P.bps);
+  int64_t cost = 0;
+  int amax = 0;
+  for (int b = 0; b < nblk; ++b) {
+    const int a = P.anchors[first + b];
+    amax = max(amax, a);
+    if (a > cs) cost += (int64_t)min(cl, a - cs) * P.B;
+  }
+  *ke_out = min(cs + cl, amax);
+  return cost;
+}
+
+__device__ __forceinline__ int64_t bwd_item_cost(const ProbDev& P, int s, int kt) {
+  const int c0 = P.cu_ctx[s];
+  const int L = P.cu_ctx[s + 1] - c0;
+  const int a0 = P.cu_anchor[s];
+  const int a1 = P.cu_anchor[s + 1];
+  const int ks = kt * kKeyTile;
+  const int tl = min(kKeyTile, L - ks);
+  // first anchor > ks (anchors are non-decreasing within the sample)
+  int lo = a0, hi = a1;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (P.anchors[mid] > ks) hi = mid; else lo = mid + 1;
+  }
+  int64_t cost = 0;
+  for (int j = lo; j < a1; ++j) cost += (int64_t)min(tl, P.anchors[j] - ks) * P.B;
+  return cost;
+}
+
+// Chunked block scan over an int array producer; writes exclusive prefixes.
+template <typename Get, typename Put>
+__device__ int64_t scan_array(int n, Get get, Put put, int64_t* ws) {
+  int64_t carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int64_t v = i < n ? get(i) : 0;
+    int64_t tot;
+    const int64_t pre = block_exclusive_scan<int64_t>(v, ws, &tot);
+    if (i < n) put(i, carry + pre);
+    carry += tot;
+  }
+  return carry;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp, PlanCaps caps) {
+  __shared__ int64_t ws[32];
+  __shared__ unsigned long long tiles_acc, dense_acc;
+  PlanHeader* H = pp.hdr;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    H->magic = kPlanMagic;
+    H->status = 0;
+    H->workers = P.workers;
+    H->groups = P.workers / P.Hkv;
+    H->flags = P.flags;
+    H->problem_hash = P.hash;
+    H->n_slabs = H->n_fwd_cand = H->n_fwd_items = H->n_slot_base = 0;
+    H->n_bwd_cand = H->n_bwd_items = 0;
+    H->fwd_total_cost = H->bwd_total_cost = H->fwd_tiles = H->dense_tiles = 0;
+    tiles_acc = 0;
+    dense_acc = 0;
+  }
+  __syncthreads();
+  const int S = P.S;
+  // ---- A: validate metadata, per-sample counts -------------------------
+  if (tid == 0) {
+    if (P.cu_ctx[0] != 0 || P.cu_anchor[0] != 0 || (int64_t)P.cu_ctx[S] != P.T ||
+        (int64_t)P.cu_anchor[S] != P.NA)
+      latch(H, SPLITKV_EMETA);
+  }
+  for (int s = tid; s < S; s += blockDim.x) {
+    const int L = P.cu_ctx[s + 1] - P.cu_ctx[s];
+    const int A = P.cu_anchor[s + 1] - P.cu_anchor[s];
+    if (L < 0 || A < 0 || L > P.max_ctx) {
+      latch(H, SPLITKV_EMETA);
+      continue;
+    }
+    pp.s_nch[s] = (L + P.chunk - 1) / P.chunk;
+    pp.s_nsl[s] = (A + P.bps - 1) / P.bps;
+    pp.s_nkt[s] = (L + kKeyTile - 1) / kKeyTile;
+    const long long rows = (long long)A * P.B * P.group;
+    atomicAdd(&dense_acc, (unsigned long long)(((rows + kRows - 1) / kRows) *
+                                               ((L + kKeyTile - 1) / kKeyTile)));
+  }
+  for (int64_t i = tid; i < P.NA; i += blockDim.x) {
+    const int s = seg_of(P.cu_anchor, S, i);
+    const int L = P.cu_ctx[s + 1] - P.cu_ctx[s];
+    const int a = P.anchors[i];
+    if (a < 0 || a > L - P.B) latch(H, SPLITKV_EMETA);
+    if (i + 1 < P.NA && i + 1 < P.cu_anchor[s + 1] && P.anchors[i + 1] < a)
+      latch(H, SPLITKV_EMETA);
+  }
+  __syncthreads();
+  if (read_status(H) != 0) return;
+  // ---- B: per-sample offsets --------------------------------------------
+  const int64_t ncand = scan_array(
+      S, [&](int s) { return (int64_t)pp.s_nch[s] * pp.s_nsl[s]; },
+      [&](int s, int64_t v) { pp.s_cand_off[s] = (int32_t)v; }, ws);
+  const int64_t nslab = scan_array(
+      S, [&](int s) { return (int64_t)pp.s_nsl[s]; },
+      [&](int s, int64_t v) { pp.s_slab_off[s] = (int32_t)v; }, ws);
+  const int64_t nbcand = scan_array(
+      S, [&](int s) { return (int64_t)pp.s_nkt[s]; },
+      [&](int s, int64_t v) { pp.s_bcand_off[s] = (int32_t)v; }, ws);
+  if (tid == 0) {
+    if (ncand > caps.NCF || nslab > caps.NSL || nbcand > caps.NCB) latch(H, SPLITKV_ECAPACITY);
+    pp.s_cand_off[S] = (int32_t)ncand;
+    pp.s_slab_off[S] = (int32_t)nslab;
+    pp.s_bcand_off[S] = (int32_t)nbcand;
+    H->n_slabs = (int32_t)nslab;
+    H->n_fwd_cand = (int32_t)ncand;
+    H->n_bwd_cand = (int32_t)nbcand;
+  }
+  __syncthreads();
+  if (read_status(H) != 0) return;
+  // ---- C: slab table ------------------------------------------------------
+  for (int sg = tid; sg < nslab; sg += blockDim.x) {
+    const int s = seg_of(pp.s_slab_off, S, sg);
+    const int sigma = sg - pp.s_slab_off[s];
+    const int a0 = P.cu_anchor[s];
+    const int A = P.cu_anchor[s + 1] - a0;
+    const int first = a0 + sigma * P.bps;
+    const int nblk = min(P.bps, A - sigma * P.bps);
+    const int amax = P.anchors[first + nblk - 1];
+    pp.sl_sample[sg] = s;
+    pp.sl_first[sg] = first;
+    pp.sl_nblk[sg] = nblk;
+    pp.sl_nact[sg] = (amax + P.chunk - 1) / P.chunk;
+  }
+  __syncthreads();
+  const int64_t nslot = scan_array(
+      (int)nslab, [&](int i) { return (int64_t)pp.sl_nact[i]; },
+      [&](int i, int64_t v) { pp.sl_slot[i] = (int32_t)v; }, ws);
+  if (tid == 0) {
+    pp.sl_slot[nslab] = (int32_t)nslot;
+    H->n_slot_base = (int32_t)nslot;
+  }
+  // ---- D: candidate costs -------------------------------------------------
+  for (int id = tid; id < ncand; id += blockDim.x) {
+    const int s = seg_of(pp.s_cand_off, S, id);
+    const int local = id - pp.s_cand_off[s];
+    const int nsl = pp.s_nsl[s];
+    const int c = local / nsl, sigma = local % nsl;
+    int ke;
+    const int64_t cost = fwd_item_cost(P, s, c, sigma, &ke);
+    pp.f_cost[id] = cost;
+    if (cost > 0) {
+      const int cs = c * P.chunk;
+      atomicAdd(&tiles_acc, (unsigned long long)((ke - cs + kKeyTile - 1) / kKeyTile));
+    }
+  }
+  for (int id = tid; id < nbcand; id += blockDim.x) {
+    const int s = seg_of(pp.s_bcand_off, S, id);
+    pp.b_cost[id] = bwd_item_cost(P, s, id - pp.s_bcand_off[s]);
+  }
+  __syncthreads();
+  // ---- E: compaction (id order preserved) ---------------------------------
+  for (int kind = 0; kind < 2; ++kind) {
+    const int n = kind == 0 ? (int)ncand : (int)nbcand;
+    const int64_t* cost = kind == 0 ? pp.f_cost : pp.b_cost;
+    int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
+    int64_t* prefix = kind == 0 ? pp.f_prefix : pp.b_prefix;
+    int64_t carry_n = 0, carry_c = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + tid;
+      const int64_t c = i < n ? cost[i] : 0;
+      int64_t tn, tc;
+      const int64_t pn = block_exclusive_scan<int64_t>(c > 0 ? 1 : 0, ws, &tn);
+      const int64_t pc = block_exclusive_scan<int64_t>(c, ws, &tc);
+      if (c > 0) {
+        item[carry_n + pn] = i;
+        prefix[carry_n + pn] = carry_c + pc;
+      }
+      carry_n += tn;
+      carry_c += tc;
+    }
+    if (tid == 0) {
+      prefix[carry_n] = carry_c;
+      if (kind == 0) {
+        H->n_fwd_items = (int32_t)carry_n;
+        H->fwd_total_cost = carry_c;
+      } else {
+        H->n_bwd_items = (int32_t)carry_n;
+        H->bwd_total_cost = carry_c;
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    H->fwd_tiles = (int64_t)tiles_acc;
+    H->dense_tiles = (int64_t)dense_acc;
+  }
+}
+
+// Rank of item i = #{j : cost_j > cost_i or (cost_j == cost_i and j < i)}.
+// Keys are unique, so the ranks form the permutation of the sort
+// (cost desc, id asc); items are in id order after compaction.
+__global__ void __launch_bounds__(256) plan_rank_kernel(PlanPtrs pp) {
+  __shared__ int64_t tile[1024];
+  const PlanHeader* H = pp.hdr;
+  if (read_status(H) != 0) return;
+  const int kind = blockIdx.y;
+  const int n = kind == 0 ? H->n_fwd_items : H->n_bwd_items;
+  const int64_t* cost = kind == 0 ? pp.f_cost : pp.b_cost;
+  const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if ((int)(blockIdx.x * blockDim.x) >= n) return;  // whole CTA idle
+  const int64_t ci = i < n ? cost[item[i]] : 0;
+  int rank = 0;
+  for (int j0 = 0; j0 < n; j0 += 1024) {
+    __syncthreads();
+    for (int t = threadIdx.x; t < 1024; t += blockDim.x)
+      tile[t] = (j0 + t < n) ? cost[item[j0 + t]] : INT64_MIN;
+    __syncthreads();
+    const int lim = min(1024, n - j0);
+    for (int t = 0; t < lim; ++t) {
+      const int64_t cj = tile[t];
+      rank += (cj > ci) | ((cj == ci) & (j0 + t < i));
+    }
+  }
+  if (i < n) {
+    (kind == 0 ? pp.f_sorted : pp.b_sorted)[rank] = i;
+    (kind == 0 ? pp.f_scost : pp.b_scost)[rank] = ci;
+  }
+}
+
+namespace {
+
+// Greedy LPT over the worker groups for one direction, run by one warp.
+// Lane l owns groups l, l+32, ... (at most kMaxGroupsPerLane each).
+__device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32_t* pos,
+                         int64_t* gload, int32_t* gcount) {
+  const int lane = threadIdx.x & 31;
+  int64_t load[kMaxGroupsPerLane];
+  int32_t cnt[kMaxGroupsPerLane];
+#pragma unroll
+  for (int k = 0; k < kMaxGroupsPerLane; ++k) {
+    load[k] = 0;
+    cnt[k] = 0;
+  }
+  for (int r0 = 0; r0 < n; r0 += 32) {
+    const int64_t mine = (r0 + lane < n) ? scost[r0 + lane] : 0;
+    const int lim = min(32, n - r0);
+    for (int t = 0; t < lim; ++t) {
+      const int64_t c = __shfl_sync(0xffffffffu, mine, t);
+      int64_t bl = INT64_MAX;
+      int bg = INT32_MAX;
+#pragma unroll
+      for (int k = 0; k < kMaxGroupsPerLane; ++k) {
+        const int gid = lane + 32 * k;
+        if (gid < G && load[k] < bl) {  // ascending gid within the lane
+          bl = load[k];
+          bg = gid;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int64_t ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        const int og = __shfl_xor_sync(0xffffffffu, bg, o);
+        if (ol < bl || (ol == bl && og < bg)) {
+          bl = ol;
+          bg = og;
+        }
+      }
+      if ((bg & 31) == lane) {
+        const int kk = bg >> 5;
+#pragma unroll
+        for (int k = 0; k < kMaxGroupsPerLane; ++k) {
+          if (k == kk) {
+            grp[r0 + t] = bg;
+            pos[r0 + t] = cnt[k];
+            cnt[k] += 1;
+            load[k] += c;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxGroupsPerLane; ++k) {
+    const int gid = lane + 32 * k;
+    if (gid < G) {
+      gload[gid] = load[k];
+      gcount[gid] = cnt[k];
+    }
+  }
+}
+
+__device__ __forceinline__ QEntry decode_fwd(const ProbDev& P, const PlanPtrs& pp, int cand,
+                                             int g) {
+  const int s = seg_of(pp.s_cand_off, P.S, cand);
+  const int local = cand - pp.s_cand_off[s];
+  const int nsl = pp.s_nsl[s];
+  QEntry e;
+  e.s = s;
+  e.c = local / nsl;
+  e.slab = pp.s_slab_off[s] + local % nsl;
+  e.g = g;
+  return e;
+}
+
+__device__ __forceinline__ QEntry decode_bwd(const ProbDev& P, const PlanPtrs& pp, int cand,
+                                             int g) {
+  const int s = seg_of(pp.s_bcand_off, P.S, cand);
+  QEntry e;
+  e.s = s;
+  e.c = cand - pp.s_bcand_off[s];
+  e.slab = 0;
+  e.g = g;
+  return e;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs pp) {
+  __shared__ int64_t ws[32];
+  __shared__ int64_t gload[2][32 * kMaxGroupsPerLane];
+  __shared__ int32_t gcount[2][32 * kMaxGroupsPerLane];
+  const PlanHeader* H = pp.hdr;
+  if (read_status(H) != 0) return;
+  const int tid = threadIdx.x;
+  const int m = P.workers, Hkv = P.Hkv, G = m / Hkv;
+  const bool contiguous = (P.flags & SPLITKV_FLAG_CONTIGUOUS) != 0;
+  const int warp = tid >> 5;
+  if (warp < 2) {
+    const int n = warp == 0 ? H->n_fwd_items : H->n_bwd_items;
+    lpt_warp(n, G, warp == 0 ? pp.f_scost : pp.b_scost, warp == 0 ? pp.f_grp : pp.b_grp,
+             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp]);
+  }
+  __syncthreads();
+  for (int kind = 0; kind < 2; ++kind) {
+    const int n = kind == 0 ? H->n_fwd_items : H->n_bwd_items;
+    const int64_t N = (int64_t)n * Hkv;  // per-head items
+    const int64_t* cost = kind == 0 ? pp.f_cost : pp.b_cost;
+    const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
+    const int64_t* prefix = kind == 0 ? pp.f_prefix : pp.b_prefix;
+    int32_t* qoff = kind == 0 ? pp.f_qoff : pp.b_qoff;
+    QEntry* queue = kind == 0 ? pp.f_queue : pp.b_queue;
+    int64_t* load_lpt = kind == 0 ? pp.f_load_lpt : pp.b_load_lpt;
+    int64_t* load_contig = kind == 0 ? pp.f_load_contig : pp.b_load_contig;
+    // Per-head cost prefix F(x) over the per-head items in id order.
+    auto F = [&](int64_t x) -> int64_t {
+      const int64_t b = x / Hkv, r = x % Hkv;
+      int64_t v = prefix[b] * Hkv;
+      if (r) v += r * cost[item[b]];
+      return v;
+    };
+    for (int w = tid; w < m; w += blockDim.x) {
+      load_lpt[w] = gload[kind][w / Hkv];
+      const int64_t lo = (int64_t)w * N / m, hi = (int64_t)(w + 1) * N / m;
+      load_contig[w] = F(hi) - F(lo);
+    }
+    if (!contiguous) {
+      const int64_t tot = scan_array(
+          m, [&](int w) { return (int64_t)gcount[kind][w / Hkv]; },
+          [&](int w, int64_t v) { qoff[w] = (int32_t)v; }, ws);
+      if (tid == 0) qoff[m] = (int32_t)tot;
+      __syncthreads();
+      const int32_t* sorted = kind == 0 ? pp.f_sorted : pp.b_sorted;
+      const int32_t* grp = kind == 0 ? pp.f_grp : pp.b_grp;
+      const int32_t* pos = kind == 0 ? pp.f_pos : pp.b_pos;
+      for (int r = tid; r < n; r += blockDim.x) {
+        const int cand = item[sorted[r]];
+        const int Gr = grp[r], p = pos[r];
+        for (int g = 0; g < Hkv; ++g) {
+          QEntry e = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
+          queue[qoff[Gr * Hkv + g] + p] = e;
+        }
+      }
+    } else {
+      for (int w = tid; w <= m; w += blockDim.x) qoff[w] = (int32_t)((int64_t)w * N / m);
+      for (int64_t x = tid; x < N; x += blockDim.x) {
+        const int cand = item[x / Hkv];
+        const int g = (int)(x % Hkv);
+        queue[x] = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace skv
+
+namespace skv {
+
+cudaError_t launch_plan(const ProbDev& P, const PlanPtrs& pp, const PlanCaps& caps,
+                        cudaStream_t st) {
+  plan_setup_kernel<<<1, 1024, 0, st>>>(P, pp, caps);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int64_t maxn = caps.NCF > caps.NCB ? caps.NCF : caps.NCB;
+  dim3 grid((unsigned)((maxn + 255) / 256 > 0 ? (maxn + 255) / 256 : 1), 2);
+  plan_rank_kernel<<<grid, 256, 0, st>>>(pp);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  plan_assign_kernel<<<1, 1024, 0, st>>>(P, pp);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

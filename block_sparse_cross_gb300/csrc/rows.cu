@@ -1,0 +1,340 @@
+// Row kernels of the split (HBM-bound, CUDA cores):
+//
+//  merge        per (query, head): the draft-block partial over the block's
+//               own B draft keys, then the exact log-sum-exp merge of every
+//               chunk partial of the row in ascending chunk order, then the
+//               draft partial — the "reconcile the normalisation" step of the
+//               rit.work article on Split-KV (section "Split-KV двигает
+//               запросы, а не ключи и значения"); exact, so the result equals
+//               the single-device attention.
+//  bwd_draft    per (draft block, kv head): D = rowsum(dO * O) for its rows,
+//               the full backward of the B x B draft self-block (dKd, dVd
+//               summed over the group's heads in fixed order) and the draft
+//               term of dQ (fp32, unscaled).
+//  dq_reduce    per (query, head): dQ = scale * (sum over chunk partials in
+//               ascending chunk order + draft term); the query gradients are
+//               what moves between shards in the article's description.
+//  zero         context rows that no draft block sees get dK = dV = 0.
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace skv {
+
+namespace {
+
+struct RowGeom {
+  int slab;     // global slab index
+  int r;        // row inside the slab's 128-row item
+  int anchor;
+  int nact;     // chunks whose keys the row sees: ceil(anchor / C)
+};
+
+__device__ __forceinline__ RowGeom row_geom(const ProbDev& P, const PlanPtrs& pp, int n, int h) {
+  RowGeom G;
+  const int j = n / P.B, qi = n % P.B;
+  const int s = seg_of(P.cu_anchor, P.S, j);
+  const int lj = j - P.cu_anchor[s];
+  G.slab = pp.s_slab_off[s] + lj / P.bps;
+  const int b = lj % P.bps;
+  G.r = (b * P.B + qi) * P.group + (h % P.group);
+  G.anchor = P.anchors[j];
+  G.nact = (G.anchor + P.chunk - 1) / P.chunk;
+  return G;
+}
+
+template <typename T, int EPL>
+__device__ __forceinline__ void ld_vec(const T* p, float* v) {
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) v[i] = ld_f(p + i);
+}
+template <typename T, int EPL>
+__device__ __forceinline__ void st_vec(T* p, const float* v) {
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) st_f(p + i, v[i]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One warp per (query n, head h); lane owns dims [lane*EPL, lane*EPL + EPL).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                    const T* __restrict__ Q,
+                                                    const T* __restrict__ Kd,
+                                                    const T* __restrict__ Vd,
+                                                    T* __restrict__ O, float* __restrict__ LSE) {
+  constexpr int EPL = D / 32;
+  if (read_status(pp.hdr) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= P.NQ * P.Hq) return;
+  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
+  const int g = h / P.group;
+  const int j = n / P.B;
+  const RowGeom G = row_geom(P, pp, n, h);
+  const int x0 = lane * EPL;
+  // draft partial over the block's B draft keys (bidirectional within the block)
+  float q[EPL], od[EPL], tmp[EPL];
+  ld_vec<T, EPL>(Q + ((size_t)n * P.Hq + h) * D + x0, q);
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    q[i] *= P.scale;
+    od[i] = 0.f;
+  }
+  float md = -INFINITY, ld = 0.f;
+  for (int t = 0; t < P.B; ++t) {
+    const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
+    ld_vec<T, EPL>(Kd + kro, tmp);
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) part = fmaf(q[i], tmp[i], part);
+    const float sc = warp_sum(part);
+    ld_vec<T, EPL>(Vd + kro, tmp);
+    if (sc > md) {
+      const float f = expf(md - sc);
+      ld = ld * f + 1.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) od[i] = fmaf(od[i], f, tmp[i]);
+      md = sc;
+    } else {
+      const float p = expf(sc - md);
+      ld += p;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) od[i] = fmaf(p, tmp[i], od[i]);
+    }
+  }
+  const float lse_d = md + logf(ld);
+  // pass 1: max and normaliser over chunk partials (+ draft)
+  const size_t slot0 = (size_t)pp.sl_slot[G.slab];
+  float M = lse_d;
+  for (int c = lane; c < G.nact; c += 32)
+    M = fmaxf(M, wk.part_lse[((slot0 + c) * P.Hkv + g) * kRows + G.r]);
+  M = warp_max(M);
+  float Ls = 0.f;
+  for (int c = lane; c < G.nact; c += 32)
+    Ls += expf(wk.part_lse[((slot0 + c) * P.Hkv + g) * kRows + G.r] - M);
+  Ls = warp_sum(Ls) + expf(lse_d - M);
+  const float invL = 1.f / Ls;
+  // pass 2: weighted sum in ascending chunk order, then the draft partial
+  float acc[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+  for (int c = 0; c < G.nact; ++c) {
+    const size_t row = ((slot0 + c) * P.Hkv + g) * kRows + G.r;
+    const float wgt = expf(wk.part_lse[row] - M) * invL;
+    const float* po = wk.part_o + row * D + x0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wgt, po[i], acc[i]);
+  }
+  const float wd = expf(lse_d - M) * invL / ld;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wd, od[i], acc[i]);
+  st_vec<T, EPL>(O + ((size_t)n * P.Hq + h) * D + x0, acc);
+  if (lane == 0) LSE[(size_t)h * P.NQ + n] = M + logf(Ls);
+}
+
+// One CTA per (draft block j, kv head g); thread r = (qi, hg) row of the
+// block, r = qi * group + hg (B * group <= 128 rows).
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                        const T* __restrict__ Q,
+                                                        const T* __restrict__ Kd,
+                                                        const T* __restrict__ Vd,
+                                                        const T* __restrict__ O,
+                                                        const float* __restrict__ LSE,
+                                                        const T* __restrict__ dO,
+                                                        T* __restrict__ dKd,
+                                                        T* __restrict__ dVd) {
+  constexpr int RS = D + 1;                 // padded row stride (floats)
+  extern __shared__ float sm[];
+  const int B = P.B, R = B * P.group;
+  float* kd = sm;                           // [B][D]
+  float* vd = kd + B * D;                   // [B][D]
+  float* qs = vd + B * D;                   // [R][RS]
+  float* dos = qs + R * RS;                 // [R][RS]
+  float* ps = dos + R * RS;                 // [R][B]
+  float* dss = ps + R * B;                  // [R][B]
+  if (read_status(pp.hdr) != 0) return;
+  const int j = blockIdx.x, g = blockIdx.y;
+  const int tid = threadIdx.x;
+  for (int idx = tid; idx < B * D; idx += blockDim.x) {
+    const int t = idx / D, x = idx % D;
+    const size_t o = ((size_t)(j * B + t) * P.Hkv + g) * D + x;
+    kd[idx] = ld_f(Kd + o);
+    vd[idx] = ld_f(Vd + o);
+  }
+  for (int idx = tid; idx < R * D; idx += blockDim.x) {
+    const int r = idx / D, x = idx % D;
+    const int n = j * B + r / P.group, h = g * P.group + r % P.group;
+    const size_t o = ((size_t)n * P.Hq + h) * D + x;
+    qs[r * RS + x] = ld_f(Q + o);
+    dos[r * RS + x] = ld_f(dO + o);
+  }
+  __syncthreads();
+  if (tid < R) {
+    const int r = tid;
+    const int n = j * B + r / P.group, h = g * P.group + r % P.group;
+    const T* orow = O + ((size_t)n * P.Hq + h) * D;
+    float Dr = 0.f;
+    for (int x = 0; x < D; ++x) Dr = fmaf(dos[r * RS + x], ld_f(orow + x), Dr);
+    wk.dvec[(size_t)h * P.NQ + n] = Dr;
+    const float lse = LSE[(size_t)h * P.NQ + n];
+    for (int t = 0; t < B; ++t) {
+      float sc = 0.f, dp = 0.f;
+      for (int x = 0; x < D; ++x) {
+        sc = fmaf(qs[r * RS + x], kd[t * D + x], sc);
+        dp = fmaf(dos[r * RS + x], vd[t * D + x], dp);
+      }
+      const float p = expf(sc * P.scale - lse);
+      ps[r * B + t] = p;
+      dss[r * B + t] = p * (dp - Dr);
+    }
+    float* dqd = wk.dq_draft + ((size_t)n * P.Hq + h) * D;
+    for (int x = 0; x < D; ++x) {
+      float a = 0.f;
+      for (int t = 0; t < B; ++t) a = fmaf(dss[r * B + t], kd[t * D + x], a);
+      dqd[x] = a;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < B * D; idx += blockDim.x) {
+    const int t = idx / D, x = idx % D;
+    float av = 0.f, ak = 0.f;
+    for (int r = 0; r < R; ++r) {
+      av = fmaf(ps[r * B + t], dos[r * RS + x], av);
+      ak = fmaf(dss[r * B + t], qs[r * RS + x], ak);
+    }
+    const size_t o = ((size_t)(j * B + t) * P.Hkv + g) * D + x;
+    st_f(dVd + o, av);
+    st_f(dKd + o, ak * P.scale);
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                        T* __restrict__ dQ) {
+  constexpr int EPL = D / 32;
+  if (read_status(pp.hdr) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= P.NQ * P.Hq) return;
+  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
+  const int g = h / P.group;
+  const RowGeom G = row_geom(P, pp, n, h);
+  const int x0 = lane * EPL;
+  const size_t slot0 = (size_t)pp.sl_slot[G.slab];
+  float acc[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+  for (int c = 0; c < G.nact; ++c) {
+    const float* po = wk.part_o + (((slot0 + c) * P.Hkv + g) * kRows + G.r) * D + x0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] += po[i];
+  }
+  const float* dd = wk.dq_draft + ((size_t)n * P.Hq + h) * D + x0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = (acc[i] + dd[i]) * P.scale;
+  st_vec<T, EPL>(dQ + ((size_t)n * P.Hq + h) * D + x0, acc);
+}
+
+// Rows of sample s at local index >= 128 * ceil(a_last / 128) are in no
+// backward item (no block sees them); their key/value gradients are zero.
+template <typename T>
+__global__ void zero_uncovered_kernel(ProbDev P, PlanPtrs pp, T* __restrict__ dKc,
+                                      T* __restrict__ dVc) {
+  if (read_status(pp.hdr) != 0) return;
+  const int64_t row_elems = (int64_t)P.Hkv * P.d;
+  for (int64_t t = blockIdx.x; t < P.T; t += gridDim.x) {
+    const int s = seg_of(P.cu_ctx, P.S, t);
+    const int local = (int)(t - P.cu_ctx[s]);
+    const int a0 = P.cu_anchor[s], a1 = P.cu_anchor[s + 1];
+    const int alast = a1 > a0 ? P.anchors[a1 - 1] : 0;
+    const int covered = (alast + kKeyTile - 1) / kKeyTile * kKeyTile;
+    if (local < covered) continue;
+    for (int64_t x = threadIdx.x; x < row_elems; x += blockDim.x) {
+      st_f(dKc + t * row_elems + x, 0.f);
+      st_f(dVc + t * row_elems + x, 0.f);
+    }
+  }
+}
+
+template <typename F>
+cudaError_t dispatch(const ProbDev& P, F&& f) {
+  using D64 = std::integral_constant<int, 64>;
+  using D128 = std::integral_constant<int, 128>;
+  if (P.dtype == SPLITKV_FP32) return P.d == 64 ? f(float(), D64()) : f(float(), D128());
+  return P.d == 64 ? f(__nv_bfloat16(), D64()) : f(__nv_bfloat16(), D128());
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                         const void* Q, const void* Kd, const void* Vd, void* O, float* LSE,
+                         cudaStream_t st) {
+  return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
+    using T = decltype(tag);
+    constexpr int D = decltype(dtag)::value;
+    const int64_t warps = P.NQ * P.Hq;
+    if (warps == 0) return cudaSuccess;
+    merge_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (T*)O, LSE);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                             const void* Q, const void* Kd, const void* Vd, const void* O,
+                             const float* LSE, const void* dO, void* dKd, void* dVd,
+                             cudaStream_t st) {
+  return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
+    using T = decltype(tag);
+    constexpr int D = decltype(dtag)::value;
+    if (P.NA == 0) return cudaSuccess;
+    const int R = P.B * P.group;
+    const size_t smem = sizeof(float) * (2 * P.B * D + 2 * R * (D + 1) + 2 * R * P.B);
+    auto k = bwd_draft_kernel<T, D>;
+    cudaError_t err =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)P.NA, (unsigned)P.Hkv);
+    k<<<grid, 128, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O,
+                               LSE, (const T*)dO, (T*)dKd, (T*)dVd);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
+                             cudaStream_t st) {
+  return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
+    using T = decltype(tag);
+    constexpr int D = decltype(dtag)::value;
+    const int64_t warps = P.NQ * P.Hq;
+    if (warps == 0) return cudaSuccess;
+    dq_reduce_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(P, pp, wk, (T*)dQ);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,
+                                  cudaStream_t st) {
+  if (P.T == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)(P.T < 4096 ? P.T : 4096);
+  if (P.dtype == SPLITKV_FP32)
+    zero_uncovered_kernel<float><<<grid, 256, 0, st>>>(P, pp, (float*)dKc, (float*)dVc);
+  else
+    zero_uncovered_kernel<__nv_bfloat16>
+        <<<grid, 256, 0, st>>>(P, pp, (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,265 @@
+/*
+ * splitkv.h — C ABI of the GB300 split-KV block-sparse cross-attention library.
+ *
+ * What it computes. Exact anchor-masked cross-attention of short draft-query
+ * blocks over a long context, forward and backward (Split-KV: Efficient
+ * Context Parallelism for Training Diffusion Drafters, arXiv:2611.05926,
+ * abstract: anchor sampling builds compact draft queries that cross-attend to
+ * a much longer context under a block-sparse mask). For draft block j of
+ * sample s with anchor a_j, the B query rows of the block attend to
+ *   - the context keys [0, a_j) of sample s (strict prefix), and
+ *   - the B keys of the block's own draft tokens (bidirectional),
+ * with softmax scale `scale`; query head h reads kv head h / (Hq / Hkv).
+ *
+ * How. The paper's context-parallel recipe (rit.work article on Split-KV,
+ * section "Split-KV двигает запросы, а не ключи и значения": K/V shards stay
+ * where they are, every participant sees all queries, computes its local
+ * part of attention, the normalisation is reconciled, the result returns to
+ * the query owners; the split reproduces the single-device result exactly)
+ * is mapped onto the SMs of one GPU: KV chunks are the shards, persistent
+ * CTAs are the participants, per-chunk (lse, O) partials are merged exactly
+ * by log-sum-exp, and dQ partials are reduced in a fixed order. A planner
+ * prices every work item by its realized masked work and assigns items with
+ * longest-processing-time-first (abstract; rit.work article, paragraph on
+ * anchor sampling and load imbalance).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major, contiguous:
+ *      Q, O, dO, dQ        [N_q, Hq, d]      dtype     N_q = B * total_anchors
+ *      Kc, Vc, dKc, dVc    [T, Hkv, d]       dtype     T = total_ctx
+ *      Kd, Vd, dKd, dVd    [N_q, Hkv, d]     dtype     (draft-token keys/values)
+ *      LSE                 [Hq, N_q]         float32   natural log of the row's
+ *                                                      softmax normaliser
+ *    Draft block j (global order over samples) owns query rows [jB, jB+B).
+ *    Every pointer must be 16-byte aligned.
+ *  - The caller owns every buffer, including both workspaces; the library
+ *    never allocates, frees or synchronises device memory, except where a
+ *    function says it reads back to the host.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream). The buffers must stay valid until the stream passes
+ *    the enqueued work.
+ *  - Every function returns a status code (SPLITKV_OK on success) and never
+ *    throws or aborts. Host-detectable errors (null pointers, unsupported
+ *    shapes, workspace too small) are returned immediately. Errors found on
+ *    the device (invalid anchors, a plan that belongs to another problem, a
+ *    pipeline wait that timed out) are latched in a status word inside the
+ *    plan workspace; kernels that see it set skip their work, and
+ *    splitkv_plan_stats() / splitkv_device_status() read it back.
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* splitkv_stream; /* == cudaStream_t */
+
+/* Status codes. */
+enum {
+  SPLITKV_OK = 0,
+  SPLITKV_EINVAL = 1,       /* bad argument: null pointer, negative size, bad metadata */
+  SPLITKV_EUNSUPPORTED = 2, /* shape/dtype outside the supported set */
+  SPLITKV_EWORKSPACE = 3,   /* a workspace is smaller than splitkv_workspace_size() says */
+  SPLITKV_ECUDA = 4,        /* a CUDA runtime call failed */
+  SPLITKV_EDEVICE = 5,      /* no usable sm_100-family device */
+  SPLITKV_ETIMEOUT = 6,     /* device status: a bounded pipeline wait gave up */
+  SPLITKV_EPLAN = 7,        /* device status: plan built for a different problem */
+  SPLITKV_EMETA = 8,        /* device status: cu_ctx/cu_anchor/anchors inconsistent */
+  SPLITKV_ECAPACITY = 9     /* device status: metadata exceeds the host-declared sizes */
+};
+
+/* Compute dtypes (inputs and outputs; accumulation is always fp32). */
+enum { SPLITKV_BF16 = 0, SPLITKV_FP32 = 1 };
+
+/* Problem flags. */
+enum {
+  /* Use the CUDA-core (FMA) attention kernels instead of the tensor-core
+   * ones. bf16 problems default to tcgen05 tensor cores; fp32 problems always
+   * use the CUDA-core kernels (exact fp32 products). */
+  SPLITKV_FLAG_CUDA_CORE = 1,
+  /* Execute the naive contiguous assignment (worker w takes items
+   * [floor(w n/m), floor((w+1) n/m)) in id order) instead of LPT. */
+  SPLITKV_FLAG_CONTIGUOUS = 2
+};
+
+/*
+ * Problem description. Device pointers: cu_ctx, cu_anchor, anchors. Every
+ * other field is a host value.
+ *
+ *  num_samples   S >= 1 packed samples.
+ *  cu_ctx        int32 [S+1] device; cu_ctx[0] = 0, non-decreasing, cu_ctx[S] = total_ctx.
+ *                Sample s owns context rows [cu_ctx[s], cu_ctx[s+1]) of Kc/Vc.
+ *  cu_anchor     int32 [S+1] device; cu_anchor[0] = 0, non-decreasing,
+ *                cu_anchor[S] = total_anchors. Sample s owns draft blocks
+ *                [cu_anchor[s], cu_anchor[s+1]).
+ *  anchors       int32 [total_anchors] device; sample-local anchor positions,
+ *                non-decreasing within a sample, 0 <= a <= L_s - B.
+ *  total_ctx     T = cu_ctx[S] (host copy, sizes Kc/Vc).
+ *  total_anchors cu_anchor[S] (host copy); N_q = B * total_anchors.
+ *  max_ctx       an upper bound on max_s L_s (sizes the plan).
+ *  B             draft block size (queries per anchor).
+ *  Hq, Hkv       query / kv heads; Hq % Hkv == 0; group = Hq / Hkv.
+ *  d             head dim: 64 or 128.
+ *  chunk         KV chunk length C (keys) of the split; a multiple of 128.
+ *  scale         softmax scale (usually 1/sqrt(d)).
+ *  dtype         SPLITKV_BF16 or SPLITKV_FP32.
+ *  num_workers   persistent CTAs the plan balances over; 0 = the device's SM
+ *                count rounded down to a multiple of Hkv. Must be a multiple
+ *                of Hkv and at most 256 * Hkv (and at most 4096).
+ *  flags         SPLITKV_FLAG_* bits.
+ *
+ * Supported set: 128 % (B * group) == 0 (a work item is 128 (query, head)
+ * rows = 128 / (B*group) whole draft blocks), d in {64, 128}, dtype bf16 or
+ * fp32. Anything else returns SPLITKV_EUNSUPPORTED.
+ */
+typedef struct splitkv_problem {
+  int32_t num_samples;
+  const int32_t* cu_ctx;
+  const int32_t* cu_anchor;
+  const int32_t* anchors;
+  int64_t total_ctx;
+  int64_t total_anchors;
+  int32_t max_ctx;
+  int32_t B;
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t d;
+  int32_t chunk;
+  float scale;
+  int32_t dtype;
+  int32_t num_workers;
+  int32_t flags;
+} splitkv_problem;
+
+/* Plan statistics (host struct filled by splitkv_plan_stats). Costs are in
+ * masked (query, key) pairs; loads are per persistent CTA. */
+typedef struct splitkv_stats {
+  int32_t device_status;      /* SPLITKV_OK or the latched device error */
+  int32_t workers;            /* persistent CTAs the plan uses */
+  int64_t fwd_items;          /* forward items (sample, chunk, slab, kv head), cost > 0 */
+  int64_t bwd_items;          /* backward items (sample, 128-key tile, kv head), cost > 0 */
+  int64_t fwd_slots;          /* forward/dQ partial slots in use */
+  int64_t fwd_total_cost;
+  int64_t bwd_total_cost;
+  int64_t fwd_lpt_max_load;
+  int64_t fwd_contig_max_load;
+  int64_t bwd_lpt_max_load;
+  int64_t bwd_contig_max_load;
+  double fwd_lpt_imbalance;   /* max/mean - 1 over workers */
+  double fwd_contig_imbalance;
+  double bwd_lpt_imbalance;
+  double bwd_contig_imbalance;
+  int64_t fwd_tiles;          /* 128x128 (row, key) tiles the forward computes */
+  int64_t dense_tiles;        /* tiles of the dense (N_q*group/128) x (L/128) x Hkv grid */
+  size_t work_bytes_used;     /* exact bytes of the work workspace this plan needs */
+} splitkv_stats;
+
+/*
+ * splitkv_workspace_size — bytes of the two caller-owned workspaces.
+ *   plan_bytes: holds the plan (costs, LPT queues, slab tables, status word);
+ *               built by splitkv_plan, read by splitkv_fwd / splitkv_bwd.
+ *   work_bytes: fp32 partials of the split (per chunk (lse, O) in the forward,
+ *               per chunk dQ and the draft-block terms in the backward). This
+ *               is an upper bound computed from host scalars; the exact need
+ *               of a built plan is splitkv_stats.work_bytes_used.
+ * Host-only; no device work. Errors: EINVAL (null), EUNSUPPORTED.
+ */
+int splitkv_workspace_size(const splitkv_problem* prob, size_t* plan_bytes, size_t* work_bytes);
+
+/*
+ * splitkv_plan — build the work plan on the device (no host synchronisation).
+ *   Validates the device metadata (latched as SPLITKV_EMETA / ECAPACITY),
+ *   prices every forward item (sample s, chunk c, slab of draft blocks, kv
+ *   head) and backward item (sample, 128-key tile, kv head) by
+ *       cost = sum over anchors a_j > start of min(len, a_j - start) * B
+ *   (the chunk's realized masked work, Split-KV abstract), drops cost-0
+ *   items, sorts by (cost desc, item id asc) and assigns greedily to the
+ *   least-loaded worker (ties: lowest worker id) — LPT as the rit.work
+ *   article describes it. The plan depends only on the metadata; one plan
+ *   serves every layer that shares the mask.
+ *   plan_ws: device buffer of at least plan_bytes (splitkv_workspace_size).
+ * Errors: EINVAL, EUNSUPPORTED, EWORKSPACE, EDEVICE, ECUDA.
+ */
+int splitkv_plan(const splitkv_problem* prob, void* plan_ws, size_t plan_bytes,
+                 splitkv_stream stream);
+
+/*
+ * splitkv_fwd — forward pass. Writes O (dtype) and LSE (fp32, natural log).
+ *   Persistent CTAs walk their LPT queues; each item computes the online-
+ *   softmax partial (lse, O) of 128 query rows over one KV chunk ("local
+ *   part", rit.work article, Split-KV section); a merge kernel then adds the
+ *   draft-block partial and combines all partials of a row exactly by
+ *   log-sum-exp in ascending chunk order ("reconcile the normalisation").
+ *   work: device buffer of at least work_bytes. prob must be the problem the
+ *   plan was built for (checked on the device -> SPLITKV_EPLAN).
+ * Errors: EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA.
+ */
+int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws,
+                const void* Q, const void* Kc, const void* Vc, const void* Kd, const void* Vd,
+                void* O, float* LSE, void* work, size_t work_bytes, splitkv_stream stream);
+
+/*
+ * splitkv_bwd — backward pass of loss = sum(dO * O).
+ *   Inputs are the forward's inputs plus its outputs O and LSE and the
+ *   upstream gradient dO. Writes dQ, dKc, dVc, dKd, dVd (dtype; every row is
+ *   written, context rows no block sees get zero). dK/dV of a context key
+ *   are produced by the one CTA that owns its 128-key tile (kept local, as
+ *   the rit.work article's Split-KV section keeps K/V gradients with their
+ *   shard); dQ is produced per (chunk, item) as an fp32 partial and reduced
+ *   in ascending chunk order (deterministic, no atomics).
+ * Errors: EINVAL, EUNSUPPORTED, EWORKSPACE, ECUDA.
+ */
+int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws,
+                const void* Q, const void* Kc, const void* Vc, const void* Kd, const void* Vd,
+                const void* O, const float* LSE, const void* dO,
+                void* dQ, void* dKc, void* dVc, void* dKd, void* dVd,
+                void* work, size_t work_bytes, splitkv_stream stream);
+
+/*
+ * splitkv_plan_stats — SYNCHRONISES `stream`, then reads the plan back and
+ *   fills *out: item counts, LPT and contiguous per-worker imbalance, skip
+ *   accounting and the latched device status.
+ * Errors: EINVAL, ECUDA.
+ */
+int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv_stats* out,
+                       splitkv_stream stream);
+
+/*
+ * splitkv_plan_export — SYNCHRONISES `stream` and copies the LPT result to
+ *   host arrays, for verification against an independent implementation.
+ *   kind: 0 = forward items, 1 = backward items. For every item of positive
+ *   cost, in LPT order (cost desc, id asc), writes
+ *     ids[i]    per-kv-head item id (forward: ((sample, chunk, slab) index) *
+ *               Hkv + kv head; backward: ((sample, key tile) index) * Hkv + kv head)
+ *     costs[i]  its cost
+ *     worker[i] the persistent CTA it is assigned to
+ *     pos[i]    its position in that CTA's queue
+ *   capacity: length of each host array; *count receives the item count
+ *   (nothing is written past capacity).
+ * Errors: EINVAL, ECUDA.
+ */
+int splitkv_plan_export(const splitkv_problem* prob, const void* plan_ws, int kind,
+                        int64_t* ids, int64_t* costs, int32_t* worker, int32_t* pos,
+                        int64_t capacity, int64_t* count, splitkv_stream stream);
+
+/* splitkv_device_status — SYNCHRONISES `stream`; *status = latched device status. */
+int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int* status,
+                          splitkv_stream stream);
+
+/* splitkv_resolve_workers — the persistent-CTA count a plan for `prob` uses
+ * on the current device (host-only apart from a device attribute query). */
+int splitkv_resolve_workers(const splitkv_problem* prob, int* workers);
+
+/* Static description of a status code (never NULL). */
+const char* splitkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_H */

@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def _ensure_library():
+    """Builds libsplitkv.so in-tree if it is missing or older than its sources."""
+    import importlib.util
+    path = os.path.join(ROOT, "block_sparse_cross_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("skv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+_ensure_library()
