@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Throughput of the split-KV hot path on GB300: one step = plan + forward +
+backward of anchor-masked block-sparse cross-attention over one batch.
+
+Metric: useful (masked) fwd+bwd TFLOP/s, FLOP = Hq * d * 14 * sum_j B*(a_j+B)
+(4 forward + 10 backward per (query, key) pair per head and dim, the draft
+self-block included), also as % of the dense bf16 tensor peak, plus the
+planned LPT imbalance against naive contiguous assignment.
+
+Default workload: config 2 (one sample, L = 65536 keys, prompt 8192,
+256 anchors x B = 16 = 4096 draft queries, Hq 32 / Hkv 8, d 128, chunk
+2048, bf16, seeded N(0,1) inputs). K + V are 256 MiB > L2, so every step
+streams them from HBM.
+
+N > 1 GPUs (torchrun): every rank runs its own independent batch (weak
+scaling, no data-path collective); gloo is used only for the barrier and the
+max-over-ranks timing reduction.
+
+--impl reference times the float64 CPU oracle (oracle/) on the host cores,
+each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "useful masked cross-attn fwd+bwd TFLOP/s, % of bf16 TC peak; LPT imbalance"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# algorithmic FLOP per (context pair, head, dim) of each attention kernel
+KERNEL_FLOP_PER_PAIR_DIM = {"fwd_attention": 4, "bwd_dq": 6, "bwd_dkdv": 8}
+
+
+def workload_desc(w) -> str:
+    lens = np.diff(w.cu_ctx)
+    return (f"{w.name}: {w.num_samples} sample(s), L={'/'.join(map(str, lens[:8]))}, "
+            f"{w.total_anchors} anchors x B={w.B} = {w.n_q} queries, Hq={w.Hq}/Hkv={w.Hkv}, "
+            f"d={w.d}, chunk={w.chunk}")
+
+
+def context_pairs(w) -> int:
+    return int((w.B * w.anchors.astype(np.int64)).sum())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return FALLBACK_PEAK, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Dist:
+    def __init__(self):
+        self.rank, self.world, self.local = dist_env()
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def profile_traffic(kernel: str, source_sha: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_ncu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != source_sha:
+        return None
+    return float(m_b.group(1))
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "tc_common.cuh", "common.cuh", "layout.h"):
+        with open(os.path.join(ROOT, "block_sparse_cross_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_seconds(w, host, blocks):
+    import oracle.attention as OA
+    t0 = time.perf_counter()
+    OA.forward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"], blocks=blocks)
+    OA.backward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"], host["dO"],
+                blocks=blocks)
+    return time.perf_counter() - t0
+
+
+def sample_flop(w, blocks) -> int:
+    a = w.anchors[np.asarray(blocks, np.int64)].astype(np.int64)
+    return int(w.Hq * w.d * 14 * (w.B * (a + w.B)).sum())
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def calibrate_blocks(w, host, target_s: float, rng_seed: int):
+    """Seeded block sample whose oracle fwd+bwd takes about target_s."""
+    rng = np.random.default_rng(rng_seed)
+    order = rng.permutation(w.total_anchors)
+    cum = np.cumsum([sample_flop(w, [b]) for b in order])
+    n = 1
+    t = oracle_sample_seconds(w, host, order[:n])
+    for _ in range(4):
+        if 0.6 * target_s <= t <= 1.5 * target_s or (t < target_s and n == w.total_anchors):
+            break
+        rate = cum[n - 1] / max(t, 1e-6)            # oracle FLOP/s on this sample
+        n = int(np.clip(np.searchsorted(cum, rate * target_s, side="right"), 1, w.total_anchors))
+        t = oracle_sample_seconds(w, host, order[:n])
+    return np.sort(order[:n]), t
+
+
+def host_inputs(w, seed_offset=1):
+    t = W.tensors(w, seed_offset)
+    return {k: W.round_to_bf16(v) for k, v in t.items()}
+
+
+def run_reference(args, d: Dist):
+    if d.rank != 0:
+        return 0
+    w = W.config(args.config, args.sweep)
+    host = host_inputs(w)
+    budget = max(20.0, min(150.0, args.reference_budget_s))
+    per_step = budget / max(1, args.steps + args.warmup)
+    blocks, _ = calibrate_blocks(w, host, per_step, w.seed + 99)
+    for _ in range(args.warmup):
+        oracle_sample_seconds(w, host, blocks)
+    times = [oracle_sample_seconds(w, host, blocks) for _ in range(args.steps)]
+    flop = sample_flop(w, blocks)
+    v = flop / statistics.mean(times) / 1e12
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "sample": f"{len(blocks)} of {w.total_anchors} draft blocks, all {w.Hq} heads, fwd+bwd"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{len(blocks)} seeded draft blocks x {w.Hq} heads of {w.name}, float64 numpy fwd+bwd"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, d: Dist):
+    import torch
+    import block_sparse_cross_gb300 as S
+
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    w = W.config(args.config, args.sweep)
+    t32 = W.tensors(w, seed_offset=1 + d.rank)  # independent batch per rank
+    names_in = ("Q", "Kc", "Vc", "Kd", "Vd", "dO")
+    pinned = {k: torch.from_numpy(t32[k]).to(torch.bfloat16).pin_memory() for k in names_in}
+    del t32
+    gpu = {k: v.to(dev) for k, v in pinned.items()}
+    meta_host = [torch.from_numpy(a.astype(np.int32)).pin_memory()
+                 for a in (w.cu_ctx, w.cu_anchor, w.anchors)]
+    meta = [m.to(dev) for m in meta_host]
+    kv = S.SplitKV(*meta, w.total_ctx, w.total_anchors, w.max_ctx, w.B, w.Hq, w.Hkv, w.d,
+                   w.chunk, w.scale)
+    outs = {"O": torch.empty_like(gpu["Q"]), "LSE": torch.empty(w.Hq, w.n_q, device=dev),
+            "dQ": torch.empty_like(gpu["Q"]), "dKc": torch.empty_like(gpu["Kc"]),
+            "dVc": torch.empty_like(gpu["Vc"]), "dKd": torch.empty_like(gpu["Kd"]),
+            "dVd": torch.empty_like(gpu["Vd"])}
+    out_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+
+    def step():
+        kv.plan()
+        kv.forward(gpu["Q"], gpu["Kc"], gpu["Vc"], gpu["Kd"], gpu["Vd"], outs["O"], outs["LSE"])
+        kv.backward(gpu["Q"], gpu["Kc"], gpu["Vc"], gpu["Kd"], gpu["Vd"], outs["O"], outs["LSE"],
+                    gpu["dO"], outs["dQ"], outs["dKc"], outs["dVc"], outs["dKd"], outs["dVd"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if kv.device_status() != S.SPLITKV_OK:
+        raise RuntimeError("device status " + S.splitkv_status_string(kv.device_status()))
+    st = kv.stats()
+
+    # ---- device-timed region (inputs resident) ----
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(d.local)
+    sampler = ClockSampler(gpu_id)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    S.splitkv_profile_enable(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    S.splitkv_profile_enable(False)
+    clocks = sampler.stop()
+    d.barrier()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = d.max(ms_local)
+    pst, ktimes = S.splitkv_profile_read()
+
+    flop_step = w.useful_flop(14)
+    value = d.sum(flop_step) * args.steps / (ms * args.steps * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
+
+    # ---- per-kernel roofline from the live CUDA-event brackets ----
+    cp = context_pairs(w)
+    kernels = {}
+    for name, (launches, tot) in ktimes.items():
+        if launches == 0:
+            continue
+        per_launch = tot / launches if name != "plan" else tot / (launches / 3)
+        entry = {"launches": launches, "ms_total": tot, "ms_per_launch": per_launch}
+        if name in KERNEL_FLOP_PER_PAIR_DIM:
+            f = KERNEL_FLOP_PER_PAIR_DIM[name] * w.d * w.Hq * cp
+            entry["tflops"] = f / (per_launch * 1e-3) / 1e12
+        kernels[name] = entry
+    attn = {k: v for k, v in kernels.items() if k in KERNEL_FLOP_PER_PAIR_DIM}
+    dom = max(attn, key=lambda k: attn[k]["ms_total"])
+    sha = kernel_source_sha()
+    traffic = profile_traffic(dom, sha)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": attn[dom]["tflops"], "peak": peak,
+                "unit": "TFLOP/s", "frac": attn[dom]["tflops"] / peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                "flop_per_launch": KERNEL_FLOP_PER_PAIR_DIM[dom] * w.d * w.Hq * cp}
+    launches_total = sum(v["launches"] for v in kernels.values())
+    fwd_ms = sum(kernels.get(k, {}).get("ms_total", 0.0) for k in ("fwd_attention", "merge")) / args.steps
+    bwd_ms = sum(kernels.get(k, {}).get("ms_total", 0.0)
+                 for k in ("bwd_draft", "bwd_dq", "bwd_dkdv", "dq_reduce", "zero_uncovered")) / args.steps
+    plan_ms = kernels.get("plan", {}).get("ms_total", 0.0) / args.steps
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values()) + \
+            sum(m.numel() * m.element_size() for m in meta_host)
+        d2h = sum(v.numel() * v.element_size() for v in outs.values())
+        d.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            for k in names_in:
+                gpu[k].copy_(pinned[k], non_blocking=True)
+            for m, mh in zip(meta, meta_host):
+                m.copy_(mh, non_blocking=True)
+            step()
+            for k in outs:
+                out_host[k].copy_(outs[k], non_blocking=True)
+        torch.cuda.synchronize()
+        t_e2e = d.max(time.perf_counter() - t0)
+        e2e = {"value": d.sum(flop_step) * args.steps / t_e2e / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": 1e3 * t_e2e / args.steps}
+
+    # ---- CPU oracle baseline (rank 0, N = 1) ----
+    cpu = None
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        host = {k: v.float().numpy() for k, v in pinned.items()}
+        blocks, _ = calibrate_blocks(w, host, args.cpu_target_s, w.seed + 99)
+        t = oracle_sample_seconds(w, host, blocks)
+        cpu = {"value": sample_flop(w, blocks) / t / 1e12, "unit": UNIT,
+               "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{len(blocks)} seeded draft blocks x {w.Hq} heads of {w.name} "
+                         f"({t:.1f} s), float64 numpy fwd+bwd"}
+
+    if d.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": d.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(w), "global_batch": d.world * w.n_q,
+                       "seq_len": int(w.max_ctx), "parallelism": f"replicas x{d.world}",
+                       "l2": "inputs larger than L2 (K+V 256 MiB per step)"
+                             if args.config == 2 else "see workload",
+                       "step": "plan + forward + backward"},
+            "pct_of_peak": 100.0 * value / d.world / peak,
+            "lpt_imbalance": {"fwd": st.fwd_lpt_imbalance, "bwd": st.bwd_lpt_imbalance},
+            "contiguous_imbalance": {"fwd": st.fwd_contig_imbalance, "bwd": st.bwd_contig_imbalance},
+            "skip_rate": 1.0 - st.fwd_tiles / max(1, st.dense_tiles),
+            "phase_ms": {"plan": plan_ms, "fwd": fwd_ms, "bwd": bwd_ms},
+            "phase_tflops": {"fwd": w.useful_flop(4) / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
+                             "bwd": w.useful_flop(10) / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None},
+            "kernels": kernels,
+            "roofline": roofline,
+            "gpu_launches": launches_total,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--sweep", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-target-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    d = Dist()
+    try:
+        rc = run_reference(args, d) if args.impl == "reference" else run_ours(args, d)
+    finally:
+        d.close()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

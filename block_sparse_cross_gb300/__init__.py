@@ -42,6 +42,9 @@ SPLITKV_BF16 = 0
 SPLITKV_FP32 = 1
 SPLITKV_FLAG_CUDA_CORE = 1
 SPLITKV_FLAG_CONTIGUOUS = 2
+SPLITKV_NUM_KERNELS = 8
+(SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,
+ SPLITKV_K_BWD_DKDV, SPLITKV_K_DQ_REDUCE, SPLITKV_K_ZERO) = range(8)
 
 
 class splitkv_problem(ctypes.Structure):
@@ -106,6 +109,9 @@ _SIGS = {
     "splitkv_device_status": ([_P, _vp, ctypes.POINTER(ctypes.c_int), _vp], ctypes.c_int),
     "splitkv_resolve_workers": ([_P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "splitkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "splitkv_profile_enable": ([ctypes.c_int], ctypes.c_int),
+    "splitkv_profile_read": ([_vp, _vp, ctypes.c_int], ctypes.c_int),
+    "splitkv_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -151,6 +157,24 @@ def _check(where: str, st: int) -> None:
 # ---- same-name wrappers ----------------------------------------------------
 def splitkv_status_string(status: int) -> str:
     return _lib.splitkv_status_string(int(status)).decode()
+
+
+def splitkv_kernel_name(kernel_id: int) -> str:
+    return _lib.splitkv_kernel_name(int(kernel_id)).decode()
+
+
+def splitkv_profile_enable(on: bool) -> int:
+    return _lib.splitkv_profile_enable(1 if on else 0)
+
+
+def splitkv_profile_read():
+    """Returns (status, {kernel name: (launches, total_ms)})."""
+    import numpy as np
+    n = SPLITKV_NUM_KERNELS
+    launches = np.zeros(n, np.int32)
+    ms = np.zeros(n, np.float64)
+    st = _lib.splitkv_profile_read(launches.ctypes.data, ms.ctypes.data, n)
+    return st, {splitkv_kernel_name(i): (int(launches[i]), float(ms[i])) for i in range(n)}
 
 
 def splitkv_workspace_size(prob: splitkv_problem):

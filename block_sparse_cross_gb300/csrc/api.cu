@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "kernels.h"
@@ -155,9 +156,87 @@ bool use_tensor_cores(const ProbDev& P) {
   return P.dtype == SPLITKV_BF16 && !(P.flags & SPLITKV_FLAG_CUDA_CORE);
 }
 
+// ---- launch timing --------------------------------------------------------
+struct ProfRec {
+  int kernel, launches;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void prof_clear() {
+  for (auto& r : g_prof_recs) {
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+}
+
+// Runs a launcher; when timing is on, brackets it with events on `st`.
+template <typename F>
+cudaError_t timed(int kernel, int launches, cudaStream_t st, F&& f) {
+  std::unique_lock<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) {
+    lk.unlock();
+    return f();
+  }
+  cudaEvent_t a = prof_event(), b = prof_event();
+  cudaEventRecord(a, st);
+  const cudaError_t e = f();
+  cudaEventRecord(b, st);
+  g_prof_recs.push_back({kernel, launches, a, b});
+  return e;
+}
+
 }  // namespace
 
 extern "C" {
+
+int splitkv_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on) prof_clear();
+  g_prof_on = on != 0;
+  return SPLITKV_OK;
+}
+
+int splitkv_profile_read(int32_t* launches, double* total_ms, int n) {
+  if (!launches || !total_ms || n < 0) return SPLITKV_EINVAL;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < n; ++i) {
+    launches[i] = 0;
+    total_ms[i] = 0.0;
+  }
+  for (const auto& r : g_prof_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return SPLITKV_ECUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return SPLITKV_ECUDA;
+    if (r.kernel < n) {
+      launches[r.kernel] += r.launches;
+      total_ms[r.kernel] += ms;
+    }
+  }
+  return SPLITKV_OK;
+}
+
+const char* splitkv_kernel_name(int kernel_id) {
+  static const char* names[SPLITKV_NUM_KERNELS] = {
+      "plan", "fwd_attention", "merge", "bwd_draft", "bwd_dq", "bwd_dkdv", "dq_reduce",
+      "zero_uncovered"};
+  return (kernel_id >= 0 && kernel_id < SPLITKV_NUM_KERNELS) ? names[kernel_id] : "unknown";
+}
 
 int splitkv_workspace_size(const splitkv_problem* prob, size_t* plan_bytes, size_t* work_bytes) {
   const int st = check_problem(prob);
@@ -181,7 +260,8 @@ int splitkv_plan(const splitkv_problem* prob, void* plan_ws, size_t plan_bytes,
   int st = setup(prob, plan_ws, &c);
   if (st) return st;
   if (plan_bytes < plan_bytes_for(prob)) return SPLITKV_EWORKSPACE;
-  return cuda_status(launch_plan(c.P, c.pp, c.caps, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  return cuda_status(timed(SPLITKV_K_PLAN, 3, s, [&] { return launch_plan(c.P, c.pp, c.caps, s); }));
 }
 
 int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q, const void* Kc,
@@ -201,10 +281,13 @@ int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   WorkPtrs wk;
   work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = use_tensor_cores(c.P) ? launch_fwd_tc(c.P, c.pp, wk, Q, Kc, Vc, s)
-                                        : launch_fwd_simt(c.P, c.pp, wk, Q, Kc, Vc, s);
+  cudaError_t e = timed(SPLITKV_K_FWD_ATTN, 1, s, [&] {
+    return use_tensor_cores(c.P) ? launch_fwd_tc(c.P, c.pp, wk, Q, Kc, Vc, s)
+                                 : launch_fwd_simt(c.P, c.pp, wk, Q, Kc, Vc, s);
+  });
   if (e != cudaSuccess) return SPLITKV_ECUDA;
-  return cuda_status(launch_merge(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, s));
+  return cuda_status(
+      timed(SPLITKV_K_MERGE, 1, s, [&] { return launch_merge(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, s); }));
 }
 
 int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q, const void* Kc,
@@ -225,24 +308,31 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
   if (prob->total_ctx > 0) {
-    e = launch_zero_uncovered(c.P, c.pp, dKc, dVc, s);
+    e = timed(SPLITKV_K_ZERO, 1, s, [&] { return launch_zero_uncovered(c.P, c.pp, dKc, dVc, s); });
     if (e != cudaSuccess) return SPLITKV_ECUDA;
   }
   if (!any_q) return SPLITKV_OK;
   WorkPtrs wk;
   work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
-  e = launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, s);
+  e = timed(SPLITKV_K_BWD_DRAFT, 1, s, [&] {
+    return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, s);
+  });
   if (e != cudaSuccess) return SPLITKV_ECUDA;
   const bool tc = use_tensor_cores(c.P);
-  e = tc ? launch_bwd_dq_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s)
-         : launch_bwd_dq_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s);
+  e = timed(SPLITKV_K_BWD_DQ, 1, s, [&] {
+    return tc ? launch_bwd_dq_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s)
+              : launch_bwd_dq_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s);
+  });
   if (e != cudaSuccess) return SPLITKV_ECUDA;
   if (prob->total_ctx > 0) {
-    e = tc ? launch_bwd_dkdv_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s)
-           : launch_bwd_dkdv_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s);
+    e = timed(SPLITKV_K_BWD_DKDV, 1, s, [&] {
+      return tc ? launch_bwd_dkdv_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s)
+                : launch_bwd_dkdv_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s);
+    });
     if (e != cudaSuccess) return SPLITKV_ECUDA;
   }
-  return cuda_status(launch_dq_reduce(c.P, c.pp, wk, dQ, s));
+  return cuda_status(
+      timed(SPLITKV_K_DQ_REDUCE, 1, s, [&] { return launch_dq_reduce(c.P, c.pp, wk, dQ, s); }));
 }
 
 int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int* status,

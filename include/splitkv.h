@@ -255,6 +255,32 @@ int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int*
  * on the current device (host-only apart from a device attribute query). */
 int splitkv_resolve_workers(const splitkv_problem* prob, int* workers);
 
+/*
+ * Launch timing (the library's tracing hook; not thread-safe).
+ * splitkv_profile_enable(1) clears earlier records and from then on brackets
+ * every kernel launch the library makes with a pair of CUDA events recorded
+ * on the launch stream (no synchronisation is added). splitkv_profile_enable(0)
+ * stops recording. splitkv_profile_read() waits for the recorded events and
+ * returns, per kernel family id (SPLITKV_K_*), the number of kernel launches
+ * and their summed device time in milliseconds; arrays have length n (at
+ * most SPLITKV_NUM_KERNELS entries are written). Errors: EINVAL, ECUDA.
+ */
+enum {
+  SPLITKV_K_PLAN = 0,        /* planner: setup, rank, assign (3 launches) */
+  SPLITKV_K_FWD_ATTN = 1,    /* forward partial attention (persistent) */
+  SPLITKV_K_MERGE = 2,       /* draft partial + log-sum-exp merge */
+  SPLITKV_K_BWD_DRAFT = 3,   /* D = rowsum(dO*O) + draft-block backward */
+  SPLITKV_K_BWD_DQ = 4,      /* dQ chunk partials (persistent) */
+  SPLITKV_K_BWD_DKDV = 5,    /* dK/dV of 128-key tiles (persistent) */
+  SPLITKV_K_DQ_REDUCE = 6,   /* dQ = scale * sum of partials */
+  SPLITKV_K_ZERO = 7,        /* zero dK/dV rows no block sees */
+  SPLITKV_NUM_KERNELS = 8
+};
+int splitkv_profile_enable(int on);
+int splitkv_profile_read(int32_t* launches, double* total_ms, int n);
+/* Name of a kernel family id (never NULL). */
+const char* splitkv_kernel_name(int kernel_id);
+
 /* Static description of a status code (never NULL). */
 const char* splitkv_status_string(int status);
 
