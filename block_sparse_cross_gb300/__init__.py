@@ -43,6 +43,7 @@ SPLITKV_FP32 = 1
 SPLITKV_FLAG_CUDA_CORE = 1
 SPLITKV_FLAG_CONTIGUOUS = 2
 SPLITKV_NUM_KERNELS = 8
+SPLITKV_NOALLOC_SCRATCH_BYTES = 64 << 20
 (SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,
  SPLITKV_K_BWD_DKDV, SPLITKV_K_DQ_REDUCE, SPLITKV_K_ZERO) = range(8)
 
@@ -109,6 +110,7 @@ _SIGS = {
     "splitkv_device_status": ([_P, _vp, ctypes.POINTER(ctypes.c_int), _vp], ctypes.c_int),
     "splitkv_resolve_workers": ([_P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "splitkv_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "splitkv_fwd_noalloc": ([_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "splitkv_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "splitkv_profile_read": ([_vp, _vp, ctypes.c_int], ctypes.c_int),
     "splitkv_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
@@ -199,6 +201,12 @@ def splitkv_fwd(prob, plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE, work, work_bytes: int,
     return _lib.splitkv_fwd(ctypes.byref(prob), _ptr(plan_ws), _ptr(Q), _ptr(Kc), _ptr(Vc),
                             _ptr(Kd), _ptr(Vd), _ptr(O), _ptr(LSE), _ptr(work), work_bytes,
                             _stream(stream))
+
+
+def splitkv_fwd_noalloc(prob, Q, Kc, Vc, Kd, Vd, O, LSE, stream=None) -> int:
+    """Forward without caller workspaces (fixed per-device scratch array)."""
+    return _lib.splitkv_fwd_noalloc(ctypes.byref(prob), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(Kd),
+                                    _ptr(Vd), _ptr(O), _ptr(LSE), _stream(stream))
 
 
 def splitkv_bwd(prob, plan_ws, Q, Kc, Vc, Kd, Vd, O, LSE, dO, dQ, dKc, dVc, dKd, dVd, work,

@@ -256,6 +256,35 @@ int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int*
 int splitkv_resolve_workers(const splitkv_problem* prob, int* workers);
 
 /*
+ * splitkv_fwd_noalloc — the forward pass (plan + splitkv_fwd) for callers
+ *   that cannot allocate device memory where they call it: code running in
+ *   another framework's per-call hook where that framework owns all device
+ *   memory and forbids allocation, or services that freeze device allocation
+ *   after start-up. The paper has no counterpart; this entry point exists
+ *   only for such callers.
+ *   Same problem description and the same device tensors as splitkv_fwd
+ *   (inputs Q, Kc, Vc, Kd, Vd; outputs O, LSE); no workspaces. The plan and
+ *   the forward partials live in one file-scope device array of
+ *   SPLITKV_NOALLOC_SCRATCH_BYTES per device, reserved when the library's
+ *   device code is loaded and held until the process exits. The library
+ *   calls no cudaMalloc / cudaFree and no allocating routine here.
+ *   The first call on a device looks up that array's device address
+ *   (cudaGetSymbolAddress) with the device current; make that first call
+ *   before any stream capture.
+ *   Limit: problems whose splitkv_workspace_size() plan_bytes (rounded up to
+ *   256) + work_bytes exceed SPLITKV_NOALLOC_SCRATCH_BYTES return
+ *   SPLITKV_EWORKSPACE; use splitkv_plan + splitkv_fwd with your own
+ *   workspaces for them.
+ *   Every call on a device shares the array and leaves its contents behind;
+ *   calls whose work overlaps on the GPU (e.g. on two streams) race on it.
+ *   Order them on one stream. Errors: as splitkv_plan and splitkv_fwd.
+ */
+#define SPLITKV_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int splitkv_fwd_noalloc(const splitkv_problem* prob, const void* Q, const void* Kc,
+                        const void* Vc, const void* Kd, const void* Vd, void* O, float* LSE,
+                        splitkv_stream stream);
+
+/*
  * Launch timing (the library's tracing hook; not thread-safe).
  * splitkv_profile_enable(1) clears earlier records and from then on brackets
  * every kernel launch the library makes with a pair of CUDA events recorded
