@@ -125,7 +125,8 @@ size_t plan_bytes_for(const splitkv_problem* p) {
 
 size_t work_bytes_for(const splitkv_problem* p) {
   const PlanCaps c = caps_of(p, kMaxWorkers);
-  return work_layout(c.NCF * p->Hkv, p->total_anchors * p->B, p->Hq, p->d, nullptr, nullptr);
+  return work_layout(c.NCF * p->Hkv, p->total_anchors * p->B, p->Hq, p->d, p->B, nullptr,
+                     nullptr);
 }
 
 struct Ctx {
@@ -279,7 +280,7 @@ int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   if (work_bytes < work_bytes_for(prob)) return SPLITKV_EWORKSPACE;
   if (!any_q) return SPLITKV_OK;
   WorkPtrs wk;
-  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B, (char*)work, &wk);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = timed(SPLITKV_K_FWD_ATTN, 1, s, [&] {
     return use_tensor_cores(c.P) ? launch_fwd_tc(c.P, c.pp, wk, Q, Kc, Vc, s)
@@ -313,7 +314,7 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   }
   if (!any_q) return SPLITKV_OK;
   WorkPtrs wk;
-  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, (char*)work, &wk);
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B, (char*)work, &wk);
   e = timed(SPLITKV_K_BWD_DRAFT, 1, s, [&] {
     return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, s);
   });
@@ -392,7 +393,7 @@ int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv
   out->fwd_tiles = h.fwd_tiles * Hkv;
   out->dense_tiles = h.dense_tiles * Hkv;
   out->work_bytes_used =
-      work_layout(out->fwd_slots, c.P.NQ, prob->Hq, prob->d, nullptr, nullptr);
+      work_layout(out->fwd_slots, c.P.NQ, prob->Hq, prob->d, prob->B, nullptr, nullptr);
   return SPLITKV_OK;
 }
 

@@ -74,13 +74,19 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // ===========================================================================
 // Forward
 // ===========================================================================
+// K and V tiles sit in separate rings: a K tile is released as soon as the
+// S MMA that reads it completes, long before the PV MMA releases its V tile,
+// so K loads run further ahead of the MMAs than a shared K+V stage allows.
+constexpr int kFwdNK = 3, kFwdNV = 3;
+
 template <int D>
 struct FwdLayout {
   static constexpr int kSub = D / 64;
+  static constexpr uint32_t tile = kSub * kSubBytes;  // one 128 x D bf16 tile
   static constexpr uint32_t q = 0;
-  static constexpr uint32_t stage0 = kSub * kSubBytes;
-  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes;  // K then V
-  static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
+  static constexpr uint32_t k0 = tile;
+  static constexpr uint32_t v0 = k0 + kFwdNK * tile;
+  static constexpr uint32_t bars = v0 + kFwdNV * tile;
   static constexpr uint32_t total = bars + 512 + 1024;  // + alignment slack
 };
 
@@ -95,10 +101,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + kNS;
-  uint64_t* kv_empty = v_full + kNS;
-  uint64_t* s_full = kv_empty + kNS;  // [2]
+  uint64_t* k_full = bars + 2;         // [kFwdNK]
+  uint64_t* k_empty = k_full + kFwdNK;
+  uint64_t* v_full = k_empty + kFwdNK; // [kFwdNV]
+  uint64_t* v_empty = v_full + kFwdNV;
+  uint64_t* s_full = v_empty + kFwdNV;  // [2]
   uint64_t* p_ready = s_full + 2;     // [2]
   uint64_t* pv_done = p_ready + 2;
   uint64_t* o_free = pv_done + 1;
@@ -111,10 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kFwdNK; ++s) {
       mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < kFwdNV; ++s) {
       mbar_init(v_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+      mbar_init(v_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full + b, 1);
@@ -138,39 +148,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producers: lane 0 Q and K, lane 1 V ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t nq = 0, nkv = 0;
+      uint32_t nq = 0, nk = 0;
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, kSub * kSubBytes);
+        mbar_expect_tx(q_full, Lay::tile);
         for (int i = 0; i < kSub; ++i)
           tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
-          const uint32_t s = nkv % kNS, u = nkv / kNS;
-          if (u > 0 && !(ok = mbar_wait(kv_empty + s, (u - 1) & 1, abort_flag))) break;
-          uint8_t* kb = smem + Lay::stage0 + s * Lay::stage_bytes;
-          uint8_t* vb = kb + kSub * kSubBytes;
-          const int row = I.row0 + t * kKeyTile;
-          mbar_expect_tx(k_full + s, kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i) tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, row);
-          mbar_expect_tx(v_full + s, kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i) tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, row);
-          ++nkv;
+          const uint32_t s = nk % kFwdNK, u = nk / kFwdNK;
+          if (u > 0 && !(ok = mbar_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
+          mbar_expect_tx(k_full + s, Lay::tile);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          ++nk;
         }
       }
       if (!ok) {  // let every copy in flight land before the CTA exits
         if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, kDrainNs);
-        for (uint32_t j = nkv > (uint32_t)kNS ? nkv - kNS : 0; j < nkv; ++j) {
-          mbar_wait_drain(k_full + j % kNS, (j / kNS) & 1, kDrainNs);
-          mbar_wait_drain(v_full + j % kNS, (j / kNS) & 1, kDrainNs);
+        for (uint32_t j = nk > (uint32_t)kFwdNK ? nk - kFwdNK : 0; j < nk; ++j)
+          mbar_wait_drain(k_full + j % kFwdNK, (j / kFwdNK) & 1, kDrainNs);
+      }
+    } else if (lane == 1) {
+      tma_prefetch_desc(&tmV);
+      uint32_t nv = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        for (int t = 0; t < I.ntiles; ++t) {
+          const uint32_t s = nv % kFwdNV, u = nv / kFwdNV;
+          if (u > 0 && !(ok = mbar_wait(v_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
+          mbar_expect_tx(v_full + s, Lay::tile);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          ++nv;
         }
+      }
+      if (!ok) {
+        for (uint32_t j = nv > (uint32_t)kFwdNV ? nv - kFwdNV : 0; j < nv; ++j)
+          mbar_wait_drain(v_full + j % kFwdNV, (j / kFwdNV) & 1, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -179,24 +203,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(smem + Lay::q);
-      uint32_t nkv = 0, ns = 0, nit = 0;
+      uint32_t ns = 0, nit = 0;  // ns: tiles issued (S buffer, K and V ring index)
       bool ok = true;
       bool pend = false, pend_first = false;
-      uint32_t pend_s = 0, pend_stage = 0, pend_par = 0, pend_item = 0;
+      uint32_t pend_s = 0, pend_item = 0;
       auto issue_pv = [&]() -> bool {
         const uint32_t sb = pend_s & 1;
+        const uint32_t vs = pend_s % kFwdNV;
         if (!mbar_wait(p_ready + sb, (pend_s >> 1) & 1, abort_flag)) return false;
         if (pend_first && pend_item > 0 && !mbar_wait(o_free, (pend_item - 1) & 1, abort_flag))
           return false;
-        if (!mbar_wait(v_full + pend_stage, pend_par, abort_flag)) return false;
+        if (!mbar_wait(v_full + vs, (pend_s / kFwdNV) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t v_addr =
-            smem_u32(smem + Lay::stage0 + pend_stage * Lay::stage_bytes + kSub * kSubBytes);
+        const uint32_t v_addr = smem_u32(smem + Lay::v0 + vs * Lay::tile);
 #pragma unroll
         for (int kk = 0; kk < kKeyTile / 16; ++kk)
           mma_ts(tO, tS + sb * 128 + kk * 8, desc_mnmajor(v_addr, kk), kIdPV,
                  (pend_first && kk == 0) ? 0u : 1u);
-        mma_commit(kv_empty + pend_stage);
+        mma_commit(v_empty + vs);
         mma_commit(pv_done);
         return true;
       };
@@ -204,23 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
         tc_fence_after();
-        for (int t = 0; t < I.ntiles; ++t, ++nkv, ++ns) {
-          const uint32_t s = nkv % kNS, par = (nkv / kNS) & 1;
-          if (!(ok = mbar_wait(k_full + s, par, abort_flag))) break;
+        for (int t = 0; t < I.ntiles; ++t, ++ns) {
+          const uint32_t ks = ns % kFwdNK;
+          if (!(ok = mbar_wait(k_full + ks, (ns / kFwdNK) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
+          const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
           const uint32_t sb = ns & 1;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tS + sb * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
                    kk > 0 ? 1u : 0u);
           mma_commit(s_full + sb);
+          mma_commit(k_empty + ks);
           if (t == I.ntiles - 1) mma_commit(q_empty);
           if (pend && !(ok = issue_pv())) break;
           pend = true;
           pend_s = ns;
-          pend_stage = s;
-          pend_par = par;
           pend_first = (t == 0);
           pend_item = nit;
         }
@@ -339,14 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // dQ (same items as the forward)
 // ===========================================================================
+// K is read by S (early) and by dQ (late) of its tile, V only by dP: a ring
+// of three K tiles and a ring of two V tiles, each released after its last
+// reader.
+constexpr int kDqNK = 3, kDqNV = 2;
+
 template <int D>
 struct DqLayout {
   static constexpr int kSub = D / 64;
+  static constexpr uint32_t tile = kSub * kSubBytes;
   static constexpr uint32_t q = 0;
-  static constexpr uint32_t dO = kSub * kSubBytes;
-  static constexpr uint32_t stage0 = 2 * kSub * kSubBytes;
-  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes;  // K then V
-  static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
+  static constexpr uint32_t dO = tile;
+  static constexpr uint32_t k0 = 2 * tile;
+  static constexpr uint32_t v0 = k0 + kDqNK * tile;
+  static constexpr uint32_t bars = v0 + kDqNV * tile;
   static constexpr uint32_t total = bars + 512 + 1024;
 };
 
@@ -362,11 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + kNS;
-  uint64_t* kv_empty = v_full + kNS;
-  uint64_t* dp_full = kv_empty + kNS;
-  uint64_t* p_ready = dp_full + 1;
+  uint64_t* k_full = bars + 2;          // [kDqNK]
+  uint64_t* k_empty = k_full + kDqNK;
+  uint64_t* v_full = k_empty + kDqNK;   // [kDqNV]
+  uint64_t* v_empty = v_full + kDqNV;
+  uint64_t* s_full = v_empty + kDqNV;   // [2] S of tile t is in TMEM (alternating)
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* p_ready = dp_full + 1;     // softmax wrote dS (bf16) over S
   uint64_t* dq_done = p_ready + 1;
   uint64_t* dq_free = dq_done + 1;
   uint64_t* mma_drain = dq_free + 1;
@@ -378,11 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kDqNK; ++s) {
       mbar_init(k_full + s, 1);
-      mbar_init(v_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+      mbar_init(k_empty + s, 1);
     }
+    for (int s = 0; s < kDqNV; ++s) {
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_full + 1, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 4);
     mbar_init(dq_done, 1);
@@ -403,41 +439,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
+    // ---------------- TMA producers: lane 0 Q, dO and K, lane 1 V ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t nq = 0, nkv = 0;
+      uint32_t nq = 0, nk = 0;
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, 2 * kSub * kSubBytes);
+        mbar_expect_tx(q_full, 2 * Lay::tile);
         for (int i = 0; i < kSub; ++i) {
           tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
           tma_load_3d(smem + Lay::dO + i * kSubBytes, &tmdO, q_full, 64 * i, I.g * P.group, I.n0);
         }
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
-          const uint32_t s = nkv % kNS, u = nkv / kNS;
-          if (u > 0 && !(ok = mbar_wait(kv_empty + s, (u - 1) & 1, abort_flag))) break;
-          uint8_t* kb = smem + Lay::stage0 + s * Lay::stage_bytes;
-          uint8_t* vb = kb + kSub * kSubBytes;
-          const int row = I.row0 + t * kKeyTile;
-          mbar_expect_tx(k_full + s, kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i) tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, row);
-          mbar_expect_tx(v_full + s, kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i) tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, row);
-          ++nkv;
+          const uint32_t s = nk % kDqNK, u = nk / kDqNK;
+          if (u > 0 && !(ok = mbar_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
+          mbar_expect_tx(k_full + s, Lay::tile);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          ++nk;
         }
       }
       if (!ok) {
         if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, kDrainNs);
-        for (uint32_t j = nkv > (uint32_t)kNS ? nkv - kNS : 0; j < nkv; ++j) {
-          mbar_wait_drain(k_full + j % kNS, (j / kNS) & 1, kDrainNs);
-          mbar_wait_drain(v_full + j % kNS, (j / kNS) & 1, kDrainNs);
+        for (uint32_t j = nk > (uint32_t)kDqNK ? nk - kDqNK : 0; j < nk; ++j)
+          mbar_wait_drain(k_full + j % kDqNK, (j / kDqNK) & 1, kDrainNs);
+      }
+    } else if (lane == 1) {
+      tma_prefetch_desc(&tmV);
+      uint32_t nv = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        for (int t = 0; t < I.ntiles; ++t) {
+          const uint32_t s = nv % kDqNV, u = nv / kDqNV;
+          if (u > 0 && !(ok = mbar_wait(v_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
+          mbar_expect_tx(v_full + s, Lay::tile);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          ++nv;
         }
+      }
+      if (!ok) {
+        for (uint32_t j = nv > (uint32_t)kDqNV ? nv - kDqNV : 0; j < nv; ++j)
+          mbar_wait_drain(v_full + j % kDqNV, (j / kDqNV) & 1, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -446,22 +497,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(smem + Lay::q);
       const uint32_t do_addr = smem_u32(smem + Lay::dO);
-      uint32_t nkv = 0, gt = 0, nit = 0;
+      uint32_t gt = 0, nit = 0;  // gt: tiles issued (TMEM region, K and V ring index)
       bool ok = true;
       bool pend = false, pend_first = false, pend_last = false;
-      uint32_t pend_t = 0, pend_stage = 0, pend_item = 0;
+      uint32_t pend_t = 0, pend_item = 0;
       auto issue_dq = [&]() -> bool {
         if (!mbar_wait(p_ready, pend_t & 1, abort_flag)) return false;
         if (pend_first && pend_item > 0 && !mbar_wait(dq_free, (pend_item - 1) & 1, abort_flag))
           return false;
         tc_fence_after();
         const uint32_t rS = (2 * pend_t) % 3;
-        const uint32_t k_addr = smem_u32(smem + Lay::stage0 + pend_stage * Lay::stage_bytes);
+        const uint32_t ks = pend_t % kDqNK;
+        const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
 #pragma unroll
         for (int kk = 0; kk < kKeyTile / 16; ++kk)
           mma_ts(tdQ, tmem + rS * 128 + kk * 8, desc_mnmajor(k_addr, kk), kIdQ,
                  (pend_first && kk == 0) ? 0u : 1u);
-        mma_commit(kv_empty + pend_stage);
+        mma_commit(k_empty + ks);
         if (pend_last) mma_commit(dq_done);
         return true;
       };
@@ -469,28 +521,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
         tc_fence_after();
-        for (int t = 0; t < I.ntiles; ++t, ++nkv, ++gt) {
-          const uint32_t s = nkv % kNS, par = (nkv / kNS) & 1;
-          if (!(ok = mbar_wait(k_full + s, par, abort_flag))) break;
-          if (!(ok = mbar_wait(v_full + s, par, abort_flag))) break;
+        for (int t = 0; t < I.ntiles; ++t, ++gt) {
+          const uint32_t ks = gt % kDqNK, vs = gt % kDqNV;
+          if (!(ok = mbar_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
-          const uint32_t v_addr = k_addr + kSub * kSubBytes;
+          const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
+          const uint32_t v_addr = smem_u32(smem + Lay::v0 + vs * Lay::tile);
           const uint32_t rS = (2 * gt) % 3, rP = (2 * gt + 1) % 3;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + rS * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
                    kk > 0 ? 1u : 0u);
+          mma_commit(s_full + (gt & 1));
           if (pend && !(ok = issue_dq())) break;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + rP * 128, desc_kmajor(do_addr, kk), desc_kmajor(v_addr, kk), kIdS,
                    kk > 0 ? 1u : 0u);
           mma_commit(dp_full);
+          mma_commit(v_empty + vs);
           if (t == I.ntiles - 1) mma_commit(q_empty);
           pend = true;
           pend_t = gt;
-          pend_stage = s;
           pend_first = (t == 0);
           pend_last = (t == I.ntiles - 1);
           pend_item = nit;
@@ -516,27 +569,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         Dr = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
       }
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
-        if (!(ok = warp_wait(dp_full, gt & 1, abort_flag))) break;
+        if (!(ok = warp_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const int lim = min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
         const uint32_t sa = tmem + lane_base + ((2 * gt) % 3) * 128;
         const uint32_t pa = tmem + lane_base + ((2 * gt + 1) % 3) * 128;
+        // phase 1 (while dQ of the previous tile and dP of this one run):
+        // P = exp(S * scale - LSE) on the row's visible keys
+        float p[128];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t sv[32];
+          tmem_ld32(sa + 32 * j, sv);
+          tmem_ld_wait(sv);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            p[32 * j + i] = (32 * j + i < lim) ? ex2(__uint_as_float(sv[i]) * sl2 - lse2) : 0.f;
+        }
+        // phase 2: dS = P * (dP - D)
+        if (!(ok = warp_wait(dp_full, gt & 1, abort_flag))) break;
+        tc_fence_after();
         uint32_t pk[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(sa + 32 * j, sv);
-          tmem_ld_wait(sv);
+          uint32_t dv[32];
           tmem_ld32(pa + 32 * j, dv);
           tmem_ld_wait(dv);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int c = 32 * j + i;
-            const float p0 = c < lim ? ex2(__uint_as_float(sv[i]) * sl2 - lse2) : 0.f;
-            const float p1 = c + 1 < lim ? ex2(__uint_as_float(sv[i + 1]) * sl2 - lse2) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dv[i]) - Dr);
-            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - Dr);
-            pk[16 * j + i / 2] = pack_bf16(d0, d1);
+            pk[16 * j + i / 2] = pack_bf16(p[c] * (__uint_as_float(dv[i]) - Dr),
+                                           p[c + 1] * (__uint_as_float(dv[i + 1]) - Dr));
           }
         }
         tmem_st32(sa, *(const uint32_t(*)[32])(pk));
@@ -626,9 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_empty = bars + 1;
   uint64_t* st_full = bars + 2;        // [kNS]
   uint64_t* st_empty = st_full + kNS;  // [kNS]
-  uint64_t* sp_full = st_empty + kNS;
-  uint64_t* p_ready = sp_full + 1;
-  uint64_t* acc_done = p_ready + 1;
+  uint64_t* s_full = st_empty + kNS;   // S^T of a slab is in TMEM
+  uint64_t* dp_full = s_full + 1;      // dP^T of a slab is in TMEM
+  uint64_t* p_ready = dp_full + 1;     // softmax wrote P^T (bf16) over S^T
+  uint64_t* ds_ready = p_ready + 1;    // softmax wrote dS^T (bf16) over dP^T
+  uint64_t* acc_done = ds_ready + 1;
   uint64_t* acc_free = acc_done + 1;
   uint64_t* mma_drain = acc_free + 1;
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
@@ -643,8 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_full + s, 33);  // 32 row-info lanes + the TMA transaction arrive
       mbar_init(st_empty + s, 1);
     }
-    mbar_init(sp_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
     mbar_init(p_ready, 4);
+    mbar_init(ds_ready, 4);
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 4);
     mbar_init(mma_drain, 1);
@@ -730,33 +797,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
       const uint32_t k_addr = smem_u32(smem + Lay::k);
       const uint32_t v_addr = smem_u32(smem + Lay::v);
+      // Per slab: S^T, dP^T, [P^T ready] dV, S^T of the next slab, [dS^T ready]
+      // dK — the next S^T is queued before dK so the tensor pipe has work
+      // while the softmax warps turn dP^T into dS^T. TMEM reuse is safe
+      // because tcgen05 MMAs of one thread execute in issue order.
+      auto issue_s = [&](uint32_t stage) {
+        const uint32_t q_addr = smem_u32(smem + Lay::stage0 + stage * Lay::stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, desc_kmajor(k_addr, kk), desc_kmajor(q_addr, kk), kIdS, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+      };
       uint32_t nst = 0, nit = 0;
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
         const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
         if (!(ok = mbar_wait(kv_full, nit & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
         tc_fence_after();
+        issue_s(nst % kNS);
         for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
           const uint32_t s = nst % kNS;
-          if (!(ok = mbar_wait(st_full + s, (nst / kNS) & 1, abort_flag))) break;
-          tc_fence_after();
           const uint32_t q_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
           const uint32_t do_addr = q_addr + kSub * kSubBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tS, desc_kmajor(k_addr, kk), desc_kmajor(q_addr, kk), kIdS, kk > 0 ? 1u : 0u);
+          const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tP, desc_kmajor(v_addr, kk), desc_kmajor(do_addr, kk), kIdS, kk > 0 ? 1u : 0u);
-          mma_commit(sp_full);
-          const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
-          if (last) mma_commit(kv_empty);
+          mma_commit(dp_full);
+          if (last) mma_commit(kv_empty);  // K and V are not read after this
           if (!(ok = mbar_wait(p_ready, nst & 1, abort_flag))) break;
           if (first && nit > 0 && !(ok = mbar_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
             mma_ts(tdV, tS + kk * 8, desc_mnmajor(do_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
+          if (!last) {
+            const uint32_t s2 = (nst + 1) % kNS;
+            if (!(ok = mbar_wait(st_full + s2, ((nst + 1) / kNS) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_s(s2);
+          }
+          if (!(ok = mbar_wait(ds_ready, nst & 1, abort_flag))) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
             mma_ts(tdK, tP + kk * 8, desc_mnmajor(q_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
@@ -781,42 +864,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = nst % kNS;
         // row info of the stage was written by the producer warp: acquire it
         // through the stage barrier (already complete; it cannot advance before
-        // this slab's p_ready), then wait for S^T / dP^T.
+        // this slab's dS^T is consumed).
         if (!(ok = warp_wait(st_full + s, (nst / kNS) & 1, abort_flag))) break;
-        if (!(ok = warp_wait(sp_full, nst & 1, abort_flag))) break;
+        if (!(ok = warp_wait(s_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
         const float* lse2 = (const float*)(sb + Lay::info_off);
         const float* dvv = lse2 + kRows;
         const int* anc = (const int*)(dvv + kRows);
-        uint32_t pkP[64], pkS[64];
+        // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs
+        uint32_t pk[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t sv[32], dv[32];
+          uint32_t sv[32];
           tmem_ld32(tS + lane_base + 32 * j, sv);
           tmem_ld_wait(sv);
-          tmem_ld32(tP + lane_base + 32 * j, dv);
-          tmem_ld_wait(dv);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int c = 32 * j + i;
             const float p0 = key < anc[c] ? ex2(__uint_as_float(sv[i]) * sl2 - lse2[c]) : 0.f;
             const float p1 =
                 key < anc[c + 1] ? ex2(__uint_as_float(sv[i + 1]) * sl2 - lse2[c + 1]) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dv[i]) - dvv[c]);
-            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - dvv[c + 1]);
-            pkP[16 * j + i / 2] = pack_bf16(p0, p1);
-            pkS[16 * j + i / 2] = pack_bf16(d0, d1);
+            pk[16 * j + i / 2] = pack_bf16(p0, p1);
           }
         }
-        tmem_st32(tS + lane_base, *(const uint32_t(*)[32])(pkP));
-        tmem_st32(tS + lane_base + 32, *(const uint32_t(*)[32])(pkP + 32));
-        tmem_st32(tP + lane_base, *(const uint32_t(*)[32])(pkS));
-        tmem_st32(tP + lane_base + 32, *(const uint32_t(*)[32])(pkS + 32));
+        tmem_st32(tS + lane_base, *(const uint32_t(*)[32])(pk));
+        tmem_st32(tS + lane_base + 32, *(const uint32_t(*)[32])(pk + 32));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_ready);
+        // phase 2: dS^T = P^T * (dP^T - D)
+        if (!(ok = warp_wait(dp_full, nst & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t dv[32];
+          tmem_ld32(tP + lane_base + 32 * j, dv);
+          tmem_ld_wait(dv);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int c = 32 * j + i;
+            const uint32_t pp2 = pk[16 * j + i / 2];
+            const float p0 = __uint_as_float(pp2 << 16), p1 = __uint_as_float(pp2 & 0xffff0000u);
+            const float d0 = p0 * (__uint_as_float(dv[i]) - dvv[c]);
+            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - dvv[c + 1]);
+            pk[16 * j + i / 2] = pack_bf16(d0, d1);
+          }
+        }
+        tmem_st32(tP + lane_base, *(const uint32_t(*)[32])(pk));
+        tmem_st32(tP + lane_base + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_ready);
       }
       if (!ok) break;
       if (!(ok = warp_wait(acc_done, nit & 1, abort_flag))) break;

@@ -145,17 +145,19 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
 }
 
 // Work workspace: partial O (or dQ) [slots][128][d] fp32, partial lse
-// [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32 and the
-// backward row term D [Hq][N_q] fp32.
+// [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32, the
+// backward row term D [Hq][N_q] fp32 and the draft-key P / dS [N_q][Hq][B].
 struct WorkPtrs {
   float* part_o;
   float* part_lse;
   float* dq_draft;
   float* dvec;
+  float* draft_p;    // [N_q][Hq][B] softmax weight of each draft key
+  float* draft_ds;   // [N_q][Hq][B] dS of each draft key
 };
 
-inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, char* base,
-                          WorkPtrs* p) {
+inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int64_t B,
+                          char* base, WorkPtrs* p) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
     off = align_up(off, 256);
@@ -168,6 +170,8 @@ inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, char
   q.part_lse = (float*)take(sizeof(float) * (size_t)slots * kRows);
   q.dq_draft = (float*)take(sizeof(float) * (size_t)nq * Hq * d);
   q.dvec = (float*)take(sizeof(float) * (size_t)Hq * nq);
+  q.draft_p = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
+  q.draft_ds = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
   if (p) *p = q;
   return align_up(off, 256);
 }

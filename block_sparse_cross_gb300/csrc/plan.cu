@@ -272,6 +272,37 @@ namespace {
 __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32_t* pos,
                          int64_t* gload, int32_t* gcount) {
   const int lane = threadIdx.x & 31;
+  // Fast path: one group per lane and 32-bit keys. While items are dealt
+  // most expensive first to the least-loaded group, max load - min load
+  // never exceeds the largest cost, so (load - running minimum) * 32 + group
+  // fits 32 bits when that cost is < 2^26, and a single warp min-reduction
+  // finds the least-loaded group with the lowest id.
+  if (G <= 32 && (n == 0 || scost[0] < (1LL << 26))) {
+    int64_t load = 0, base = 0;
+    int32_t cnt = 0;
+    for (int r0 = 0; r0 < n; r0 += 32) {
+      const int32_t mine = (r0 + lane < n) ? (int32_t)scost[r0 + lane] : 0;
+      const int lim = min(32, n - r0);
+      for (int t = 0; t < lim; ++t) {
+        const int32_t c = __shfl_sync(0xffffffffu, mine, t);
+        const uint32_t key =
+            lane < G ? ((uint32_t)(load - base) << 5) | (uint32_t)lane : 0xffffffffu;
+        const uint32_t m = __reduce_min_sync(0xffffffffu, key);
+        if ((int)(m & 31u) == lane) {
+          grp[r0 + t] = lane;
+          pos[r0 + t] = cnt;
+          cnt += 1;
+          load += c;
+        }
+        base += (int64_t)(m >> 5);
+      }
+    }
+    if (lane < G) {
+      gload[lane] = load;
+      gcount[lane] = cnt;
+    }
+    return;
+  }
   int64_t load[kMaxGroupsPerLane];
   int32_t cnt[kMaxGroupsPerLane];
 #pragma unroll

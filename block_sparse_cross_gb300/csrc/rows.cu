@@ -7,10 +7,12 @@
 //               rit.work article on Split-KV (section "Split-KV двигает
 //               запросы, а не ключи и значения"); exact, so the result equals
 //               the single-device attention.
-//  bwd_draft    per (draft block, kv head): D = rowsum(dO * O) for its rows,
-//               the full backward of the B x B draft self-block (dKd, dVd
-//               summed over the group's heads in fixed order) and the draft
+//  bwd_prep     per (query, head): D = rowsum(dO * O), the softmax weights
+//               P and gradients dS of the row's B draft keys and the draft
 //               term of dQ (fp32, unscaled).
+//  bwd_draft_kv per (draft block, kv head): dKd, dVd of the B x B draft
+//               self-block, summed over the block's rows and the group's
+//               heads in fixed order.
 //  dq_reduce    per (query, head): dQ = scale * (sum over chunk partials in
 //               ascending chunk order + draft term); the query gradients are
 //               what moves between shards in the article's description.
@@ -143,80 +145,121 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   if (lane == 0) LSE[(size_t)h * P.NQ + n] = M + logf(Ls);
 }
 
-// One CTA per (draft block j, kv head g); thread r = (qi, hg) row of the
-// block, r = qi * group + hg (B * group <= 128 rows).
+// Backward prologue, one warp per (query n, head h):
+//   D = rowsum(dO * O); for each of the block's B draft keys t:
+//   P_t = exp(scale q.kd_t - LSE), dS_t = P_t (dO.vd_t - D); the draft term
+//   of dQ = sum_t dS_t kd_t (fp32, unscaled). P_t and dS_t are kept for the
+//   draft key/value gradients.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) bwd_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
-                                                        const T* __restrict__ Q,
-                                                        const T* __restrict__ Kd,
-                                                        const T* __restrict__ Vd,
-                                                        const T* __restrict__ O,
-                                                        const float* __restrict__ LSE,
-                                                        const T* __restrict__ dO,
-                                                        T* __restrict__ dKd,
-                                                        T* __restrict__ dVd) {
-  constexpr int RS = D + 1;                 // padded row stride (floats)
+__global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                       const T* __restrict__ Q,
+                                                       const T* __restrict__ Kd,
+                                                       const T* __restrict__ Vd,
+                                                       const T* __restrict__ O,
+                                                       const float* __restrict__ LSE,
+                                                       const T* __restrict__ dO) {
+  constexpr int EPL = D / 32;
+  if (read_status(pp.hdr) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= P.NQ * P.Hq) return;
+  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
+  const int g = h / P.group;
+  const int j = n / P.B;
+  const int x0 = lane * EPL;
+  const size_t row = ((size_t)n * P.Hq + h) * D + x0;
+  float q[EPL], dov[EPL], tmp[EPL];
+  ld_vec<T, EPL>(Q + row, q);
+  ld_vec<T, EPL>(dO + row, dov);
+  ld_vec<T, EPL>(O + row, tmp);
+  float dd = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) dd = fmaf(dov[i], tmp[i], dd);
+  const float Dr = warp_sum(dd);
+  const float lse = LSE[(size_t)h * P.NQ + n];
+  if (lane == 0) wk.dvec[(size_t)h * P.NQ + n] = Dr;
+  float* prow = wk.draft_p + ((size_t)n * P.Hq + h) * P.B;
+  float* srow = wk.draft_ds + ((size_t)n * P.Hq + h) * P.B;
+  float acc[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+  for (int t = 0; t < P.B; ++t) {
+    const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
+    float kd[EPL];
+    ld_vec<T, EPL>(Kd + kro, kd);
+    ld_vec<T, EPL>(Vd + kro, tmp);
+    float sp = 0.f, dp = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      sp = fmaf(q[i], kd[i], sp);
+      dp = fmaf(dov[i], tmp[i], dp);
+    }
+    sp = warp_sum(sp);
+    dp = warp_sum(dp);
+    const float pt = expf(sp * P.scale - lse);
+    const float ds = pt * (dp - Dr);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = fmaf(ds, kd[i], acc[i]);
+    if (lane == (t & 31)) {
+      prow[t] = pt;
+      srow[t] = ds;
+    }
+  }
+  float* dqd = wk.dq_draft + row;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) dqd[i] = acc[i];
+}
+
+// Draft key/value gradients, one CTA per (draft block j, kv head g), one
+// thread per head dim x: dVd[t] = sum_r P_t(r) dO_r, dKd[t] = scale *
+// sum_r dS_t(r) q_r over the block's B * group rows r in fixed order.
+template <typename T, int D>
+__global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                         const T* __restrict__ Q,
+                                                         const T* __restrict__ dO,
+                                                         T* __restrict__ dKd,
+                                                         T* __restrict__ dVd) {
+  constexpr int TC = 16;  // draft keys per pass
   extern __shared__ float sm[];
   const int B = P.B, R = B * P.group;
-  float* kd = sm;                           // [B][D]
-  float* vd = kd + B * D;                   // [B][D]
-  float* qs = vd + B * D;                   // [R][RS]
-  float* dos = qs + R * RS;                 // [R][RS]
-  float* ps = dos + R * RS;                 // [R][B]
-  float* dss = ps + R * B;                  // [R][B]
-  if (read_status(pp.hdr) != 0) return;
+  float* ps = sm;            // [R][B]
+  float* dss = ps + R * B;   // [R][B]
   const int j = blockIdx.x, g = blockIdx.y;
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < B * D; idx += blockDim.x) {
-    const int t = idx / D, x = idx % D;
-    const size_t o = ((size_t)(j * B + t) * P.Hkv + g) * D + x;
-    kd[idx] = ld_f(Kd + o);
-    vd[idx] = ld_f(Vd + o);
-  }
-  for (int idx = tid; idx < R * D; idx += blockDim.x) {
-    const int r = idx / D, x = idx % D;
+  const int x = threadIdx.x;
+  // No status check here: bwd_prep_kernel, which runs first on the stream,
+  // skips its work on a latched error and the outputs are then undefined.
+  for (int idx = x; idx < R * B; idx += blockDim.x) {
+    const int r = idx / B, t = idx % B;
     const int n = j * B + r / P.group, h = g * P.group + r % P.group;
-    const size_t o = ((size_t)n * P.Hq + h) * D + x;
-    qs[r * RS + x] = ld_f(Q + o);
-    dos[r * RS + x] = ld_f(dO + o);
+    const size_t o = ((size_t)n * P.Hq + h) * B + t;
+    ps[idx] = wk.draft_p[o];
+    dss[idx] = wk.draft_ds[o];
   }
   __syncthreads();
-  if (tid < R) {
-    const int r = tid;
-    const int n = j * B + r / P.group, h = g * P.group + r % P.group;
-    const T* orow = O + ((size_t)n * P.Hq + h) * D;
-    float Dr = 0.f;
-    for (int x = 0; x < D; ++x) Dr = fmaf(dos[r * RS + x], ld_f(orow + x), Dr);
-    wk.dvec[(size_t)h * P.NQ + n] = Dr;
-    const float lse = LSE[(size_t)h * P.NQ + n];
-    for (int t = 0; t < B; ++t) {
-      float sc = 0.f, dp = 0.f;
-      for (int x = 0; x < D; ++x) {
-        sc = fmaf(qs[r * RS + x], kd[t * D + x], sc);
-        dp = fmaf(dos[r * RS + x], vd[t * D + x], dp);
-      }
-      const float p = expf(sc * P.scale - lse);
-      ps[r * B + t] = p;
-      dss[r * B + t] = p * (dp - Dr);
-    }
-    float* dqd = wk.dq_draft + ((size_t)n * P.Hq + h) * D;
-    for (int x = 0; x < D; ++x) {
-      float a = 0.f;
-      for (int t = 0; t < B; ++t) a = fmaf(dss[r * B + t], kd[t * D + x], a);
-      dqd[x] = a;
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < B * D; idx += blockDim.x) {
-    const int t = idx / D, x = idx % D;
-    float av = 0.f, ak = 0.f;
+  for (int t0 = 0; t0 < B; t0 += TC) {
+    float av[TC], ak[TC];
+#pragma unroll
+    for (int k = 0; k < TC; ++k) av[k] = ak[k] = 0.f;
     for (int r = 0; r < R; ++r) {
-      av = fmaf(ps[r * B + t], dos[r * RS + x], av);
-      ak = fmaf(dss[r * B + t], qs[r * RS + x], ak);
+      const int n = j * B + r / P.group, h = g * P.group + r % P.group;
+      const size_t o = ((size_t)n * P.Hq + h) * D + x;
+      const float dov = ld_f(dO + o), qv = ld_f(Q + o);
+#pragma unroll
+      for (int k = 0; k < TC; ++k) {
+        if (t0 + k < B) {
+          av[k] = fmaf(ps[r * B + t0 + k], dov, av[k]);
+          ak[k] = fmaf(dss[r * B + t0 + k], qv, ak[k]);
+        }
+      }
     }
-    const size_t o = ((size_t)(j * B + t) * P.Hkv + g) * D + x;
-    st_f(dVd + o, av);
-    st_f(dKd + o, ak * P.scale);
+#pragma unroll
+    for (int k = 0; k < TC; ++k) {
+      if (t0 + k < B) {
+        const size_t o = ((size_t)(j * B + t0 + k) * P.Hkv + g) * D + x;
+        st_f(dVd + o, av[k]);
+        st_f(dKd + o, ak[k] * P.scale);
+      }
+    }
   }
 }
 
@@ -299,16 +342,18 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
   return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
     using T = decltype(tag);
     constexpr int D = decltype(dtag)::value;
-    if (P.NA == 0) return cudaSuccess;
-    const int R = P.B * P.group;
-    const size_t smem = sizeof(float) * (2 * P.B * D + 2 * R * (D + 1) + 2 * R * P.B);
-    auto k = bwd_draft_kernel<T, D>;
-    cudaError_t err =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int64_t warps = P.NQ * P.Hq;
+    if (warps == 0) return cudaSuccess;
+    bwd_prep_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O, LSE, (const T*)dO);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t smem = sizeof(float) * 2 * (size_t)P.B * P.group * P.B;
+    auto k = bwd_draft_kv_kernel<T, D>;
+    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((unsigned)P.NA, (unsigned)P.Hkv);
-    k<<<grid, 128, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O,
-                               LSE, (const T*)dO, (T*)dKd, (T*)dVd);
+    k<<<grid, D, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)dO, (T*)dKd, (T*)dVd);
     return cudaGetLastError();
   });
 }
