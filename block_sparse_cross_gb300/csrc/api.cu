@@ -125,8 +125,8 @@ size_t plan_bytes_for(const splitkv_problem* p) {
 
 size_t work_bytes_for(const splitkv_problem* p) {
   const PlanCaps c = caps_of(p, kMaxWorkers);
-  return work_layout(c.NCF * p->Hkv, p->total_anchors * p->B, p->Hq, p->d, p->B, nullptr,
-                     nullptr);
+  return work_layout(c.NCF * p->Hkv, p->total_anchors * p->B, p->Hq, p->d, p->B,
+                     c.NSL * p->Hkv, nullptr, nullptr);
 }
 
 struct Ctx {
@@ -280,7 +280,8 @@ int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   if (work_bytes < work_bytes_for(prob)) return SPLITKV_EWORKSPACE;
   if (!any_q) return SPLITKV_OK;
   WorkPtrs wk;
-  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B, (char*)work, &wk);
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B,
+              c.caps.NSL * prob->Hkv, (char*)work, &wk);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = timed(SPLITKV_K_FWD_ATTN, 1, s, [&] {
     return use_tensor_cores(c.P) ? launch_fwd_tc(c.P, c.pp, wk, Q, Kc, Vc, s)
@@ -314,9 +315,10 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   }
   if (!any_q) return SPLITKV_OK;
   WorkPtrs wk;
-  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B, (char*)work, &wk);
+  work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B,
+              c.caps.NSL * prob->Hkv, (char*)work, &wk);
   e = timed(SPLITKV_K_BWD_DRAFT, 1, s, [&] {
-    return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, s);
+    return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, c.caps.NSL, s);
   });
   if (e != cudaSuccess) return SPLITKV_ECUDA;
   const bool tc = use_tensor_cores(c.P);
@@ -393,7 +395,8 @@ int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv
   out->fwd_tiles = h.fwd_tiles * Hkv;
   out->dense_tiles = h.dense_tiles * Hkv;
   out->work_bytes_used =
-      work_layout(out->fwd_slots, c.P.NQ, prob->Hq, prob->d, prob->B, nullptr, nullptr);
+      work_layout(out->fwd_slots, c.P.NQ, prob->Hq, prob->d, prob->B,
+                  (int64_t)h.n_slabs * prob->Hkv, nullptr, nullptr);
   return SPLITKV_OK;
 }
 

@@ -268,22 +268,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = ns & 1;
         if (!(ok = warp_wait(s_full + sb, (ns >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const int lim = min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
+        // padding rows (beyond the slab's blocks) compute on whatever Q rows the
+        // tile box holds; their partials are never read
+        const int lim = ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
         const uint32_t sa = tS + lane_base + sb * 128;
-        float x[128];
-        float mt = -INFINITY;
+        uint32_t x[128];  // raw scores of the row (masked entries -> -inf)
+        tmem_ld_row<128>(sa, x);
+        if (!__all_sync(0xffffffffu, lim >= kKeyTile)) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t v[32];
-          tmem_ld32(sa + 32 * j, v);
-          tmem_ld_wait(v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float xv = (32 * j + i < lim) ? __uint_as_float(v[i]) * sl2 : -INFINITY;
-            x[32 * j + i] = xv;
-            mt = fmaxf(mt, xv);
-          }
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) x[i] = __float_as_uint(-INFINITY);
         }
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
+#pragma unroll
+        for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
         const float m_new = fmaxf(m_run, mt);
         float fac = 1.f;
         bool resc = false;
@@ -294,18 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
           m_run = m_new;
         }
-        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls = 0.f;
+        const float nmu = (m_run == -INFINITY) ? 0.f : -m_run;
+        float lsum[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lsum[k] = 0.f;
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2(x[2 * i] - mu), p1 = ex2(x[2 * i + 1] - mu);
-          ls += p0 + p1;
+          const float p0 = ex2(fmaf(__uint_as_float(x[2 * i]), sl2, nmu));
+          const float p1 = ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl2, nmu));
+          lsum[i & 7] += p0 + p1;
           pk[i] = pack_bf16(p0, p1);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lsum[k] += lsum[k + 4];
+        const float ls = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
         l = (t == 0) ? ls : l * fac + ls;
-        tmem_st32(sa, *(const uint32_t(*)[32])(pk));
-        tmem_st32(sa + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st64(sa, pk);
         tmem_st_wait();
         if (t > 0) {
           if (!(ok = warp_wait(pv_done, npv & 1, abort_flag))) break;
@@ -334,14 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float* po = wk.part_o + (I.slot * kRows + r) * D;
+      {
+        uint32_t v[D];
+        tmem_ld_row<D>(tO + lane_base, v);
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        uint32_t v[32];
-        tmem_ld32(tO + lane_base + 32 * j, v);
-        tmem_ld_wait(v);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *(float4*)(po + 32 * j + i) =
+        for (int i = 0; i < D; i += 4)
+          *(float4*)(po + i) =
               make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
                           __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
       }
@@ -563,47 +569,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
       const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
-      float lse2 = 0.f, Dr = 0.f;
+      // padding rows: -inf exponent offset makes their P exactly 0
+      float nl2 = -INFINITY, Dr = 0.f;
       if (ri.n >= 0) {
-        lse2 = LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
+        nl2 = -LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
         Dr = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
       }
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         if (!(ok = warp_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const int lim = min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
+        const int lim = ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
         const uint32_t sa = tmem + lane_base + ((2 * gt) % 3) * 128;
         const uint32_t pa = tmem + lane_base + ((2 * gt + 1) % 3) * 128;
         // phase 1 (while dQ of the previous tile and dP of this one run):
-        // P = exp(S * scale - LSE) on the row's visible keys
-        float p[128];
+        // P = exp(S * scale - LSE) on the row's visible keys, kept as bf16
+        uint32_t pk[64];
+        {
+          uint32_t sv[128];
+          tmem_ld_row<128>(sa, sv);
+          if (__all_sync(0xffffffffu, lim >= kKeyTile)) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t sv[32];
-          tmem_ld32(sa + 32 * j, sv);
-          tmem_ld_wait(sv);
+            for (int i = 0; i < 128; i += 2)
+              pk[i / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)),
+                                    ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)));
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            p[32 * j + i] = (32 * j + i < lim) ? ex2(__uint_as_float(sv[i]) * sl2 - lse2) : 0.f;
+            for (int i = 0; i < 128; i += 2) {
+              const float p0 = (i < lim) ? ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)) : 0.f;
+              const float p1 = (i + 1 < lim) ? ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)) : 0.f;
+              pk[i / 2] = pack_bf16(p0, p1);
+            }
+          }
         }
         // phase 2: dS = P * (dP - D)
         if (!(ok = warp_wait(dp_full, gt & 1, abort_flag))) break;
         tc_fence_after();
-        uint32_t pk[64];
+        {
+          uint32_t dv[128];
+          tmem_ld_row<128>(pa, dv);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t dv[32];
-          tmem_ld32(pa + 32 * j, dv);
-          tmem_ld_wait(dv);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int c = 32 * j + i;
-            pk[16 * j + i / 2] = pack_bf16(p[c] * (__uint_as_float(dv[i]) - Dr),
-                                           p[c + 1] * (__uint_as_float(dv[i + 1]) - Dr));
+          for (int i = 0; i < 128; i += 2) {
+            const uint32_t pp2 = pk[i / 2];
+            pk[i / 2] = pack_bf16(__uint_as_float(pp2 << 16) * (__uint_as_float(dv[i]) - Dr),
+                                  __uint_as_float(pp2 & 0xffff0000u) * (__uint_as_float(dv[i + 1]) - Dr));
           }
         }
-        tmem_st32(sa, *(const uint32_t(*)[32])(pk));
-        tmem_st32(sa + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st64(sa, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -613,16 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
       tc_fence_after();
       float* po = wk.part_o + (I.slot * kRows + r) * D;
+      {
+        uint32_t v[D];
+        tmem_ld_row<D>(tdQ + lane_base, v);
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        uint32_t v[32];
-        tmem_ld32(tdQ + lane_base + 32 * j, v);
-        tmem_ld_wait(v);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *(float4*)(po + 32 * j + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                    __uint_as_float(v[i + 2]),
-                                                    __uint_as_float(v[i + 3]));
+        for (int i = 0; i < D; i += 4)
+          *(float4*)(po + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
       }
       tc_fence_before();
       __syncwarp();
@@ -647,7 +655,7 @@ struct KvLayout {
   static constexpr uint32_t v = kSub * kSubBytes;
   static constexpr uint32_t stage0 = 2 * kSub * kSubBytes;
   static constexpr uint32_t info_off = 2 * kSub * kSubBytes;       // inside a stage
-  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes + 2048;  // Q, dO, row info
+  static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes + 2048;  // Q, dO, row table
   static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
   static constexpr uint32_t total = bars + 512 + 1024;
 };
@@ -705,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(st_full + s, 33);  // 32 row-info lanes + the TMA transaction arrive
+      mbar_init(st_full + s, 1);
       mbar_init(st_empty + s, 1);
     }
     mbar_init(s_full, 1);
@@ -730,66 +738,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.b_qoff[blockIdx.x], q1 = pp.b_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- producer: K/V per item, Q/dO/row info per slab --------
+    // ---------------- producer: K/V per item; Q, dO and the slab's row table
+    // (one bulk copy of the precomputed record) per slab ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-    }
-    uint32_t nkv = 0, nst = 0;
-    bool ok = true;
-    for (int qi = q0; qi < q1 && ok; ++qi) {
-      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
-      if (lane == 0) {
-        if (nkv > 0) ok = mbar_wait(kv_empty, (nkv - 1) & 1, abort_flag);
-        if (ok) {
-          mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i) {
-            tma_load_3d(smem + Lay::k + i * kSubBytes, &tmK, kv_full, 64 * i, I.g, I.c0 + I.ks0);
-            tma_load_3d(smem + Lay::v + i * kSubBytes, &tmV, kv_full, 64 * i, I.g, I.c0 + I.ks0);
-          }
-          ++nkv;
+      uint32_t nkv = 0, nst = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+        if (nkv > 0 && !(ok = mbar_wait(kv_empty, (nkv - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
+        for (int i = 0; i < kSub; ++i) {
+          tma_load_3d(smem + Lay::k + i * kSubBytes, &tmK, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+          tma_load_3d(smem + Lay::v + i * kSubBytes, &tmV, kv_full, 64 * i, I.g, I.c0 + I.ks0);
         }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      nkv = __shfl_sync(0xffffffffu, nkv, 0);
-      if (!ok) break;
-      for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
-        const uint32_t s = nst % kNS, u = nst / kNS;
-        if (u > 0 && !(ok = warp_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
-        uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
-        float* lse2 = (float*)(sb + Lay::info_off);
-        float* dvv = lse2 + kRows;
-        int* anc = (int*)(dvv + kRows);
-        const int first = pp.sl_first[sg], nblk = pp.sl_nblk[sg];
-        for (int rr = lane; rr < kRows; rr += 32) {
-          const RowInfo ri = row_info(P, first, nblk, I.g, rr);
-          float l2 = 0.f, dd = 0.f;
-          if (ri.n >= 0) {
-            l2 = LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
-            dd = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
-          }
-          lse2[rr] = l2;
-          dvv[rr] = dd;
-          anc[rr] = ri.anchor;
-        }
-        if (lane == 0) {
-          mbar_expect_tx(st_full + s, 2 * kSub * kSubBytes);
-          const int n0 = first * P.B;
+        ++nkv;
+        for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
+          const uint32_t s = nst % kNS, u = nst / kNS;
+          if (u > 0 && !(ok = mbar_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
+          const int n0 = pp.sl_first[sg] * P.B;
+          mbar_expect_tx(st_full + s, 2 * kSub * kSubBytes + kRowInfoFloats * 4);
           for (int i = 0; i < kSub; ++i) {
             tma_load_3d(sb + i * kSubBytes, &tmQ, st_full + s, 64 * i, I.g * P.group, n0);
             tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
           }
+          bulk_load(sb + Lay::info_off, wk.rowinfo + ((size_t)sg * P.Hkv + I.g) * kRowInfoFloats,
+                    kRowInfoFloats * 4, st_full + s);
+          ++nst;
         }
-        mbar_arrive(st_full + s);
-        ++nst;
       }
-    }
-    if (!ok && lane == 0) {
-      if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1, kDrainNs);
-      for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
-        mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
+      if (!ok) {
+        if (nkv > 0) mbar_wait_drain(kv_full, (nkv - 1) & 1, kDrainNs);
+        for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
+          mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -869,27 +855,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(s_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
-        const float* lse2 = (const float*)(sb + Lay::info_off);
-        const float* dvv = lse2 + kRows;
+        const float* nl2 = (const float*)(sb + Lay::info_off);  // -LSE*log2(e), -inf on padding
+        const float* dvv = nl2 + kRows;
         const int* anc = (const int*)(dvv + kRows);
-        // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs
+        // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs.
+        // Rows are ordered by block and anchors rise with the block, so a key
+        // below the slab's first anchor is seen by every row (padding rows give
+        // 0 through their -inf): no per-element mask on such warps.
         uint32_t pk[64];
+        {
+          uint32_t sv[128];
+          tmem_ld_row<128>(tS + lane_base, sv);
+          if (__all_sync(0xffffffffu, key < anc[0])) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t sv[32];
-          tmem_ld32(tS + lane_base + 32 * j, sv);
-          tmem_ld_wait(sv);
+            for (int c = 0; c < 128; c += 2)
+              pk[c / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])),
+                                    ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])));
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int c = 32 * j + i;
-            const float p0 = key < anc[c] ? ex2(__uint_as_float(sv[i]) * sl2 - lse2[c]) : 0.f;
-            const float p1 =
-                key < anc[c + 1] ? ex2(__uint_as_float(sv[i + 1]) * sl2 - lse2[c + 1]) : 0.f;
-            pk[16 * j + i / 2] = pack_bf16(p0, p1);
+            for (int c = 0; c < 128; c += 2) {
+              const float p0 = key < anc[c] ? ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])) : 0.f;
+              const float p1 =
+                  key < anc[c + 1] ? ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])) : 0.f;
+              pk[c / 2] = pack_bf16(p0, p1);
+            }
           }
         }
-        tmem_st32(tS + lane_base, *(const uint32_t(*)[32])(pk));
-        tmem_st32(tS + lane_base + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st64(tS + lane_base, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -897,23 +889,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 2: dS^T = P^T * (dP^T - D)
         if (!(ok = warp_wait(dp_full, nst & 1, abort_flag))) break;
         tc_fence_after();
+        {
+          uint32_t dv[128];
+          tmem_ld_row<128>(tP + lane_base, dv);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t dv[32];
-          tmem_ld32(tP + lane_base + 32 * j, dv);
-          tmem_ld_wait(dv);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int c = 32 * j + i;
-            const uint32_t pp2 = pk[16 * j + i / 2];
+          for (int c = 0; c < 128; c += 2) {
+            const uint32_t pp2 = pk[c / 2];
             const float p0 = __uint_as_float(pp2 << 16), p1 = __uint_as_float(pp2 & 0xffff0000u);
-            const float d0 = p0 * (__uint_as_float(dv[i]) - dvv[c]);
-            const float d1 = p1 * (__uint_as_float(dv[i + 1]) - dvv[c + 1]);
-            pk[16 * j + i / 2] = pack_bf16(d0, d1);
+            pk[c / 2] = pack_bf16(p0 * (__uint_as_float(dv[c]) - dvv[c]),
+                                  p1 * (__uint_as_float(dv[c + 1]) - dvv[c + 1]));
           }
         }
-        tmem_st32(tP + lane_base, *(const uint32_t(*)[32])(pk));
-        tmem_st32(tP + lane_base + 32, *(const uint32_t(*)[32])(pk + 32));
+        tmem_st64(tP + lane_base, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -924,27 +911,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool valid = key < I.L;
       const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tdV + lane_base + 32 * j, a);
-        tmem_ld_wait(a);
-        tmem_ld32(tdK + lane_base + 32 * j, b);
-        tmem_ld_wait(b);
+      for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled)
+        uint32_t a[D];
+        tmem_ld_row<D>((which == 0 ? tdV : tdK) + lane_base, a);
+        const float f = which == 0 ? 1.f : P.scale;
+        __nv_bfloat16* dst = (which == 0 ? dVc : dKc) + off;
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 pv, pkk;
-            pv.x = pack_bf16(__uint_as_float(a[i]), __uint_as_float(a[i + 1]));
-            pv.y = pack_bf16(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3]));
-            pv.z = pack_bf16(__uint_as_float(a[i + 4]), __uint_as_float(a[i + 5]));
-            pv.w = pack_bf16(__uint_as_float(a[i + 6]), __uint_as_float(a[i + 7]));
-            pkk.x = pack_bf16(__uint_as_float(b[i]) * P.scale, __uint_as_float(b[i + 1]) * P.scale);
-            pkk.y = pack_bf16(__uint_as_float(b[i + 2]) * P.scale, __uint_as_float(b[i + 3]) * P.scale);
-            pkk.z = pack_bf16(__uint_as_float(b[i + 4]) * P.scale, __uint_as_float(b[i + 5]) * P.scale);
-            pkk.w = pack_bf16(__uint_as_float(b[i + 6]) * P.scale, __uint_as_float(b[i + 7]) * P.scale);
-            *(uint4*)(dVc + off + 32 * j + i) = pv;
-            *(uint4*)(dKc + off + 32 * j + i) = pkk;
+          for (int i = 0; i < D; i += 8) {
+            uint4 pv;
+            pv.x = pack_bf16(__uint_as_float(a[i]) * f, __uint_as_float(a[i + 1]) * f);
+            pv.y = pack_bf16(__uint_as_float(a[i + 2]) * f, __uint_as_float(a[i + 3]) * f);
+            pv.z = pack_bf16(__uint_as_float(a[i + 4]) * f, __uint_as_float(a[i + 5]) * f);
+            pv.w = pack_bf16(__uint_as_float(a[i + 6]) * f, __uint_as_float(a[i + 7]) * f);
+            *(uint4*)(dst + i) = pv;
           }
         }
       }

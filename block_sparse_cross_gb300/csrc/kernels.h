@@ -37,7 +37,7 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
 cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                              const void* Q, const void* Kd, const void* Vd, const void* O,
                              const float* LSE, const void* dO, void* dKd, void* dVd,
-                             cudaStream_t st);
+                             int64_t nsl_cap, cudaStream_t st);
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
                              cudaStream_t st);
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,

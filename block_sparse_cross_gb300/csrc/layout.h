@@ -146,7 +146,8 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
 
 // Work workspace: partial O (or dQ) [slots][128][d] fp32, partial lse
 // [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32, the
-// backward row term D [Hq][N_q] fp32 and the draft-key P / dS [N_q][Hq][B].
+// backward row term D [Hq][N_q] fp32, the draft-key P / dS [N_q][Hq][B] and
+// the per-(slab, kv head) row table the dK/dV kernel streams with each slab.
 struct WorkPtrs {
   float* part_o;
   float* part_lse;
@@ -154,10 +155,13 @@ struct WorkPtrs {
   float* dvec;
   float* draft_p;    // [N_q][Hq][B] softmax weight of each draft key
   float* draft_ds;   // [N_q][Hq][B] dS of each draft key
+  float* rowinfo;    // [slab][Hkv][3][128]: -LSE*log2(e) (-inf on padding rows), D, anchor bits
 };
 
+constexpr int kRowInfoFloats = 3 * kRows;  // one (slab, kv head) record: 1536 bytes
+
 inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int64_t B,
-                          char* base, WorkPtrs* p) {
+                          int64_t slabs_x_hkv, char* base, WorkPtrs* p) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
     off = align_up(off, 256);
@@ -172,6 +176,7 @@ inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int6
   q.dvec = (float*)take(sizeof(float) * (size_t)Hq * nq);
   q.draft_p = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
   q.draft_ds = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
+  q.rowinfo = (float*)take(sizeof(float) * (size_t)slabs_x_hkv * kRowInfoFloats);
   if (p) *p = q;
   return align_up(off, 256);
 }

@@ -94,25 +94,42 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
     od[i] = 0.f;
   }
   float md = -INFINITY, ld = 0.f;
-  for (int t = 0; t < P.B; ++t) {
-    const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
-    ld_vec<T, EPL>(Kd + kro, tmp);
-    float part = 0.f;
+  constexpr int KT = 8;  // draft keys in flight
+  for (int t0 = 0; t0 < P.B; t0 += KT) {
+    float kv[KT][EPL], vv[KT][EPL], sc[KT];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) part = fmaf(q[i], tmp[i], part);
-    const float sc = warp_sum(part);
-    ld_vec<T, EPL>(Vd + kro, tmp);
-    if (sc > md) {
-      const float f = expf(md - sc);
-      ld = ld * f + 1.f;
+    for (int u = 0; u < KT; ++u) {
+      const int t = min(t0 + u, P.B - 1);
+      const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
+      ld_vec<T, EPL>(Kd + kro, kv[u]);
+      ld_vec<T, EPL>(Vd + kro, vv[u]);
+    }
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) od[i] = fmaf(od[i], f, tmp[i]);
-      md = sc;
-    } else {
-      const float p = expf(sc - md);
-      ld += p;
+    for (int u = 0; u < KT; ++u) {
+      float part = 0.f;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) od[i] = fmaf(p, tmp[i], od[i]);
+      for (int i = 0; i < EPL; ++i) part = fmaf(q[i], kv[u][i], part);
+      sc[u] = part;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < KT; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], o);
+#pragma unroll
+    for (int u = 0; u < KT; ++u) {
+      if (t0 + u >= P.B) break;
+      if (sc[u] > md) {
+        const float f = expf(md - sc[u]);
+        ld = ld * f + 1.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) od[i] = fmaf(od[i], f, vv[u][i]);
+        md = sc[u];
+      } else {
+        const float p = expf(sc[u] - md);
+        ld += p;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) od[i] = fmaf(p, vv[u][i], od[i]);
+      }
     }
   }
   const float lse_d = md + logf(ld);
@@ -131,12 +148,21 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+#pragma unroll 4
   for (int c = 0; c < G.nact; ++c) {
     const size_t row = ((slot0 + c) * P.Hkv + g) * kRows + G.r;
     const float wgt = expf(wk.part_lse[row] - M) * invL;
-    const float* po = wk.part_o + row * D + x0;
+    if constexpr (EPL == 4) {  // 16-byte aligned: row * D * 4 and lane * 16 bytes
+      const float4 v = *(const float4*)(wk.part_o + row * D + x0);
+      acc[0] = fmaf(wgt, v.x, acc[0]);
+      acc[1] = fmaf(wgt, v.y, acc[1]);
+      acc[2] = fmaf(wgt, v.z, acc[2]);
+      acc[3] = fmaf(wgt, v.w, acc[3]);
+    } else {
+      const float* po = wk.part_o + row * D + x0;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wgt, po[i], acc[i]);
+      for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wgt, po[i], acc[i]);
+    }
   }
   const float wd = expf(lse_d - M) * invL / ld;
 #pragma unroll
@@ -183,26 +209,43 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, W
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
-  for (int t = 0; t < P.B; ++t) {
-    const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
-    float kd[EPL];
-    ld_vec<T, EPL>(Kd + kro, kd);
-    ld_vec<T, EPL>(Vd + kro, tmp);
-    float sp = 0.f, dp = 0.f;
+  constexpr int KT = 8;  // draft keys in flight
+  for (int t0 = 0; t0 < P.B; t0 += KT) {
+    float kd[KT][EPL], sp[KT], dp[KT];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      sp = fmaf(q[i], kd[i], sp);
-      dp = fmaf(dov[i], tmp[i], dp);
+    for (int u = 0; u < KT; ++u) {
+      const int t = min(t0 + u, P.B - 1);
+      const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
+      float vd[EPL];
+      ld_vec<T, EPL>(Kd + kro, kd[u]);
+      ld_vec<T, EPL>(Vd + kro, vd);
+      sp[u] = 0.f;
+      dp[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        sp[u] = fmaf(q[i], kd[u][i], sp[u]);
+        dp[u] = fmaf(dov[i], vd[i], dp[u]);
+      }
     }
-    sp = warp_sum(sp);
-    dp = warp_sum(dp);
-    const float pt = expf(sp * P.scale - lse);
-    const float ds = pt * (dp - Dr);
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) acc[i] = fmaf(ds, kd[i], acc[i]);
-    if (lane == (t & 31)) {
-      prow[t] = pt;
-      srow[t] = ds;
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < KT; ++u) {
+        sp[u] += __shfl_xor_sync(0xffffffffu, sp[u], o);
+        dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], o);
+      }
+#pragma unroll
+    for (int u = 0; u < KT; ++u) {
+      const int t = t0 + u;
+      if (t >= P.B) break;
+      const float pt = expf(sp[u] * P.scale - lse);
+      const float ds = pt * (dp[u] - Dr);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) acc[i] = fmaf(ds, kd[u][i], acc[i]);
+      if (lane == (t & 31)) {
+        prow[t] = pt;
+        srow[t] = ds;
+      }
     }
   }
   float* dqd = wk.dq_draft + row;
@@ -263,6 +306,25 @@ __global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp,
   }
 }
 
+// Row table of every (slab, kv head) for the dK/dV kernel, which streams it
+// with the slab's Q / dO tiles: -LSE*log2(e) (-inf on padding rows, so their
+// P is 0 without masking), D, and the row's anchor.
+__global__ void __launch_bounds__(128) slab_rowinfo_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                           const float* __restrict__ LSE) {
+  const int sg = blockIdx.x, g = blockIdx.y, r = threadIdx.x;
+  if (sg >= pp.hdr->n_slabs || read_status(pp.hdr) != 0) return;
+  const RowInfo ri = row_info(P, pp.sl_first[sg], pp.sl_nblk[sg], g, r);
+  float* rec = wk.rowinfo + ((size_t)sg * P.Hkv + g) * kRowInfoFloats;
+  if (ri.n >= 0) {
+    rec[r] = -LSE[(size_t)ri.h * P.NQ + ri.n] * 1.4426950408889634f;
+    rec[kRows + r] = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
+  } else {
+    rec[r] = -INFINITY;
+    rec[kRows + r] = 0.f;
+  }
+  ((int*)rec)[2 * kRows + r] = ri.anchor;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                         T* __restrict__ dQ) {
@@ -279,6 +341,7 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+#pragma unroll 4
   for (int c = 0; c < G.nact; ++c) {
     const float* po = wk.part_o + (((slot0 + c) * P.Hkv + g) * kRows + G.r) * D + x0;
 #pragma unroll
@@ -338,7 +401,7 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
 cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                              const void* Q, const void* Kd, const void* Vd, const void* O,
                              const float* LSE, const void* dO, void* dKd, void* dVd,
-                             cudaStream_t st) {
+                             int64_t nsl_cap, cudaStream_t st) {
   return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
     using T = decltype(tag);
     constexpr int D = decltype(dtag)::value;
@@ -354,6 +417,9 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
     if (err != cudaSuccess) return err;
     dim3 grid((unsigned)P.NA, (unsigned)P.Hkv);
     k<<<grid, D, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)dO, (T*)dKd, (T*)dVd);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || nsl_cap == 0) return err;
+    slab_rowinfo_kernel<<<dim3((unsigned)nsl_cap, (unsigned)P.Hkv), kRows, 0, st>>>(P, pp, wk, LSE);
     return cudaGetLastError();
   });
 }
