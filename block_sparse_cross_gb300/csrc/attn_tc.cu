@@ -16,10 +16,11 @@
 //         K/V gradients) while every slab of rows that sees it streams by:
 //         S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q.
 //
-// Warp roles (192 threads): warp 0 issues TMA (one elected lane), warp 1
-// allocates TMEM and issues every MMA (one lane), warps 2..5 own TMEM lane
-// quadrants (warp % 4) and do the softmax and the epilogue, one row (fwd/dq)
-// or one key (dkdv) per thread. All waits are bounded (tc_common.cuh); on a
+// Warp roles (320 threads): warp 0 issues TMA, warp 1 allocates TMEM and
+// issues every MMA (the warp runs the control loop, one elected lane issues),
+// warps 2..9 do the softmax and the epilogue: warp w owns TMEM lane quadrant
+// w % 4 (one row (fwd/dq) or one key (dkdv) per thread) and one half of the
+// 128 columns. All waits are bounded (tc_common.cuh); on a
 // timeout the CTA winds down, drains its copies and MMAs, frees TMEM and
 // latches SPLITKV_ETIMEOUT.
 #include <cudaTypedefs.h>
@@ -35,7 +36,8 @@ namespace {
 using namespace tc;
 
 constexpr int kNS = 2;               // pipeline stages
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;    // producer warp, MMA warp, 8 softmax warps
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -62,6 +64,12 @@ __device__ __forceinline__ FwdItem fwd_item(const ProbDev& P, const PlanPtrs& pp
   return I;
 }
 
+// TMEM column of the packed bf16 A operand (P, dS, P^T, dS^T) for k step kk
+// of a 128-key tile: each softmax column half h writes its 64 keys as 32
+// packed columns at 64h, inside its own half of the fp32 tile it read, so
+// the two halves never write where the other still reads.
+__device__ __forceinline__ uint32_t a_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const bool mine = mbar_wait(bar, parity, abort);
   return __all_sync(0xffffffffu, mine);
@@ -77,7 +85,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // K and V tiles sit in separate rings: a K tile is released as soon as the
 // S MMA that reads it completes, long before the PV MMA releases its V tile,
 // so K loads run further ahead of the MMAs than a shared K+V stage allows.
-constexpr int kFwdNK = 3, kFwdNV = 3;
+constexpr int kFwdNK = 3, kFwdNV = 2;
 
 template <int D>
 struct FwdLayout {
@@ -86,7 +94,8 @@ struct FwdLayout {
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k0 = tile;
   static constexpr uint32_t v0 = k0 + kFwdNK * tile;
-  static constexpr uint32_t bars = v0 + kFwdNV * tile;
+  static constexpr uint32_t xchg = v0 + kFwdNV * tile;  // [2 parity][2 half][128] floats
+  static constexpr uint32_t bars = xchg + 2048;
   static constexpr uint32_t total = bars + 512 + 1024;  // + alignment slack
 };
 
@@ -105,11 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + kFwdNK;
   uint64_t* v_full = k_empty + kFwdNK; // [kFwdNV]
   uint64_t* v_empty = v_full + kFwdNV;
-  uint64_t* s_full = v_empty + kFwdNV;  // [2]
-  uint64_t* p_ready = s_full + 2;     // [2]
-  uint64_t* pv_done = p_ready + 2;
-  uint64_t* o_free = pv_done + 1;
+  uint64_t* s_full = v_empty + kFwdNV;  // [3] S buffer b holds tile t with t % 3 == b
+  uint64_t* p_ready = s_full + 3;       // [3]
+  uint64_t* pv_done = p_ready + 3;      // [2] PV of tile t completes phase t / 2 of [t % 2]
+  uint64_t* o_free = pv_done + 2;
   uint64_t* mma_drain = o_free + 1;
+  uint64_t* xbar = mma_drain + 1;  // [4] row-max / row-sum exchange per lane quadrant
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -118,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(xbar + q, 64);
     for (int s = 0; s < kFwdNK; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -126,12 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(v_full + s, 1);
       mbar_init(v_empty + s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(s_full + b, 1);
-      mbar_init(p_ready + b, 4);
+      mbar_init(p_ready + b, kSoftmaxWarps);
     }
     mbar_init(pv_done, 1);
-    mbar_init(o_free, 4);
+    mbar_init(pv_done + 1, 1);
+    mbar_init(o_free, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -144,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 256;
+  const uint32_t tS = tmem, tO = tmem + 384;  // three 128-column S buffers, then O
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
@@ -198,95 +210,141 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
-      const uint32_t q_addr = smem_u32(smem + Lay::q);
+      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
+      // S of tile t is issued as soon as its K tile lands (its buffer was
+      // freed by the PV of tile t-3, issued long before); the PV of a tile is
+      // issued two tiles later, so the tensor pipe always holds the next S
+      // while the softmax warps work.
       uint32_t ns = 0, nit = 0;  // ns: tiles issued (S buffer, K and V ring index)
       bool ok = true;
-      bool pend = false, pend_first = false;
-      uint32_t pend_s = 0, pend_item = 0;
-      auto issue_pv = [&]() -> bool {
-        const uint32_t sb = pend_s & 1;
-        const uint32_t vs = pend_s % kFwdNV;
-        if (!mbar_wait(p_ready + sb, (pend_s >> 1) & 1, abort_flag)) return false;
-        if (pend_first && pend_item > 0 && !mbar_wait(o_free, (pend_item - 1) & 1, abort_flag))
-          return false;
-        if (!mbar_wait(v_full + vs, (pend_s / kFwdNV) & 1, abort_flag)) return false;
+      // pending PVs, oldest in slot a (two named slots keep them in registers)
+      uint32_t a_t = 0, a_item = 0, b_t = 0, b_item = 0;
+      bool a_first = false, b_first = false;
+      int fifo_n = 0;
+      auto issue_pv = [&](uint32_t t_, bool first, uint32_t item) -> bool {
+        const uint32_t sb = t_ % 3;
+        const uint32_t vs = t_ % kFwdNV;
+        if (!warp_wait(p_ready + sb, (t_ / 3) & 1, abort_flag)) return false;
+        if (first && item > 0 && !warp_wait(o_free, (item - 1) & 1, abort_flag)) return false;
+        if (!warp_wait(v_full + vs, (t_ / kFwdNV) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + Lay::v0 + vs * Lay::tile);
+        const uint64_t vd0 = desc_mnmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
+        const uint32_t ta = tS + sb * 128;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_ts(tO, tS + sb * 128 + kk * 8, desc_mnmajor(v_addr, kk), kIdPV,
-                 (pend_first && kk == 0) ? 0u : 1u);
-        mma_commit(v_empty + vs);
-        mma_commit(pv_done);
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            mma_ts(tO, ta + a_col(kk), vd0 + (mnmajor_off(kk) >> 4), kIdPV,
+                   (first && kk == 0) ? 0u : 1u);
+          mma_commit(v_empty + vs);
+          mma_commit(pv_done + (t_ & 1));
+        }
+        __syncwarp();
         return true;
+      };
+      auto pop = [&]() -> bool {
+        const bool r_ = issue_pv(a_t, a_first, a_item);
+        a_t = b_t;
+        a_first = b_first;
+        a_item = b_item;
+        --fifo_n;
+        return r_;
       };
       for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
+        if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
         tc_fence_after();
         for (int t = 0; t < I.ntiles; ++t, ++ns) {
           const uint32_t ks = ns % kFwdNK;
-          if (!(ok = mbar_wait(k_full + ks, (ns / kFwdNK) & 1, abort_flag))) break;
+          if (!(ok = warp_wait(k_full + ks, (ns / kFwdNK) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
-          const uint32_t sb = ns & 1;
+          const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
+          const uint32_t sb = ns % 3;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tS + sb * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(s_full + sb);
-          mma_commit(k_empty + ks);
-          if (t == I.ntiles - 1) mma_commit(q_empty);
-          if (pend && !(ok = issue_pv())) break;
-          pend = true;
-          pend_s = ns;
-          pend_first = (t == 0);
-          pend_item = nit;
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tS + sb * 128, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(s_full + sb);
+            mma_commit(k_empty + ks);
+            if (t == I.ntiles - 1) mma_commit(q_empty);
+          }
+          __syncwarp();
+          if (fifo_n == 2 && !(ok = pop())) break;
+          if (fifo_n == 0) {
+            a_t = ns;
+            a_first = (t == 0);
+            a_item = nit;
+          } else {
+            b_t = ns;
+            b_first = (t == 0);
+            b_item = nit;
+          }
+          ++fifo_n;
         }
       }
-      if (ok && pend) ok = issue_pv();
-      mma_commit(mma_drain);
+      while (ok && fifo_n > 0) ok = pop();
+      if (elect_one()) mma_commit(mma_drain);
+      __syncwarp();
       mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
   } else {
-    // ---------------- softmax + epilogue (warps 2..5) ----------------
+    // ---------------- softmax + epilogue (warps 2..9) ----------------
+    // Warp w owns TMEM lane quadrant w % 4 (rows r) and column half hf of S
+    // and O; the two warps of a quadrant exchange their row maxima every tile
+    // (and their row sums at the end of an item) through shared memory,
+    // paced by that quadrant's 64-thread mbarrier.
+    constexpr int OH = D / 2;
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
-    uint32_t ns = 0, npv = 0;
+    float* xm = (float*)(smem + Lay::xchg);
+    uint32_t ns = 0, nx = 0;
     bool ok = true;
+    auto exchange = [&](float mine, float* other) -> bool {
+      float* buf = xm + (nx & 1) * 256;
+      buf[hf * 128 + r] = mine;
+      mbar_arrive(xbar + wq);
+      const bool got = warp_wait(xbar + wq, nx & 1, abort_flag);
+      *other = buf[(1 - hf) * 128 + r];
+      ++nx;
+      return got;
+    };
     for (int qi = q0; qi < q1 && ok; ++qi) {
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
       const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
-      float m_run = -INFINITY, l = 0.f;
+      float m_run = -INFINITY, l = 0.f;  // l: this half's partial row sum
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
-        const uint32_t sb = ns & 1;
-        if (!(ok = warp_wait(s_full + sb, (ns >> 1) & 1, abort_flag))) break;
+        const uint32_t sb = ns % 3;
+        if (!(ok = warp_wait(s_full + sb, (ns / 3) & 1, abort_flag))) break;
         tc_fence_after();
         // padding rows (beyond the slab's blocks) compute on whatever Q rows the
         // tile box holds; their partials are never read
-        const int lim = ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
-        const uint32_t sa = tS + lane_base + sb * 128;
-        uint32_t x[128];  // raw scores of the row (masked entries -> -inf)
-        tmem_ld_row<128>(sa, x);
-        if (!__all_sync(0xffffffffu, lim >= kKeyTile)) {
+        const int lim = (ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile)) -
+                        64 * hf;
+        const uint32_t sa = tS + lane_base + sb * 128 + 64 * hf;
+        uint32_t x[64];  // raw scores of this half row (masked entries -> -inf)
+        tmem_ld_row<64>(sa, x);
+        if (!__all_sync(0xffffffffu, lim >= 64)) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             if (i >= lim) x[i] = __float_as_uint(-INFINITY);
         }
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
 #pragma unroll
-        for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
+        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
 #pragma unroll
         for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        float mo;
+        if (!(ok = exchange(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), &mo))) break;
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), mo) * sl2;
         const float m_new = fmaxf(m_run, mt);
         float fac = 1.f;
         bool resc = false;
@@ -301,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float lsum[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) lsum[k] = 0.f;
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 32; ++i) {
           const float p0 = ex2(fmaf(__uint_as_float(x[2 * i]), sl2, nmu));
           const float p1 = ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl2, nmu));
           lsum[i & 7] += p0 + p1;
@@ -313,21 +371,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k) lsum[k] += lsum[k + 4];
         const float ls = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
         l = (t == 0) ? ls : l * fac + ls;
-        tmem_st64(sa, pk);
+        tmem_st32(tS + lane_base + sb * 128 + 64 * hf, pk);  // packed P of this half: a_col()
         tmem_st_wait();
-        if (t > 0) {
-          if (!(ok = warp_wait(pv_done, npv & 1, abort_flag))) break;
-          ++npv;
+        // O holds the PVs of tiles before t only once the PV of tile t-1 is
+        // done; wait for it only when O must be rescaled (rare). Alternating
+        // barriers keep the parity test unambiguous although PVs run up to
+        // two tiles behind.
+        if (t > 0 && __any_sync(0xffffffffu, resc)) {  // same decision in both halves
+          const uint32_t pt = ns - 1;
+          if (!(ok = warp_wait(pv_done + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
+          {
+            uint32_t v[OH];
+            tmem_ld_row<OH>(tO + lane_base + OH * hf, v);
 #pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-              uint32_t v[32];
-              tmem_ld32(tO + lane_base + 32 * j, v);
-              tmem_ld_wait(v);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac);
-              tmem_st32(tO + lane_base + 32 * j, v);
+            for (int i = 0; i < OH; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac);
+            if constexpr (OH == 64) {
+              tmem_st64(tO + lane_base + OH * hf, v);
+            } else {
+              tmem_st32(tO + lane_base + OH * hf, v);
             }
             tmem_st_wait();
           }
@@ -337,21 +399,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_ready + sb);
       }
       if (!ok) break;
-      if (!(ok = warp_wait(pv_done, npv & 1, abort_flag))) break;
-      ++npv;
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* po = wk.part_o + (I.slot * kRows + r) * D;
       {
-        uint32_t v[D];
-        tmem_ld_row<D>(tO + lane_base, v);
+        // PV of the item's last tile L: first the PV of L-1 (then, in issue
+        // order, L-2 is done too), so that barrier L % 2 is at most one phase
+        // behind when its parity is tested.
+        const uint32_t pt = ns - 1;
+        if (pt >= 1 && !(ok = warp_wait(pv_done + ((pt - 1) & 1), ((pt - 1) >> 1) & 1, abort_flag)))
+          break;
+        if (!(ok = warp_wait(pv_done + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
+      }
+      tc_fence_after();
+      float lo;
+      if (!(ok = exchange(l, &lo))) break;
+      const float lt = hf == 0 ? l + lo : lo + l;  // same order in both halves
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      float* po = wk.part_o + (I.slot * kRows + r) * D + OH * hf;
+      {
+        uint32_t v[OH];
+        tmem_ld_row<OH>(tO + lane_base + OH * hf, v);
 #pragma unroll
-        for (int i = 0; i < D; i += 4)
+        for (int i = 0; i < OH; i += 4)
           *(float4*)(po + i) =
               make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
                           __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
       }
-      wk.part_lse[I.slot * kRows + r] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+      if (hf == 0) wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
@@ -401,10 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + kDqNK;
   uint64_t* v_full = k_empty + kDqNK;   // [kDqNV]
   uint64_t* v_empty = v_full + kDqNV;
-  uint64_t* s_full = v_empty + kDqNV;   // [2] S of tile t is in TMEM (alternating)
-  uint64_t* dp_full = s_full + 2;
-  uint64_t* p_ready = dp_full + 1;     // softmax wrote dS (bf16) over S
-  uint64_t* dq_done = p_ready + 1;
+  uint64_t* s_full = v_empty + kDqNV;  // S of tile t is in TMEM
+  uint64_t* s_read = s_full + 1;       // softmax has loaded S: its region is free
+  uint64_t* dp_full = s_read + 1;      // [2] dP of tile t (alternating)
+  uint64_t* p_ready = dp_full + 2;     // [2] softmax wrote dS (bf16) over dP of tile t
+  uint64_t* dq_done = p_ready + 2;
   uint64_t* dq_free = dq_done + 1;
   uint64_t* mma_drain = dq_free + 1;
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
@@ -424,11 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(v_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_full + 1, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_ready, 4);
+    mbar_init(s_read, kSoftmaxWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(dp_full + b, 1);
+      mbar_init(p_ready + b, kSoftmaxWarps);
+    }
     mbar_init(dq_done, 1);
-    mbar_init(dq_free, 4);
+    mbar_init(dq_free, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -441,7 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tdQ = tmem + 384;  // regions 0..2 (128 cols each) rotate S / dP
+  // TMEM: S at columns 0..127 (released as soon as the softmax has loaded it),
+  // dP of tile t (then dS over it) at region 1 + t % 2, dQ at 384.
+  const uint32_t tdQ = tmem + 384;
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
@@ -498,56 +575,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {  // MMA issuer: the whole warp, one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t q_addr = smem_u32(smem + Lay::q);
-      const uint32_t do_addr = smem_u32(smem + Lay::dO);
+      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
+      const uint64_t dod0 = desc_kmajor0(smem_u32(smem + Lay::dO));
       uint32_t gt = 0, nit = 0;  // gt: tiles issued (TMEM region, K and V ring index)
       bool ok = true;
       bool pend = false, pend_first = false, pend_last = false;
       uint32_t pend_t = 0, pend_item = 0;
       auto issue_dq = [&]() -> bool {
-        if (!mbar_wait(p_ready, pend_t & 1, abort_flag)) return false;
-        if (pend_first && pend_item > 0 && !mbar_wait(dq_free, (pend_item - 1) & 1, abort_flag))
+        if (!warp_wait(p_ready + (pend_t & 1), (pend_t >> 1) & 1, abort_flag)) return false;
+        if (pend_first && pend_item > 0 && !warp_wait(dq_free, (pend_item - 1) & 1, abort_flag))
           return false;
         tc_fence_after();
-        const uint32_t rS = (2 * pend_t) % 3;
+        const uint32_t rP = 1 + (pend_t & 1);
         const uint32_t ks = pend_t % kDqNK;
-        const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
+        const uint64_t kd0 = desc_mnmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
+        const uint32_t ta = tmem + rP * 128;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_ts(tdQ, tmem + rS * 128 + kk * 8, desc_mnmajor(k_addr, kk), kIdQ,
-                 (pend_first && kk == 0) ? 0u : 1u);
-        mma_commit(k_empty + ks);
-        if (pend_last) mma_commit(dq_done);
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            mma_ts(tdQ, ta + a_col(kk), kd0 + (mnmajor_off(kk) >> 4), kIdQ,
+                   (pend_first && kk == 0) ? 0u : 1u);
+          mma_commit(k_empty + ks);
+          if (pend_last) mma_commit(dq_done);
+        }
+        __syncwarp();
         return true;
       };
+      // per tile: [S region free] S, dP, then the dQ MMA of the previous tile
+      // once its dS is written; dP lands on the region the dQ MMA of tile t-2
+      // read (issued before, in order).
       for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (!(ok = mbar_wait(q_full, nit & 1, abort_flag))) break;
+        if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
         tc_fence_after();
         for (int t = 0; t < I.ntiles; ++t, ++gt) {
           const uint32_t ks = gt % kDqNK, vs = gt % kDqNV;
-          if (!(ok = mbar_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
+          if (!(ok = warp_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
+          if (!(ok = warp_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
+          if (gt > 0 && !(ok = warp_wait(s_read, (gt - 1) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + Lay::k0 + ks * Lay::tile);
-          const uint32_t v_addr = smem_u32(smem + Lay::v0 + vs * Lay::tile);
-          const uint32_t rS = (2 * gt) % 3, rP = (2 * gt + 1) % 3;
+          const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
+          const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
+          const uint32_t rP = 1 + (gt & 1);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + rS * 128, desc_kmajor(q_addr, kk), desc_kmajor(k_addr, kk), kIdS,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(s_full + (gt & 1));
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(s_full);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + rP * 128, dod0 + (kmajor_off(kk) >> 4), vd0 + (kmajor_off(kk) >> 4),
+                     kIdS, kk > 0 ? 1u : 0u);
+            mma_commit(dp_full + (gt & 1));
+            mma_commit(v_empty + vs);
+            if (t == I.ntiles - 1) mma_commit(q_empty);
+          }
+          __syncwarp();
           if (pend && !(ok = issue_dq())) break;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + rP * 128, desc_kmajor(do_addr, kk), desc_kmajor(v_addr, kk), kIdS,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(dp_full);
-          mma_commit(v_empty + vs);
-          if (t == I.ntiles - 1) mma_commit(q_empty);
           pend = true;
           pend_t = gt;
           pend_first = (t == 0);
@@ -556,11 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok && pend) ok = issue_dq();
-      mma_commit(mma_drain);
+      if (elect_one()) mma_commit(mma_drain);
+      __syncwarp();
       mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
   } else {
+    // softmax + epilogue (warps 2..9): lane quadrant warp % 4, column half hf
+    constexpr int OH = D / 2;
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
@@ -576,59 +668,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         Dr = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
       }
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
-        if (!(ok = warp_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(s_full, gt & 1, abort_flag))) break;
         tc_fence_after();
-        const int lim = ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile);
-        const uint32_t sa = tmem + lane_base + ((2 * gt) % 3) * 128;
-        const uint32_t pa = tmem + lane_base + ((2 * gt + 1) % 3) * 128;
-        // phase 1 (while dQ of the previous tile and dP of this one run):
+        const int lim =
+            (ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile)) - 64 * hf;
+        const uint32_t sa = tmem + lane_base + 64 * hf;
+        const uint32_t pa = tmem + lane_base + (1 + (gt & 1)) * 128 + 64 * hf;
+        // phase 1 (while dP of this tile and dQ of the previous one run):
         // P = exp(S * scale - LSE) on the row's visible keys, kept as bf16
-        uint32_t pk[64];
+        uint32_t pk[32];
         {
-          uint32_t sv[128];
-          tmem_ld_row<128>(sa, sv);
-          if (__all_sync(0xffffffffu, lim >= kKeyTile)) {
+          uint32_t sv[64];
+          tmem_ld_row<64>(sa, sv);
+          tc_fence_before();  // S is in registers: let the next S overwrite it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_read);
+          if (__all_sync(0xffffffffu, lim >= 64)) {
 #pragma unroll
-            for (int i = 0; i < 128; i += 2)
+            for (int i = 0; i < 64; i += 2)
               pk[i / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)),
                                     ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)));
           } else {
 #pragma unroll
-            for (int i = 0; i < 128; i += 2) {
+            for (int i = 0; i < 64; i += 2) {
               const float p0 = (i < lim) ? ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)) : 0.f;
               const float p1 = (i + 1 < lim) ? ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)) : 0.f;
               pk[i / 2] = pack_bf16(p0, p1);
             }
           }
         }
-        // phase 2: dS = P * (dP - D)
-        if (!(ok = warp_wait(dp_full, gt & 1, abort_flag))) break;
+        // phase 2: dS = P * (dP - D), written over this half's dP columns
+        if (!(ok = warp_wait(dp_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         {
-          uint32_t dv[128];
-          tmem_ld_row<128>(pa, dv);
+          uint32_t dv[64];
+          tmem_ld_row<64>(pa, dv);
 #pragma unroll
-          for (int i = 0; i < 128; i += 2) {
+          for (int i = 0; i < 64; i += 2) {
             const uint32_t pp2 = pk[i / 2];
             pk[i / 2] = pack_bf16(__uint_as_float(pp2 << 16) * (__uint_as_float(dv[i]) - Dr),
                                   __uint_as_float(pp2 & 0xffff0000u) * (__uint_as_float(dv[i + 1]) - Dr));
           }
         }
-        tmem_st64(sa, pk);
+        tmem_st32(pa, pk);  // packed dS of this half: columns a_col() of the dP region
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready);
+        if (lane == 0) mbar_arrive(p_ready + (gt & 1));
       }
       if (!ok) break;
       if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
       tc_fence_after();
-      float* po = wk.part_o + (I.slot * kRows + r) * D;
+      float* po = wk.part_o + (I.slot * kRows + r) * D + OH * hf;
       {
-        uint32_t v[D];
-        tmem_ld_row<D>(tdQ + lane_base, v);
+        uint32_t v[OH];
+        tmem_ld_row<OH>(tdQ + lane_base + OH * hf, v);
 #pragma unroll
-        for (int i = 0; i < D; i += 4)
+        for (int i = 0; i < OH; i += 4)
           *(float4*)(po + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
       }
@@ -718,10 +814,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 4);
-    mbar_init(ds_ready, 4);
+    mbar_init(p_ready, kSoftmaxWarps);
+    mbar_init(ds_ready, kSoftmaxWarps);
     mbar_init(acc_done, 1);
-    mbar_init(acc_free, 4);
+    mbar_init(acc_free, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -778,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {  // MMA issuer: the whole warp, one elected lane issues
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
       const uint32_t k_addr = smem_u32(smem + Lay::k);
@@ -787,19 +883,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dK — the next S^T is queued before dK so the tensor pipe has work
       // while the softmax warps turn dP^T into dS^T. TMEM reuse is safe
       // because tcgen05 MMAs of one thread execute in issue order.
+      const uint64_t kd0 = desc_kmajor0(k_addr), vd0 = desc_kmajor0(v_addr);
       auto issue_s = [&](uint32_t stage) {
-        const uint32_t q_addr = smem_u32(smem + Lay::stage0 + stage * Lay::stage_bytes);
+        const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::stage0 + stage * Lay::stage_bytes));
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tS, desc_kmajor(k_addr, kk), desc_kmajor(q_addr, kk), kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(s_full);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS, kd0 + (kmajor_off(kk) >> 4), qd0 + (kmajor_off(kk) >> 4), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(s_full);
+        }
+        __syncwarp();
       };
       uint32_t nst = 0, nit = 0;
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
         const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
-        if (!(ok = mbar_wait(kv_full, nit & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(kv_full, nit & 1, abort_flag))) break;
+        if (!(ok = warp_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
         tc_fence_after();
         issue_s(nst % kNS);
         for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
@@ -807,37 +908,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
           const uint32_t do_addr = q_addr + kSub * kSubBytes;
           const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
+          const uint64_t dod0 = desc_kmajor0(do_addr);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tP, desc_kmajor(v_addr, kk), desc_kmajor(do_addr, kk), kIdS, kk > 0 ? 1u : 0u);
-          mma_commit(dp_full);
-          if (last) mma_commit(kv_empty);  // K and V are not read after this
-          if (!(ok = mbar_wait(p_ready, nst & 1, abort_flag))) break;
-          if (first && nit > 0 && !(ok = mbar_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tP, vd0 + (kmajor_off(kk) >> 4), dod0 + (kmajor_off(kk) >> 4), kIdS,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(dp_full);
+            if (last) mma_commit(kv_empty);  // K and V are not read after this
+          }
+          __syncwarp();
+          if (!(ok = warp_wait(p_ready, nst & 1, abort_flag))) break;
+          if (first && nit > 0 && !(ok = warp_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
           tc_fence_after();
+          const uint64_t dom0 = desc_mnmajor0(do_addr);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk)
-            mma_ts(tdV, tS + kk * 8, desc_mnmajor(do_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_ts(tdV, tS + a_col(kk), dom0 + (mnmajor_off(kk) >> 4), kIdKV,
+                     (first && kk == 0) ? 0u : 1u);
+          }
+          __syncwarp();
           if (!last) {
             const uint32_t s2 = (nst + 1) % kNS;
-            if (!(ok = mbar_wait(st_full + s2, ((nst + 1) / kNS) & 1, abort_flag))) break;
+            if (!(ok = warp_wait(st_full + s2, ((nst + 1) / kNS) & 1, abort_flag))) break;
             tc_fence_after();
             issue_s(s2);
           }
-          if (!(ok = mbar_wait(ds_ready, nst & 1, abort_flag))) break;
+          if (!(ok = warp_wait(ds_ready, nst & 1, abort_flag))) break;
           tc_fence_after();
+          const uint64_t qm0 = desc_mnmajor0(q_addr);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk)
-            mma_ts(tdK, tP + kk * 8, desc_mnmajor(q_addr, kk), kIdKV, (first && kk == 0) ? 0u : 1u);
-          mma_commit(st_empty + s);
-          if (last) mma_commit(acc_done);
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_ts(tdK, tP + a_col(kk), qm0 + (mnmajor_off(kk) >> 4), kIdKV,
+                     (first && kk == 0) ? 0u : 1u);
+            mma_commit(st_empty + s);
+            if (last) mma_commit(acc_done);
+          }
+          __syncwarp();
         }
       }
-      mma_commit(mma_drain);
+      if (elect_one()) mma_commit(mma_drain);
+      __syncwarp();
       mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
   } else {
+    // softmax + epilogue (warps 2..9): key lane quadrant warp % 4, row half hf
+    constexpr int OH = D / 2;
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = wq * 32 + lane;  // key of the tile owned by this thread
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
@@ -848,32 +968,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = I.ks0 + r;
       for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
         const uint32_t s = nst % kNS;
-        // row info of the stage was written by the producer warp: acquire it
-        // through the stage barrier (already complete; it cannot advance before
-        // this slab's dS^T is consumed).
+        // row table of the stage: acquire it through the stage barrier
+        // (already complete; it cannot advance before this slab's dS^T is
+        // consumed), then wait for S^T.
         if (!(ok = warp_wait(st_full + s, (nst / kNS) & 1, abort_flag))) break;
         if (!(ok = warp_wait(s_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
-        const float* nl2 = (const float*)(sb + Lay::info_off);  // -LSE*log2(e), -inf on padding
+        const float* nl2 = (const float*)(sb + Lay::info_off) + 64 * hf;  // -LSE*log2(e)
         const float* dvv = nl2 + kRows;
         const int* anc = (const int*)(dvv + kRows);
+        const int* anc0 = anc - 64 * hf;  // the slab's first row: its smallest anchor
         // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs.
         // Rows are ordered by block and anchors rise with the block, so a key
         // below the slab's first anchor is seen by every row (padding rows give
         // 0 through their -inf): no per-element mask on such warps.
-        uint32_t pk[64];
+        uint32_t pk[32];
         {
-          uint32_t sv[128];
-          tmem_ld_row<128>(tS + lane_base, sv);
-          if (__all_sync(0xffffffffu, key < anc[0])) {
+          uint32_t sv[64];
+          tmem_ld_row<64>(tS + lane_base + 64 * hf, sv);
+          if (__all_sync(0xffffffffu, key < anc0[0])) {
 #pragma unroll
-            for (int c = 0; c < 128; c += 2)
+            for (int c = 0; c < 64; c += 2)
               pk[c / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])),
                                     ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])));
           } else {
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
+            for (int c = 0; c < 64; c += 2) {
               const float p0 = key < anc[c] ? ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])) : 0.f;
               const float p1 =
                   key < anc[c + 1] ? ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])) : 0.f;
@@ -881,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tmem_st64(tS + lane_base, pk);
+        tmem_st32(tS + lane_base + 64 * hf, pk);  // packed P^T of this half: columns a_col()
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -890,17 +1011,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(dp_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         {
-          uint32_t dv[128];
-          tmem_ld_row<128>(tP + lane_base, dv);
+          uint32_t dv[64];
+          tmem_ld_row<64>(tP + lane_base + 64 * hf, dv);
 #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
+          for (int c = 0; c < 64; c += 2) {
             const uint32_t pp2 = pk[c / 2];
             const float p0 = __uint_as_float(pp2 << 16), p1 = __uint_as_float(pp2 & 0xffff0000u);
             pk[c / 2] = pack_bf16(p0 * (__uint_as_float(dv[c]) - dvv[c]),
                                   p1 * (__uint_as_float(dv[c + 1]) - dvv[c + 1]));
           }
         }
-        tmem_st64(tP + lane_base, pk);
+        tmem_st32(tP + lane_base + 64 * hf, pk);  // packed dS^T of this half
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -910,15 +1031,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(acc_done, nit & 1, abort_flag))) break;
       tc_fence_after();
       const bool valid = key < I.L;
-      const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D;
+      const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D + OH * hf;
       for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled)
-        uint32_t a[D];
-        tmem_ld_row<D>((which == 0 ? tdV : tdK) + lane_base, a);
+        uint32_t a[OH];
+        tmem_ld_row<OH>((which == 0 ? tdV : tdK) + lane_base + OH * hf, a);
         const float f = which == 0 ? 1.f : P.scale;
         __nv_bfloat16* dst = (which == 0 ? dVc : dKc) + off;
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < D; i += 8) {
+          for (int i = 0; i < OH; i += 8) {
             uint4 pv;
             pv.x = pack_bf16(__uint_as_float(a[i]) * f, __uint_as_float(a[i + 1]) * f);
             pv.y = pack_bf16(__uint_as_float(a[i + 2]) * f, __uint_as_float(a[i + 3]) * f);

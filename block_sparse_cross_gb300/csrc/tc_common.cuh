@@ -153,6 +153,20 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// True in exactly one lane of a converged warp (the lowest). An MMA-issuing
+// warp runs its whole control loop with all 32 lanes, so that every value it
+// feeds the tensor unit (descriptors, TMEM addresses) is warp-uniform, and
+// lets this lane alone issue the MMAs and their commits.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // Arrives on `bar` once every previously issued tcgen05 op of this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -178,6 +192,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= (uint64_t)1 << 46;  // descriptor version (sm_100 family)
   d |= (uint64_t)2 << 61;  // 128-byte swizzle
   return d;
+}
+
+// Byte offset of k step kk (16 elements) inside a K-major / MN-major tile.
+__host__ __device__ constexpr uint32_t kmajor_off(int kk) {
+  return (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+}
+__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return (uint32_t)kk * 2048u; }
+// Descriptor of a tile's first k step; the descriptor of step kk is this
+// plus off(kk) / 16 (the start-address field is bits 0..13 in 16-byte units
+// and shared-memory addresses stay below 2^18 bytes, so no carry leaves it).
+__device__ __forceinline__ uint64_t desc_kmajor0(uint32_t tile_saddr) {
+  return sdesc_sw128(tile_saddr, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor0(uint32_t tile_saddr) {
+  return sdesc_sw128(tile_saddr, 16384u, 1024u);
 }
 
 // K-major operand: 128 rows x D (sub-tiles of 64), k step kk of 16 elements.
@@ -258,16 +287,25 @@ __device__ __forceinline__ void tmem_ld_wait64(uint32_t (&r)[64]) {
                :
                : "memory");
 }
-// A whole row of N (64 or 128) fp32 columns: one load, one wait.
+// A whole row of N (32, 64 or 128) fp32 columns: one load, one wait.
 template <int N>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[N]) {
   if constexpr (N == 128) {
     tmem_ld128(taddr, r);
     tmem_ld_wait128(r);
-  } else {
+  } else if constexpr (N == 64) {
     tmem_ld64(taddr, r);
     tmem_ld_wait64(r);
+  } else {
+    static_assert(N == 32, "row width");
+    tmem_ld32(taddr, r);
+    tmem_ld_wait(r);
   }
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
