@@ -37,6 +37,7 @@ using namespace tc;
 
 constexpr int kNS = 2;               // pipeline stages
 constexpr int kThreads = 320;    // producer warp, MMA warp, 8 softmax warps
+constexpr int kFwdThreads = 352; // forward: + a second MMA-issuing warp (PV)
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
 constexpr float kLn2 = 0.6931471805599453f;
@@ -100,7 +101,7 @@ struct FwdLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, ProbDev P, PlanPtrs pp, WorkPtrs wk) {
   using Lay = FwdLayout<D>;
@@ -108,18 +109,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
+  // Tile t (counted over the CTA's items) uses S buffer, K stage and the
+  // barriers below at index t % 3, and V stage t % 2. S of tile t is issued
+  // once PV of tile t-3 (same buffer) is done; PV of tile t once its P is
+  // written. The K stage is free when S is done (s_full), the V stage when
+  // PV is done (sfree of that tile).
+  static_assert(kFwdNK == 3 && kFwdNV == 2, "ring sizes tied to the S buffers");
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;         // [kFwdNK]
-  uint64_t* k_empty = k_full + kFwdNK;
-  uint64_t* v_full = k_empty + kFwdNK; // [kFwdNV]
-  uint64_t* v_empty = v_full + kFwdNV;
-  uint64_t* s_full = v_empty + kFwdNV;  // [3] S buffer b holds tile t with t % 3 == b
-  uint64_t* p_ready = s_full + 3;       // [3]
-  uint64_t* pv_done = p_ready + 3;      // [2] PV of tile t completes phase t / 2 of [t % 2]
-  uint64_t* o_free = pv_done + 2;
-  uint64_t* mma_drain = o_free + 1;
-  uint64_t* xbar = mma_drain + 1;  // [4] row-max / row-sum exchange per lane quadrant
+  uint64_t* k_full = bars + 2;          // [3]
+  uint64_t* v_full = k_full + kFwdNK;   // [2]
+  uint64_t* s_full = v_full + kFwdNV;   // [3] S of tile t is in buffer t % 3
+  uint64_t* p_ready = s_full + 3;       // [3] its P (bf16) is written over it
+  uint64_t* sfree = p_ready + 3;        // [3] PV of tile t is done
+  uint64_t* o_free = sfree + 3;         // the epilogue has read O
+  uint64_t* mma_drain = o_free + 1;     // [2] one per issuing warp
+  uint64_t* xbar = mma_drain + 2;       // [4] row-max / row-sum exchange per lane quadrant
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -129,22 +134,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int q = 0; q < 4; ++q) mbar_init(xbar + q, 64);
-    for (int s = 0; s < kFwdNK; ++s) {
-      mbar_init(k_full + s, 1);
-      mbar_init(k_empty + s, 1);
-    }
-    for (int s = 0; s < kFwdNV; ++s) {
-      mbar_init(v_full + s, 1);
-      mbar_init(v_empty + s, 1);
-    }
+    for (int s = 0; s < kFwdNK; ++s) mbar_init(k_full + s, 1);
+    for (int s = 0; s < kFwdNV; ++s) mbar_init(v_full + s, 1);
     for (int b = 0; b < 3; ++b) {
       mbar_init(s_full + b, 1);
       mbar_init(p_ready + b, kSoftmaxWarps);
+      mbar_init(sfree + b, 1);
     }
-    mbar_init(pv_done, 1);
-    mbar_init(pv_done + 1, 1);
     mbar_init(o_free, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
+    mbar_init(mma_drain + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -175,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nk % kFwdNK, u = nk / kFwdNK;
-          if (u > 0 && !(ok = mbar_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
+          // stage s is free once S of tile nk - 3 is done
+          if (u > 0 && !(ok = mbar_wait(s_full + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
           mbar_expect_tx(k_full + s, Lay::tile);
           for (int i = 0; i < kSub; ++i)
@@ -195,8 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         for (int t = 0; t < I.ntiles; ++t) {
-          const uint32_t s = nv % kFwdNV, u = nv / kFwdNV;
-          if (u > 0 && !(ok = mbar_wait(v_empty + s, (u - 1) & 1, abort_flag))) break;
+          const uint32_t s = nv % kFwdNV;
+          // stage s is free once PV of tile nv - 2 is done
+          if (nv >= 2 && !(ok = mbar_wait(sfree + (nv - 2) % 3, ((nv - 2) / 3) & 1, abort_flag)))
+            break;
           uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
           mbar_expect_tx(v_full + s, Lay::tile);
           for (int i = 0; i < kSub; ++i)
@@ -210,87 +212,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
-    {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
-      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
-      // S of tile t is issued as soon as its K tile lands (its buffer was
-      // freed by the PV of tile t-3, issued long before); the PV of a tile is
-      // issued two tiles later, so the tensor pipe always holds the next S
-      // while the softmax warps work.
-      uint32_t ns = 0, nit = 0;  // ns: tiles issued (S buffer, K and V ring index)
-      bool ok = true;
-      // pending PVs, oldest in slot a (two named slots keep them in registers)
-      uint32_t a_t = 0, a_item = 0, b_t = 0, b_item = 0;
-      bool a_first = false, b_first = false;
-      int fifo_n = 0;
-      auto issue_pv = [&](uint32_t t_, bool first, uint32_t item) -> bool {
-        const uint32_t sb = t_ % 3;
-        const uint32_t vs = t_ % kFwdNV;
-        if (!warp_wait(p_ready + sb, (t_ / 3) & 1, abort_flag)) return false;
-        if (first && item > 0 && !warp_wait(o_free, (item - 1) & 1, abort_flag)) return false;
-        if (!warp_wait(v_full + vs, (t_ / kFwdNV) & 1, abort_flag)) return false;
+    // ---------------- S issuer: the whole warp, one elected lane issues ----------------
+    // A commit holds its thread until the MMAs it tracks are nearly done, so
+    // S and PV are issued by two warps: while one waits on its commit the
+    // other keeps the tensor pipe fed.
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+    const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
+    uint32_t ns = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      for (int t = 0; t < I.ntiles; ++t, ++ns) {
+        const uint32_t b = ns % 3;
+        if (!(ok = warp_wait(k_full + b, (ns / 3) & 1, abort_flag))) break;
+        if (ns >= 3 && !(ok = warp_wait(sfree + b, (ns / 3 - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + b * Lay::tile));
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS + b * 128, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(s_full + b);  // also frees K stage b
+          if (t == I.ntiles - 1) mma_commit(q_empty);
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) mma_commit(mma_drain);
+    __syncwarp();
+    mbar_wait_drain(mma_drain, 0, kDrainNs);
+  } else if (warp == kSoftmaxWarps + 2) {
+    // ---------------- PV issuer ----------------
+    constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+    uint32_t np = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      for (int t = 0; t < I.ntiles; ++t, ++np) {
+        const uint32_t b = np % 3, vs = np % kFwdNV;
+        if (!(ok = warp_wait(p_ready + b, (np / 3) & 1, abort_flag))) break;
+        if (t == 0 && nit > 0 && !(ok = warp_wait(o_free, (nit - 1) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(v_full + vs, (np / kFwdNV) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t vd0 = desc_mnmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
-        const uint32_t ta = tS + sb * 128;
+        const uint32_t ta = tS + b * 128;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk)
             mma_ts(tO, ta + a_col(kk), vd0 + (mnmajor_off(kk) >> 4), kIdPV,
-                   (first && kk == 0) ? 0u : 1u);
-          mma_commit(v_empty + vs);
-          mma_commit(pv_done + (t_ & 1));
+                   (t == 0 && kk == 0) ? 0u : 1u);
+          mma_commit(sfree + b);
         }
         __syncwarp();
-        return true;
-      };
-      auto pop = [&]() -> bool {
-        const bool r_ = issue_pv(a_t, a_first, a_item);
-        a_t = b_t;
-        a_first = b_first;
-        a_item = b_item;
-        --fifo_n;
-        return r_;
-      };
-      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
-        tc_fence_after();
-        for (int t = 0; t < I.ntiles; ++t, ++ns) {
-          const uint32_t ks = ns % kFwdNK;
-          if (!(ok = warp_wait(k_full + ks, (ns / kFwdNK) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
-          const uint32_t sb = ns % 3;
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tS + sb * 128, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
-                     kk > 0 ? 1u : 0u);
-            mma_commit(s_full + sb);
-            mma_commit(k_empty + ks);
-            if (t == I.ntiles - 1) mma_commit(q_empty);
-          }
-          __syncwarp();
-          if (fifo_n == 2 && !(ok = pop())) break;
-          if (fifo_n == 0) {
-            a_t = ns;
-            a_first = (t == 0);
-            a_item = nit;
-          } else {
-            b_t = ns;
-            b_first = (t == 0);
-            b_item = nit;
-          }
-          ++fifo_n;
-        }
       }
-      while (ok && fifo_n > 0) ok = pop();
-      if (elect_one()) mma_commit(mma_drain);
-      __syncwarp();
-      mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
+    if (elect_one()) mma_commit(mma_drain + 1);
+    __syncwarp();
+    mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else {
     // ---------------- softmax + epilogue (warps 2..9) ----------------
     // Warp w owns TMEM lane quadrant w % 4 (rows r) and column half hf of S
@@ -374,12 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tS + lane_base + sb * 128 + 64 * hf, pk);  // packed P of this half: a_col()
         tmem_st_wait();
         // O holds the PVs of tiles before t only once the PV of tile t-1 is
-        // done; wait for it only when O must be rescaled (rare). Alternating
-        // barriers keep the parity test unambiguous although PVs run up to
-        // two tiles behind.
+        // done; wait for it only when O must be rescaled (rare).
         if (t > 0 && __any_sync(0xffffffffu, resc)) {  // same decision in both halves
           const uint32_t pt = ns - 1;
-          if (!(ok = warp_wait(pv_done + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
+          if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
           tc_fence_after();
           {
             uint32_t v[OH];
@@ -400,13 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       {
-        // PV of the item's last tile L: first the PV of L-1 (then, in issue
-        // order, L-2 is done too), so that barrier L % 2 is at most one phase
-        // behind when its parity is tested.
-        const uint32_t pt = ns - 1;
-        if (pt >= 1 && !(ok = warp_wait(pv_done + ((pt - 1) & 1), ((pt - 1) >> 1) & 1, abort_flag)))
-          break;
-        if (!(ok = warp_wait(pv_done + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
+        const uint32_t pt = ns - 1;  // PV of the item's last tile
+        if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
       }
       tc_fence_after();
       float lo;
@@ -417,16 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t v[OH];
         tmem_ld_row<OH>(tO + lane_base + OH * hf, v);
+        tc_fence_before();  // O is in registers: the next item's PVs may overwrite it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
 #pragma unroll
-        for (int i = 0; i < OH; i += 4)
-          *(float4*)(po + i) =
-              make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                          __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+        for (int i = 0; i < OH; i += 8)
+          st_global_v8(po + i, __uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                       __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv,
+                       __uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv,
+                       __uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
       }
       if (hf == 0) wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
     }
   }
 
@@ -471,9 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = bars + 1;
   uint64_t* k_full = bars + 2;          // [kDqNK]
   uint64_t* k_empty = k_full + kDqNK;
+  // V is read only by dP: V stage and dp_full of tile t are both t % 2, so
+  // dP's commit frees the V stage.
+  static_assert(kDqNV == 2, "V ring size tied to dp_full");
   uint64_t* v_full = k_empty + kDqNK;   // [kDqNV]
-  uint64_t* v_empty = v_full + kDqNV;
-  uint64_t* s_full = v_empty + kDqNV;  // S of tile t is in TMEM
+  uint64_t* s_full = v_full + kDqNV;   // S of tile t is in TMEM
   uint64_t* s_read = s_full + 1;       // softmax has loaded S: its region is free
   uint64_t* dp_full = s_read + 1;      // [2] dP of tile t (alternating)
   uint64_t* p_ready = dp_full + 2;     // [2] softmax wrote dS (bf16) over dP of tile t
@@ -492,10 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
     }
-    for (int s = 0; s < kDqNV; ++s) {
-      mbar_init(v_full + s, 1);
-      mbar_init(v_empty + s, 1);
-    }
+    for (int s = 0; s < kDqNV; ++s) mbar_init(v_full + s, 1);
     mbar_init(s_full, 1);
     mbar_init(s_read, kSoftmaxWarps);
     for (int b = 0; b < 2; ++b) {
@@ -561,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nv % kDqNV, u = nv / kDqNV;
-          if (u > 0 && !(ok = mbar_wait(v_empty + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = mbar_wait(dp_full + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
           mbar_expect_tx(v_full + s, Lay::tile);
           for (int i = 0; i < kSub; ++i)
@@ -630,8 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < D / 16; ++kk)
               mma_ss(tmem + rP * 128, dod0 + (kmajor_off(kk) >> 4), vd0 + (kmajor_off(kk) >> 4),
                      kIdS, kk > 0 ? 1u : 0u);
-            mma_commit(dp_full + (gt & 1));
-            mma_commit(v_empty + vs);
+            mma_commit(dp_full + (gt & 1));  // also frees V stage vs == gt % 2
             if (t == I.ntiles - 1) mma_commit(q_empty);
           }
           __syncwarp();
@@ -1124,11 +1096,11 @@ cudaError_t launch_fwd_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& 
   if (P.d == 128) {
     auto k = fwd_tc_kernel<128>;
     if ((e = prep(k, FwdLayout<128>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kThreads, FwdLayout<128>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+    k<<<P.workers, kFwdThreads, FwdLayout<128>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
   } else {
     auto k = fwd_tc_kernel<64>;
     if ((e = prep(k, FwdLayout<64>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kThreads, FwdLayout<64>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+    k<<<P.workers, kFwdThreads, FwdLayout<64>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
   }
   return cudaGetLastError();
 }

@@ -219,6 +219,14 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, int kk) {
   return sdesc_sw128(tile_saddr + (uint32_t)kk * 2048u, 16384u, 1024u);
 }
 
+// 32-byte global store (one full sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float* p, float a0, float a1, float a2, float a3,
+                                             float a4, float a5, float a6, float a7) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a0),
+               "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+               : "memory");
+}
+
 // ---- TMEM <-> registers ----------------------------------------------------
 #define SKV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                   "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
