@@ -36,8 +36,8 @@ namespace {
 using namespace tc;
 
 constexpr int kNS = 2;               // pipeline stages
-constexpr int kThreads = 320;    // producer warp, MMA warp, 8 softmax warps
-constexpr int kFwdThreads = 352; // forward: + a second MMA-issuing warp (PV)
+// producer warp, MMA warp, 8 softmax warps, a second MMA-issuing warp
+constexpr int kThreads = 352;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
 constexpr float kLn2 = 0.6931471805599453f;
@@ -101,7 +101,7 @@ struct FwdLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, ProbDev P, PlanPtrs pp, WorkPtrs wk) {
   using Lay = FwdLayout<D>;
@@ -453,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_read = s_full + 1;       // softmax has loaded S: its region is free
   uint64_t* dp_full = s_read + 1;      // [2] dP of tile t (alternating)
   uint64_t* p_ready = dp_full + 2;     // [2] softmax wrote dS (bf16) over dP of tile t
-  uint64_t* dq_done = p_ready + 2;
+  uint64_t* rfree = p_ready + 2;       // [2] the dQ MMA of tile t has read its dS region
+  uint64_t* dq_done = rfree + 2;
   uint64_t* dq_free = dq_done + 1;
-  uint64_t* mma_drain = dq_free + 1;
+  uint64_t* mma_drain = dq_free + 1;   // [2] one per issuing warp
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -474,10 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(dp_full + b, 1);
       mbar_init(p_ready + b, kSoftmaxWarps);
+      mbar_init(rfree + b, 1);
     }
     mbar_init(dq_done, 1);
     mbar_init(dq_free, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
+    mbar_init(mma_drain + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -548,78 +551,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    {  // MMA issuer: the whole warp, one elected lane issues
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
-      const uint64_t dod0 = desc_kmajor0(smem_u32(smem + Lay::dO));
-      uint32_t gt = 0, nit = 0;  // gt: tiles issued (TMEM region, K and V ring index)
-      bool ok = true;
-      bool pend = false, pend_first = false, pend_last = false;
-      uint32_t pend_t = 0, pend_item = 0;
-      auto issue_dq = [&]() -> bool {
-        if (!warp_wait(p_ready + (pend_t & 1), (pend_t >> 1) & 1, abort_flag)) return false;
-        if (pend_first && pend_item > 0 && !warp_wait(dq_free, (pend_item - 1) & 1, abort_flag))
-          return false;
+    // ---------------- S and dP issuer (whole warp, one elected lane) ----------------
+    // dP of tile t lands on the region the dQ MMA of tile t-2 read: wait for
+    // that MMA (issued by the other warp) through rfree.
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+    const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
+    const uint64_t dod0 = desc_kmajor0(smem_u32(smem + Lay::dO));
+    uint32_t gt = 0, nit = 0;  // gt: tiles issued (TMEM region, K and V ring index)
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      for (int t = 0; t < I.ntiles; ++t, ++gt) {
+        const uint32_t ks = gt % kDqNK, vs = gt % kDqNV;
+        if (!(ok = warp_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
+        if (gt > 0 && !(ok = warp_wait(s_read, (gt - 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t rP = 1 + (pend_t & 1);
-        const uint32_t ks = pend_t % kDqNK;
+        const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
+        const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
+        const uint32_t rP = 1 + (gt & 1);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(s_full);
+        }
+        __syncwarp();
+        if (gt >= 2 && !(ok = warp_wait(rfree + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + rP * 128, dod0 + (kmajor_off(kk) >> 4), vd0 + (kmajor_off(kk) >> 4),
+                   kIdS, kk > 0 ? 1u : 0u);
+          mma_commit(dp_full + (gt & 1));  // also frees V stage vs == gt % 2
+          if (t == I.ntiles - 1) mma_commit(q_empty);  // Q and dO are read by S and dP only
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) mma_commit(mma_drain);
+    __syncwarp();
+    mbar_wait_drain(mma_drain, 0, kDrainNs);
+  } else if (warp == kSoftmaxWarps + 2) {
+    // ---------------- dQ issuer ----------------
+    constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
+    uint32_t gt = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      for (int t = 0; t < I.ntiles; ++t, ++gt) {
+        if (!(ok = warp_wait(p_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+        if (t == 0 && nit > 0 && !(ok = warp_wait(dq_free, (nit - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t ks = gt % kDqNK;
         const uint64_t kd0 = desc_mnmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
-        const uint32_t ta = tmem + rP * 128;
+        const uint32_t ta = tmem + (1 + (gt & 1)) * 128;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk)
             mma_ts(tdQ, ta + a_col(kk), kd0 + (mnmajor_off(kk) >> 4), kIdQ,
-                   (pend_first && kk == 0) ? 0u : 1u);
+                   (t == 0 && kk == 0) ? 0u : 1u);
+          mma_commit(rfree + (gt & 1));
           mma_commit(k_empty + ks);
-          if (pend_last) mma_commit(dq_done);
+          if (t == I.ntiles - 1) mma_commit(dq_done);
         }
         __syncwarp();
-        return true;
-      };
-      // per tile: [S region free] S, dP, then the dQ MMA of the previous tile
-      // once its dS is written; dP lands on the region the dQ MMA of tile t-2
-      // read (issued before, in order).
-      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
-        tc_fence_after();
-        for (int t = 0; t < I.ntiles; ++t, ++gt) {
-          const uint32_t ks = gt % kDqNK, vs = gt % kDqNV;
-          if (!(ok = warp_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
-          if (!(ok = warp_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
-          if (gt > 0 && !(ok = warp_wait(s_read, (gt - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
-          const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
-          const uint32_t rP = 1 + (gt & 1);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
-                     kk > 0 ? 1u : 0u);
-            mma_commit(s_full);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem + rP * 128, dod0 + (kmajor_off(kk) >> 4), vd0 + (kmajor_off(kk) >> 4),
-                     kIdS, kk > 0 ? 1u : 0u);
-            mma_commit(dp_full + (gt & 1));  // also frees V stage vs == gt % 2
-            if (t == I.ntiles - 1) mma_commit(q_empty);
-          }
-          __syncwarp();
-          if (pend && !(ok = issue_dq())) break;
-          pend = true;
-          pend_t = gt;
-          pend_first = (t == 0);
-          pend_last = (t == I.ntiles - 1);
-          pend_item = nit;
-        }
       }
-      if (ok && pend) ok = issue_dq();
-      if (elect_one()) mma_commit(mma_drain);
-      __syncwarp();
-      mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
+    if (elect_one()) mma_commit(mma_drain + 1);
+    __syncwarp();
+    mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else {
     // softmax + epilogue (warps 2..9): lane quadrant warp % 4, column half hf
     constexpr int OH = D / 2;
@@ -695,14 +699,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t v[OH];
         tmem_ld_row<OH>(tdQ + lane_base + OH * hf, v);
+        tc_fence_before();  // dQ is in registers: the next item's MMAs may overwrite it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_free);
 #pragma unroll
-        for (int i = 0; i < OH; i += 4)
-          *(float4*)(po + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        for (int i = 0; i < OH; i += 8)
+          st_global_v8(po + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]),
+                       __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
+                       __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
     }
   }
 
@@ -778,10 +784,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!plan_ok_cta(P, pp.hdr)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // st_full takes one arrival from each of the two producer lanes
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(st_full + s, 1);
+      mbar_init(st_full + s, 2);
       mbar_init(st_empty + s, 1);
     }
     mbar_init(s_full, 1);
@@ -806,8 +813,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.b_qoff[blockIdx.x], q1 = pp.b_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- producer: K/V per item; Q, dO and the slab's row table
-    // (one bulk copy of the precomputed record) per slab ----------------
+    // ---------------- producers: lane 0 K/V per item, then Q and the slab's
+    // row table (one bulk copy of the precomputed record) per slab; lane 1
+    // dO per slab ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
@@ -829,11 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u > 0 && !(ok = mbar_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
           const int n0 = pp.sl_first[sg] * P.B;
-          mbar_expect_tx(st_full + s, 2 * kSub * kSubBytes + kRowInfoFloats * 4);
-          for (int i = 0; i < kSub; ++i) {
+          mbar_expect_tx(st_full + s, kSub * kSubBytes + kRowInfoFloats * 4);
+          for (int i = 0; i < kSub; ++i)
             tma_load_3d(sb + i * kSubBytes, &tmQ, st_full + s, 64 * i, I.g * P.group, n0);
-            tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
-          }
           bulk_load(sb + Lay::info_off, wk.rowinfo + ((size_t)sg * P.Hkv + I.g) * kRowInfoFloats,
                     kRowInfoFloats * 4, st_full + s);
           ++nst;
@@ -844,87 +850,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
           mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
       }
+    } else if (lane == 1) {  // dO of every slab, in parallel with lane 0's Q
+      tma_prefetch_desc(&tmdO);
+      uint32_t nst = 0;
+      bool ok = true;
+      for (int qi = q0; qi < q1 && ok; ++qi) {
+        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+        for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
+          const uint32_t s = nst % kNS, u = nst / kNS;
+          if (u > 0 && !(ok = mbar_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
+          uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
+          const int n0 = pp.sl_first[sg] * P.B;
+          mbar_expect_tx(st_full + s, kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
+          ++nst;
+        }
+      }
+      if (!ok) {
+        for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
+          mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
+      }
     }
   } else if (warp == 1) {
-    {  // MMA issuer: the whole warp, one elected lane issues
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
-      const uint32_t k_addr = smem_u32(smem + Lay::k);
-      const uint32_t v_addr = smem_u32(smem + Lay::v);
-      // Per slab: S^T, dP^T, [P^T ready] dV, S^T of the next slab, [dS^T ready]
-      // dK — the next S^T is queued before dK so the tensor pipe has work
-      // while the softmax warps turn dP^T into dS^T. TMEM reuse is safe
-      // because tcgen05 MMAs of one thread execute in issue order.
-      const uint64_t kd0 = desc_kmajor0(k_addr), vd0 = desc_kmajor0(v_addr);
-      auto issue_s = [&](uint32_t stage) {
-        const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::stage0 + stage * Lay::stage_bytes));
+    // ---------------- MMA issuer (whole warp, one elected lane) ----------------
+    // Per slab: S^T, dP^T, [P^T ready] dV, S^T of the next slab, [dS^T ready]
+    // dK — the next S^T is queued before dK so the tensor pipe has work
+    // while the softmax warps turn dP^T into dS^T. TMEM reuse is safe
+    // because tcgen05 MMAs of one thread execute in issue order. Every
+    // 128x128 product here reads both operands from shared memory, whose
+    // bandwidth the MMAs of one slab already fill, so a single in-order
+    // issuer loses nothing to a second one.
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
+    const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k));
+    const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v));
+    auto issue_s = [&](uint32_t stage) {
+      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::stage0 + stage * Lay::stage_bytes));
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, kd0 + (kmajor_off(kk) >> 4), qd0 + (kmajor_off(kk) >> 4), kIdS,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+      }
+      __syncwarp();
+    };
+    uint32_t nst = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+      if (!(ok = warp_wait(kv_full, nit & 1, abort_flag))) break;
+      if (!(ok = warp_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
+      tc_fence_after();
+      issue_s(nst % kNS);
+      for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
+        const uint32_t s = nst % kNS;
+        const uint32_t q_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
+        const uint32_t do_addr = q_addr + kSub * kSubBytes;
+        const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
+        const uint64_t dod0 = desc_kmajor0(do_addr);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tS, kd0 + (kmajor_off(kk) >> 4), qd0 + (kmajor_off(kk) >> 4), kIdS,
+            mma_ss(tP, vd0 + (kmajor_off(kk) >> 4), dod0 + (kmajor_off(kk) >> 4), kIdS,
                    kk > 0 ? 1u : 0u);
-          mma_commit(s_full);
+          mma_commit(dp_full);
+          if (last) mma_commit(kv_empty);  // K and V are not read after this
         }
         __syncwarp();
-      };
-      uint32_t nst = 0, nit = 0;
-      bool ok = true;
-      for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
-        if (!(ok = warp_wait(kv_full, nit & 1, abort_flag))) break;
-        if (!(ok = warp_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(p_ready, nst & 1, abort_flag))) break;
+        if (first && nit > 0 && !(ok = warp_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
         tc_fence_after();
-        issue_s(nst % kNS);
-        for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
-          const uint32_t s = nst % kNS;
-          const uint32_t q_addr = smem_u32(smem + Lay::stage0 + s * Lay::stage_bytes);
-          const uint32_t do_addr = q_addr + kSub * kSubBytes;
-          const bool first = (sg == I.sl_lo), last = (sg == I.sl_hi - 1);
-          const uint64_t dod0 = desc_kmajor0(do_addr);
-          if (elect_one()) {
+        const uint64_t dom0 = desc_mnmajor0(do_addr);
+        if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tP, vd0 + (kmajor_off(kk) >> 4), dod0 + (kmajor_off(kk) >> 4), kIdS,
-                     kk > 0 ? 1u : 0u);
-            mma_commit(dp_full);
-            if (last) mma_commit(kv_empty);  // K and V are not read after this
-          }
-          __syncwarp();
-          if (!(ok = warp_wait(p_ready, nst & 1, abort_flag))) break;
-          if (first && nit > 0 && !(ok = warp_wait(acc_free, (nit - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t dom0 = desc_mnmajor0(do_addr);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-              mma_ts(tdV, tS + a_col(kk), dom0 + (mnmajor_off(kk) >> 4), kIdKV,
-                     (first && kk == 0) ? 0u : 1u);
-          }
-          __syncwarp();
-          if (!last) {
-            const uint32_t s2 = (nst + 1) % kNS;
-            if (!(ok = warp_wait(st_full + s2, ((nst + 1) / kNS) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_s(s2);
-          }
-          if (!(ok = warp_wait(ds_ready, nst & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t qm0 = desc_mnmajor0(q_addr);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-              mma_ts(tdK, tP + a_col(kk), qm0 + (mnmajor_off(kk) >> 4), kIdKV,
-                     (first && kk == 0) ? 0u : 1u);
-            mma_commit(st_empty + s);
-            if (last) mma_commit(acc_done);
-          }
-          __syncwarp();
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts(tdV, tS + a_col(kk), dom0 + (mnmajor_off(kk) >> 4), kIdKV,
+                   (first && kk == 0) ? 0u : 1u);
         }
+        __syncwarp();
+        if (!last) {
+          const uint32_t s2 = (nst + 1) % kNS;
+          if (!(ok = warp_wait(st_full + s2, ((nst + 1) / kNS) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_s(s2);
+        }
+        if (!(ok = warp_wait(ds_ready, nst & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t qm0 = desc_mnmajor0(q_addr);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts(tdK, tP + a_col(kk), qm0 + (mnmajor_off(kk) >> 4), kIdKV,
+                   (first && kk == 0) ? 0u : 1u);
+          mma_commit(st_empty + s);
+          if (last) mma_commit(acc_done);
+        }
+        __syncwarp();
       }
-      if (elect_one()) mma_commit(mma_drain);
-      __syncwarp();
-      mbar_wait_drain(mma_drain, 0, kDrainNs);
     }
+    if (elect_one()) mma_commit(mma_drain);
+    __syncwarp();
+    mbar_wait_drain(mma_drain, 0, kDrainNs);
+  } else if (warp == kSoftmaxWarps + 2) {
+    // the launch's last warp issues MMAs in the other kernels; idle here
   } else {
     // softmax + epilogue (warps 2..9): key lane quadrant warp % 4, row half hf
     constexpr int OH = D / 2;
@@ -1007,6 +1037,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled)
         uint32_t a[OH];
         tmem_ld_row<OH>((which == 0 ? tdV : tdK) + lane_base + OH * hf, a);
+        if (which == 1) {  // both accumulators read: the next item may overwrite them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_free);
+        }
         const float f = which == 0 ? 1.f : P.scale;
         __nv_bfloat16* dst = (which == 0 ? dVc : dKc) + off;
         if (valid) {
@@ -1021,9 +1056,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_free);
     }
   }
 
@@ -1096,11 +1128,11 @@ cudaError_t launch_fwd_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& 
   if (P.d == 128) {
     auto k = fwd_tc_kernel<128>;
     if ((e = prep(k, FwdLayout<128>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kFwdThreads, FwdLayout<128>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+    k<<<P.workers, kThreads, FwdLayout<128>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
   } else {
     auto k = fwd_tc_kernel<64>;
     if ((e = prep(k, FwdLayout<64>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kFwdThreads, FwdLayout<64>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
+    k<<<P.workers, kThreads, FwdLayout<64>::total, st>>>(m.q, m.k, m.v, P, pp, wk);
   }
   return cudaGetLastError();
 }
