@@ -36,8 +36,12 @@ namespace {
 using namespace tc;
 
 constexpr int kNS = 2;               // pipeline stages
-// producer warp, MMA warp, 8 softmax warps, a second MMA-issuing warp
-constexpr int kThreads = 352;
+// Warps 0 (TMA), 1 (MMA), 2..9 (softmax) in every kernel; the forward and
+// dQ kernels add warp 10 (a second MMA issuer) and warps 11..14 (epilogue,
+// one per TMEM lane quadrant).
+constexpr int kThreads = 480;    // forward and dQ
+constexpr int kThreadsKv = 320;  // dK / dV
+constexpr int kEpiWarp0 = 11;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
 constexpr float kLn2 = 0.6931471805599453f;
@@ -96,7 +100,8 @@ struct FwdLayout {
   static constexpr uint32_t k0 = tile;
   static constexpr uint32_t v0 = k0 + kFwdNK * tile;
   static constexpr uint32_t xchg = v0 + kFwdNV * tile;  // [2 parity][2 half][128] floats
-  static constexpr uint32_t bars = xchg + 2048;
+  static constexpr uint32_t lm = xchg + 2048;  // [3][128] floats: l of each half, row max
+  static constexpr uint32_t bars = lm + 1536;
   static constexpr uint32_t total = bars + 512 + 1024;  // + alignment slack
 };
 
@@ -122,9 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_full + kFwdNV;   // [3] S of tile t is in buffer t % 3
   uint64_t* p_ready = s_full + 3;       // [3] its P (bf16) is written over it
   uint64_t* sfree = p_ready + 3;        // [3] PV of tile t is done
-  uint64_t* o_free = sfree + 3;         // the epilogue has read O
-  uint64_t* mma_drain = o_free + 1;     // [2] one per issuing warp
-  uint64_t* xbar = mma_drain + 2;       // [4] row-max / row-sum exchange per lane quadrant
+  uint64_t* o_free = sfree + 3;         // the epilogue has read O and the row sums
+  uint64_t* lm_ready = o_free + 1;      // the softmax has written the item's row sums
+  uint64_t* mma_drain = lm_ready + 1;   // [2] one per issuing warp
+  uint64_t* xbar = mma_drain + 2;       // [4] row-max exchange per lane quadrant
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -141,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_ready + b, kSoftmaxWarps);
       mbar_init(sfree + b, 1);
     }
-    mbar_init(o_free, kSoftmaxWarps);
+    mbar_init(o_free, 4);
+    mbar_init(lm_ready, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 1, 1);
     *abort_flag = 0;
@@ -156,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tO = tmem + 384;  // three 128-column S buffers, then O
+  float* lm = (float*)(smem + Lay::lm);
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
@@ -271,12 +279,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) mma_commit(mma_drain + 1);
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
+  } else if (warp >= kEpiWarp0) {
+    // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
+    // Waits for the item's last PV and its row sums, loads O, releases it
+    // (and the row sums) to the next item, then writes the chunk partial
+    // (O / l, lse): the softmax warps never wait for it.
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    uint32_t ns = 0, nit = 0;
+    bool ok = true;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      ns += I.ntiles;
+      const uint32_t pt = ns - 1;  // the item's last tile
+      if (!(ok = warp_wait(lm_ready, nit & 1, abort_flag))) break;
+      if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
+      tc_fence_after();
+      const float lt = lm[r] + lm[128 + r];  // column half 0, then half 1
+      const float m_run = lm[256 + r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      float* po = wk.part_o + (I.slot * kRows + r) * D;
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
+        uint32_t v[64];
+        tmem_ld_row<64>(tO + lane_base + 64 * h, v);
+        if (h == D / 64 - 1) {  // O and the row sums are in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);
+        }
+#pragma unroll
+        for (int i = 0; i < 64; i += 8)
+          st_global_v8(po + 64 * h + i, __uint_as_float(v[i]) * inv,
+                       __uint_as_float(v[i + 1]) * inv, __uint_as_float(v[i + 2]) * inv,
+                       __uint_as_float(v[i + 3]) * inv, __uint_as_float(v[i + 4]) * inv,
+                       __uint_as_float(v[i + 5]) * inv, __uint_as_float(v[i + 6]) * inv,
+                       __uint_as_float(v[i + 7]) * inv);
+      }
+      wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+    }
   } else {
-    // ---------------- softmax + epilogue (warps 2..9) ----------------
-    // Warp w owns TMEM lane quadrant w % 4 (rows r) and column half hf of S
-    // and O; the two warps of a quadrant exchange their row maxima every tile
-    // (and their row sums at the end of an item) through shared memory,
-    // paced by that quadrant's 64-thread mbarrier.
+    // ---------------- softmax (warps 2..9) ----------------
+    // Warp w owns TMEM lane quadrant w % 4 (rows r) and column half hf of S;
+    // the two warps of a quadrant exchange their row maxima every tile
+    // through shared memory, paced by that quadrant's 64-thread mbarrier.
     constexpr int OH = D / 2;
     const int wq = warp & 3;
     const int hf = (warp - 2) >> 2;
@@ -295,9 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++nx;
       return got;
     };
-    for (int qi = q0; qi < q1 && ok; ++qi) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
+    // The next item's record and row are loaded before this item's epilogue
+    // waits, so their dependent global loads overlap it.
+    FwdItem In{};
+    RowInfo rin{};
+    if (q0 < q1) {
+      In = fwd_item(P, pp, pp.f_queue[q0]);
+      rin = row_info(P, In.first, In.nblk, In.g, r);
+    }
+    for (int qi = q0, nit = 0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = In;
+      const RowInfo ri = rin;
       float m_run = -INFINITY, l = 0.f;  // l: this half's partial row sum
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
         const uint32_t sb = ns % 3;
@@ -377,30 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_ready + sb);
       }
       if (!ok) break;
-      {
-        const uint32_t pt = ns - 1;  // PV of the item's last tile
-        if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
+      if (qi + 1 < q1) {
+        In = fwd_item(P, pp, pp.f_queue[qi + 1]);
+        rin = row_info(P, In.first, In.nblk, In.g, r);
       }
-      tc_fence_after();
-      float lo;
-      if (!(ok = exchange(l, &lo))) break;
-      const float lt = hf == 0 ? l + lo : lo + l;  // same order in both halves
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      float* po = wk.part_o + (I.slot * kRows + r) * D + OH * hf;
-      {
-        uint32_t v[OH];
-        tmem_ld_row<OH>(tO + lane_base + OH * hf, v);
-        tc_fence_before();  // O is in registers: the next item's PVs may overwrite it
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
-#pragma unroll
-        for (int i = 0; i < OH; i += 8)
-          st_global_v8(po + i, __uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                       __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv,
-                       __uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv,
-                       __uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
-      }
-      if (hf == 0) wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+      // hand the row sums to the epilogue once it has read the previous item's
+      if (nit > 0 && !(ok = warp_wait(o_free, (nit - 1) & 1, abort_flag))) break;
+      lm[hf * 128 + r] = l;
+      if (hf == 0) lm[256 + r] = m_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(lm_ready);
     }
   }
 
@@ -478,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(rfree + b, 1);
     }
     mbar_init(dq_done, 1);
-    mbar_init(dq_free, kSoftmaxWarps);
+    mbar_init(dq_free, 4);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 1, 1);
     *abort_flag = 0;
@@ -624,8 +665,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) mma_commit(mma_drain + 1);
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
+  } else if (warp >= kEpiWarp0) {
+    // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
+    // Loads the item's dQ partial once its last dQ MMA is done, releases the
+    // accumulator to the next item and writes the partial.
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    bool ok = true;
+    uint32_t nit = 0;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
+      tc_fence_after();
+      float* po = wk.part_o + (I.slot * kRows + r) * D;
+#pragma unroll 1
+      for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
+        uint32_t v[64];
+        tmem_ld_row<64>(tdQ + lane_base + 64 * h, v);
+        if (h == D / 64 - 1) {  // dQ is in registers: the next item may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dq_free);
+        }
+#pragma unroll
+        for (int i = 0; i < 64; i += 8)
+          st_global_v8(po + 64 * h + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]),
+                       __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
+                       __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+      }
+    }
   } else {
-    // softmax + epilogue (warps 2..9): lane quadrant warp % 4, column half hf
+    // softmax (warps 2..9): lane quadrant warp % 4, column half hf
     constexpr int OH = D / 2;
     const int wq = warp & 3;
     const int hf = (warp - 2) >> 2;
@@ -634,15 +706,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = P.scale_log2;
     uint32_t gt = 0, nit = 0;
     bool ok = true;
-    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      const RowInfo ri = row_info(P, I.first, I.nblk, I.g, r);
+    // The next item's record, row and row statistics are loaded before this
+    // item's epilogue waits, so their dependent global loads overlap it.
+    FwdItem In{};
+    RowInfo rin{};
+    float nl2n = -INFINITY, Drn = 0.f;
+    auto load_next = [&](int qn) {
+      In = fwd_item(P, pp, pp.f_queue[qn]);
+      rin = row_info(P, In.first, In.nblk, In.g, r);
       // padding rows: -inf exponent offset makes their P exactly 0
-      float nl2 = -INFINITY, Dr = 0.f;
-      if (ri.n >= 0) {
-        nl2 = -LSE[(size_t)ri.h * P.NQ + ri.n] * kLog2e;
-        Dr = wk.dvec[(size_t)ri.h * P.NQ + ri.n];
+      nl2n = -INFINITY;
+      Drn = 0.f;
+      if (rin.n >= 0) {
+        nl2n = -LSE[(size_t)rin.h * P.NQ + rin.n] * kLog2e;
+        Drn = wk.dvec[(size_t)rin.h * P.NQ + rin.n];
       }
+    };
+    if (q0 < q1) load_next(q0);
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = In;
+      const RowInfo ri = rin;
+      const float nl2 = nl2n, Dr = Drn;
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         if (!(ok = warp_wait(s_full, gt & 1, abort_flag))) break;
         tc_fence_after();
@@ -676,14 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 2: dS = P * (dP - D), written over this half's dP columns
         if (!(ok = warp_wait(dp_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        {
-          uint32_t dv[64];
-          tmem_ld_row<64>(pa, dv);
 #pragma unroll
-          for (int i = 0; i < 64; i += 2) {
-            const uint32_t pp2 = pk[i / 2];
-            pk[i / 2] = pack_bf16(__uint_as_float(pp2 << 16) * (__uint_as_float(dv[i]) - Dr),
-                                  __uint_as_float(pp2 & 0xffff0000u) * (__uint_as_float(dv[i + 1]) - Dr));
+        for (int c = 0; c < 2; ++c) {  // 32 columns at a time (register budget)
+          uint32_t dv[32];
+          tmem_ld_row<32>(pa + 32 * c, dv);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const uint32_t pp2 = pk[16 * c + i / 2];
+            pk[16 * c + i / 2] =
+                pack_bf16(__uint_as_float(pp2 << 16) * (__uint_as_float(dv[i]) - Dr),
+                          __uint_as_float(pp2 & 0xffff0000u) * (__uint_as_float(dv[i + 1]) - Dr));
           }
         }
         tmem_st32(pa, pk);  // packed dS of this half: columns a_col() of the dP region
@@ -693,22 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_ready + (gt & 1));
       }
       if (!ok) break;
-      if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
-      tc_fence_after();
-      float* po = wk.part_o + (I.slot * kRows + r) * D + OH * hf;
-      {
-        uint32_t v[OH];
-        tmem_ld_row<OH>(tdQ + lane_base + OH * hf, v);
-        tc_fence_before();  // dQ is in registers: the next item's MMAs may overwrite it
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dq_free);
-#pragma unroll
-        for (int i = 0; i < OH; i += 8)
-          st_global_v8(po + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]),
-                       __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
-                       __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
-      }
+      if (qi + 1 < q1) load_next(qi + 1);
     }
   }
 
@@ -757,7 +828,7 @@ __device__ __forceinline__ KvItem kv_item(const ProbDev& P, const PlanPtrs& pp, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKv, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        ProbDev P, PlanPtrs pp, WorkPtrs wk, const float* __restrict__ LSE,
@@ -953,8 +1024,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) mma_commit(mma_drain);
     __syncwarp();
     mbar_wait_drain(mma_drain, 0, kDrainNs);
-  } else if (warp == kSoftmaxWarps + 2) {
-    // the launch's last warp issues MMAs in the other kernels; idle here
   } else {
     // softmax + epilogue (warps 2..9): key lane quadrant warp % 4, row half hf
     constexpr int OH = D / 2;
@@ -1165,12 +1234,12 @@ cudaError_t launch_bwd_dkdv_tc(const ProbDev& P, const PlanPtrs& pp, const WorkP
   if (P.d == 128) {
     auto k = bwd_dkdv_tc_kernel<128>;
     if ((e = prep(k, KvLayout<128>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kThreads, KvLayout<128>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
+    k<<<P.workers, kThreadsKv, KvLayout<128>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
                                                           (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
   } else {
     auto k = bwd_dkdv_tc_kernel<64>;
     if ((e = prep(k, KvLayout<64>::total)) != cudaSuccess) return e;
-    k<<<P.workers, kThreads, KvLayout<64>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
+    k<<<P.workers, kThreadsKv, KvLayout<64>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
                                                          (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
   }
   return cudaGetLastError();
