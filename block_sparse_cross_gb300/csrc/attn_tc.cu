@@ -370,16 +370,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (i >= lim) x[i] = __float_as_uint(-INFINITY);
         }
+        // row max: eight chains of three-input maxima
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
 #pragma unroll
-        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
+        for (int i = 8; i < 56; i += 16)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+          for (int k = 0; k < 8; ++k)
+            mx[k] = max3f(mx[k], __uint_as_float(x[i + k]), __uint_as_float(x[i + 8 + k]));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[56 + k]));
+        const float mh = fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], max3f(mx[5], mx[6], mx[7])));
         float mo;
-        if (!(ok = exchange(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), &mo))) break;
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), mo) * sl2;
+        if (!(ok = exchange(mh, &mo))) break;
+        const float mt = fmaxf(mh, mo) * sl2;
         const float m_new = fmaxf(m_run, mt);
         float fac = 1.f;
         bool resc = false;
@@ -391,20 +396,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m_new;
         }
         const float nmu = (m_run == -INFINITY) ? 0.f : -m_run;
-        float lsum[8];
+        // P = 2^(x * scale*log2(e) - m) two columns per packed instruction
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(nmu, nmu);
+        uint64_t lsum[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) lsum[k] = 0.f;
+        for (int k = 0; k < 4; ++k) lsum[k] = 0ull;  // (+0.f, +0.f)
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(x[2 * i]), sl2, nmu));
-          const float p1 = ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl2, nmu));
-          lsum[i & 7] += p0 + p1;
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), sl2x2,
+                           nmux2),
+                    y0, y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          lsum[i & 3] = f2_add(lsum[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16(p0, p1);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) lsum[k] += lsum[k + 4];
-        const float ls = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+        float ls;
+        {
+          const uint64_t a = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
+          float a0, a1;
+          f2_unpack(a, a0, a1);
+          ls = a0 + a1;
+        }
         l = (t == 0) ? ls : l * fac + ls;
         tmem_st32(tS + lane_base + sb * 128 + 64 * hf, pk);  // packed P of this half: a_col()
         tmem_st_wait();
@@ -744,10 +758,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(s_read);
           if (__all_sync(0xffffffffu, lim >= 64)) {
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2, nl2);
 #pragma unroll
-            for (int i = 0; i < 64; i += 2)
-              pk[i / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)),
-                                    ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)));
+            for (int i = 0; i < 64; i += 2) {
+              float y0, y1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2,
+                               nl2x2),
+                        y0, y1);
+              pk[i / 2] = pack_bf16(ex2(y0), ex2(y1));
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
@@ -760,16 +779,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase 2: dS = P * (dP - D), written over this half's dP columns
         if (!(ok = warp_wait(dp_full + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
+        {
+          const uint64_t dr2 = f2_pack(Dr, Dr);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {  // 32 columns at a time (register budget)
-          uint32_t dv[32];
-          tmem_ld_row<32>(pa + 32 * c, dv);
+          for (int c = 0; c < 2; ++c) {  // 32 columns at a time (register budget)
+            uint32_t dv[32];
+            tmem_ld_row<32>(pa + 32 * c, dv);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const uint32_t pp2 = pk[16 * c + i / 2];
-            pk[16 * c + i / 2] =
-                pack_bf16(__uint_as_float(pp2 << 16) * (__uint_as_float(dv[i]) - Dr),
-                          __uint_as_float(pp2 & 0xffff0000u) * (__uint_as_float(dv[i + 1]) - Dr));
+            for (int i = 0; i < 32; i += 2) {
+              const uint32_t pp2 = pk[16 * c + i / 2];
+              const uint64_t d2 =
+                  f2_mul(f2_pack(__uint_as_float(pp2 << 16), __uint_as_float(pp2 & 0xffff0000u)),
+                         f2_sub(f2_pack(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), dr2));
+              float d0, d1;
+              f2_unpack(d2, d0, d1);
+              pk[16 * c + i / 2] = pack_bf16(d0, d1);
+            }
           }
         }
         tmem_st32(pa, pk);  // packed dS of this half: columns a_col() of the dP region
@@ -1059,10 +1084,16 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
           uint32_t sv[64];
           tmem_ld_row<64>(tS + lane_base + 64 * hf, sv);
           if (__all_sync(0xffffffffu, key < anc0[0])) {
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t* nl2x2 = (const uint64_t*)nl2;  // (row c, row c + 1) pairs
 #pragma unroll
-            for (int c = 0; c < 64; c += 2)
-              pk[c / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])),
-                                    ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])));
+            for (int c = 0; c < 64; c += 2) {
+              float y0, y1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                               nl2x2[c / 2]),
+                        y0, y1);
+              pk[c / 2] = pack_bf16(ex2(y0), ex2(y1));
+            }
           } else {
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
@@ -1084,12 +1115,16 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         {
           uint32_t dv[64];
           tmem_ld_row<64>(tP + lane_base + 64 * hf, dv);
+          const uint64_t* dvv2 = (const uint64_t*)dvv;  // (row c, row c + 1) pairs
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
             const uint32_t pp2 = pk[c / 2];
-            const float p0 = __uint_as_float(pp2 << 16), p1 = __uint_as_float(pp2 & 0xffff0000u);
-            pk[c / 2] = pack_bf16(p0 * (__uint_as_float(dv[c]) - dvv[c]),
-                                  p1 * (__uint_as_float(dv[c + 1]) - dvv[c + 1]));
+            const uint64_t d2 =
+                f2_mul(f2_pack(__uint_as_float(pp2 << 16), __uint_as_float(pp2 & 0xffff0000u)),
+                       f2_sub(f2_pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), dvv2[c / 2]));
+            float d0, d1;
+            f2_unpack(d2, d0, d1);
+            pk[c / 2] = pack_bf16(d0, d1);
           }
         }
         tmem_st32(tP + lane_base + 64 * hf, pk);  // packed dS^T of this half
