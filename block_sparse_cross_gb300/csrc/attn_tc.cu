@@ -37,10 +37,11 @@ using namespace tc;
 
 constexpr int kNS = 2;               // pipeline stages
 // Warps 0 (TMA), 1 (MMA), 2..9 (softmax) in every kernel; the forward and
-// dQ kernels add warp 10 (a second MMA issuer) and warps 11..14 (epilogue,
-// one per TMEM lane quadrant).
-constexpr int kThreads = 480;    // forward and dQ
-constexpr int kThreadsKv = 320;  // dK / dV
+// dQ kernels add warp 10 (a second MMA issuer), warps 11..14 (epilogue, one
+// per TMEM lane quadrant) and warp 15 (V loads).
+constexpr int kThreads = 512;    // forward and dQ
+constexpr int kVWarp = 15;
+constexpr int kThreadsKv = 352;  // dK / dV: warp 10 loads dO
 constexpr int kEpiWarp0 = 11;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- TMA producers: lane 0 Q and K, lane 1 V ----------------
+    // ---------------- TMA producer: Q and K (V comes from warp 15) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -196,7 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = nk > (uint32_t)kFwdNK ? nk - kFwdNK : 0; j < nk; ++j)
           mbar_wait_drain(k_full + j % kFwdNK, (j / kFwdNK) & 1, kDrainNs);
       }
-    } else if (lane == 1) {
+    }
+  } else if (warp == kVWarp) {
+    // ---------------- V producer: its own warp, so that it runs in parallel
+    // with the Q/K producer instead of taking turns with it ----------------
+    if (lane == 0) {
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) mma_commit(mma_drain + 1);
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
     // Waits for the item's last PV and its row sums, loads O, releases it
     // (and the row sums) to the next item, then writes the chunk partial
@@ -553,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- TMA producers: lane 0 Q, dO and K, lane 1 V ----------------
+    // ---------------- TMA producer: Q, dO and K (V comes from warp 15) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
@@ -584,7 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = nk > (uint32_t)kDqNK ? nk - kDqNK : 0; j < nk; ++j)
           mbar_wait_drain(k_full + j % kDqNK, (j / kDqNK) & 1, kDrainNs);
       }
-    } else if (lane == 1) {
+    }
+  } else if (warp == kVWarp) {
+    // ---------------- V producer (its own warp) ----------------
+    if (lane == 0) {
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
@@ -679,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) mma_commit(mma_drain + 1);
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
     // Loads the item's dQ partial once its last dQ MMA is done, releases the
     // accumulator to the next item and writes the partial.
@@ -880,7 +888,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   if (!plan_ok_cta(P, pp.hdr)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    // st_full takes one arrival from each of the two producer lanes
+    // st_full takes one arrival from each of the two producer warps
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int s = 0; s < kNS; ++s) {
@@ -909,9 +917,9 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   const int q0 = pp.b_qoff[blockIdx.x], q1 = pp.b_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ---------------- producers: lane 0 K/V per item, then Q and the slab's
-    // row table (one bulk copy of the precomputed record) per slab; lane 1
-    // dO per slab ----------------
+    // ---------------- producer: K/V per item, then Q and the slab's row table
+    // (one bulk copy of the precomputed record) per slab; dO comes from
+    // warp 10 ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
@@ -946,7 +954,11 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         for (uint32_t j = nst > (uint32_t)kNS ? nst - kNS : 0; j < nst; ++j)
           mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
       }
-    } else if (lane == 1) {  // dO of every slab, in parallel with lane 0's Q
+    }
+  } else if (warp == kSoftmaxWarps + 2) {
+    // ---------------- dO producer: its own warp, so that it runs in parallel
+    // with the Q producer instead of taking turns with it ----------------
+    if (lane == 0) {
       tma_prefetch_desc(&tmdO);
       uint32_t nst = 0;
       bool ok = true;

@@ -135,33 +135,49 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   const float lse_d = md + logf(ld);
   // pass 1: max and normaliser over chunk partials (+ draft)
   const size_t slot0 = (size_t)pp.sl_slot[G.slab];
+  const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + G.r;  // chunk c at c * Hkv * 128
+  const size_t cstride = (size_t)P.Hkv * kRows;
   float M = lse_d;
-  for (int c = lane; c < G.nact; c += 32)
-    M = fmaxf(M, wk.part_lse[((slot0 + c) * P.Hkv + g) * kRows + G.r]);
+  for (int c = lane; c < G.nact; c += 32) M = fmaxf(M, plse[c * cstride]);
   M = warp_max(M);
   float Ls = 0.f;
-  for (int c = lane; c < G.nact; c += 32)
-    Ls += expf(wk.part_lse[((slot0 + c) * P.Hkv + g) * kRows + G.r] - M);
+  for (int c = lane; c < G.nact; c += 32) Ls += expf(plse[c * cstride] - M);
   Ls = warp_sum(Ls) + expf(lse_d - M);
   const float invL = 1.f / Ls;
-  // pass 2: weighted sum in ascending chunk order, then the draft partial
+  // pass 2: weighted sum in ascending chunk order, then the draft partial.
+  // Lane c of each group of 32 chunks holds chunk c's weight; eight rows are
+  // in flight per step.
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < G.nact; ++c) {
-    const size_t row = ((slot0 + c) * P.Hkv + g) * kRows + G.r;
-    const float wgt = expf(wk.part_lse[row] - M) * invL;
-    if constexpr (EPL == 4) {  // 16-byte aligned: row * D * 4 and lane * 16 bytes
-      const float4 v = *(const float4*)(wk.part_o + row * D + x0);
-      acc[0] = fmaf(wgt, v.x, acc[0]);
-      acc[1] = fmaf(wgt, v.y, acc[1]);
-      acc[2] = fmaf(wgt, v.z, acc[2]);
-      acc[3] = fmaf(wgt, v.w, acc[3]);
-    } else {
-      const float* po = wk.part_o + row * D + x0;
+  const float* pbase = wk.part_o + (slot0 * P.Hkv + g) * kRows * D + (size_t)G.r * D + x0;
+  const size_t ostride = cstride * D;
+  for (int cb = 0; cb < G.nact; cb += 32) {
+    const int nc = min(32, G.nact - cb);
+    const float e = lane < nc ? expf(plse[(cb + lane) * cstride] - M) * invL : 0.f;
+    constexpr int U = 8;
+    for (int c0 = 0; c0 < nc; c0 += U) {
+      float v[U][EPL];
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wgt, po[i], acc[i]);
+      for (int u = 0; u < U; ++u) {
+        const int c = min(c0 + u, nc - 1);  // clamped rows get weight 0 below
+        const float* po = pbase + (size_t)(cb + c) * ostride;
+        if constexpr (EPL == 4) {  // 16-byte aligned: row * D * 4 and lane * 16 bytes
+          const float4 t = *(const float4*)po;
+          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) v[u][i] = po[i];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float wgt = __shfl_sync(0xffffffffu, e, min(c0 + u, 31));
+        if (c0 + u < nc) {
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wgt, v[u][i], acc[i]);
+        }
+      }
     }
   }
   const float wd = expf(lse_d - M) * invL / ld;
