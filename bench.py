@@ -186,13 +186,37 @@ def kernel_source_sha() -> str:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample_seconds(w, host, blocks):
+def oracle_sample(w, host, blocks):
+    """(seconds, O, LSE, dQ) of the oracle's fwd+bwd restricted to `blocks`."""
     import oracle.attention as OA
     t0 = time.perf_counter()
-    OA.forward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"], blocks=blocks)
-    OA.backward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"], host["dO"],
-                blocks=blocks)
-    return time.perf_counter() - t0
+    O, LSE = OA.forward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"],
+                        blocks=blocks)
+    g = OA.backward(w, host["Q"], host["Kc"], host["Vc"], host["Kd"], host["Vd"], host["dO"],
+                    blocks=blocks)
+    return time.perf_counter() - t0, O, LSE, g["dQ"]
+
+
+def oracle_sample_seconds(w, host, blocks):
+    return oracle_sample(w, host, blocks)[0]
+
+
+def oracle_errors(w, blocks, ref, outs):
+    """Errors of the GPU outputs against the oracle on the sampled blocks' rows
+    (O, LSE and dQ rows are exact per row; dK/dV sum over all blocks)."""
+    _, O, LSE, dQ = ref
+    rows = np.concatenate([np.arange(int(j) * w.B, (int(j) + 1) * w.B) for j in blocks])
+
+    def rel(a, b):
+        den = np.linalg.norm(b)
+        return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
+    Og = outs["O"].float().cpu().numpy()[rows].astype(np.float64)
+    Lg = outs["LSE"].cpu().numpy()[:, rows].astype(np.float64)
+    dQg = outs["dQ"].float().cpu().numpy()[rows].astype(np.float64)
+    return {"rows": int(rows.size), "heads": int(w.Hq),
+            "O_rel_l2": rel(Og, O[rows]), "O_max_abs": float(np.abs(Og - O[rows]).max()),
+            "LSE_max_abs": float(np.abs(Lg - LSE[:, rows]).max()),
+            "dQ_rel_l2": rel(dQg, dQ[rows])}
 
 
 def sample_flop(w, blocks) -> int:
@@ -217,14 +241,16 @@ def calibrate_blocks(w, host, target_s: float, rng_seed: int):
     order = rng.permutation(w.total_anchors)
     cum = np.cumsum([sample_flop(w, [b]) for b in order])
     n = 1
-    t = oracle_sample_seconds(w, host, order[:n])
+    ref = oracle_sample(w, host, order[:n])
     for _ in range(4):
+        t = ref[0]
         if 0.6 * target_s <= t <= 1.5 * target_s or (t < target_s and n == w.total_anchors):
             break
         rate = cum[n - 1] / max(t, 1e-6)            # oracle FLOP/s on this sample
         n = int(np.clip(np.searchsorted(cum, rate * target_s, side="right"), 1, w.total_anchors))
-        t = oracle_sample_seconds(w, host, order[:n])
-    return np.sort(order[:n]), t
+        ref = oracle_sample(w, host, order[:n])
+    calibrate_blocks.last = ref
+    return np.sort(order[:n]), ref[0]
 
 
 def host_inputs(w, seed_offset=1):
@@ -278,8 +304,9 @@ def run_ours(args, d: Dist):
     meta_host = [torch.from_numpy(a.astype(np.int32)).pin_memory()
                  for a in (w.cu_ctx, w.cu_anchor, w.anchors)]
     meta = [m.to(dev) for m in meta_host]
+    flags = S.SPLITKV_FLAG_CONTIGUOUS if args.contiguous else 0
     kv = S.SplitKV(*meta, w.total_ctx, w.total_anchors, w.max_ctx, w.B, w.Hq, w.Hkv, w.d,
-                   w.chunk, w.scale)
+                   w.chunk, w.scale, flags=flags)
     outs = {"O": torch.empty_like(gpu["Q"]), "LSE": torch.empty(w.Hq, w.n_q, device=dev),
             "dQ": torch.empty_like(gpu["Q"]), "dKc": torch.empty_like(gpu["Kc"]),
             "dVc": torch.empty_like(gpu["Vc"]), "dKd": torch.empty_like(gpu["Kd"]),
@@ -323,6 +350,7 @@ def run_ours(args, d: Dist):
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = d.max(ms_local)
     pst, ktimes = S.splitkv_profile_read()
+    busy = busy_imbalance(kv, S)
 
     flop_step = w.useful_flop(14)
     value = d.sum(flop_step) * args.steps / (ms * args.steps * 1e-3) / 1e12
@@ -378,16 +406,20 @@ def run_ours(args, d: Dist):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
-    # ---- CPU oracle baseline (rank 0, N = 1) ----
+    # ---- CPU oracle baseline (rank 0, N = 1), and the errors of the GPU
+    # outputs against it on the same sampled rows ----
     cpu = None
+    errors = None
     if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
         host = {k: v.float().numpy() for k, v in pinned.items()}
         blocks, _ = calibrate_blocks(w, host, args.cpu_target_s, w.seed + 99)
-        t = oracle_sample_seconds(w, host, blocks)
+        ref = oracle_sample(w, host, blocks)
+        t = ref[0]
         cpu = {"value": sample_flop(w, blocks) / t / 1e12, "unit": UNIT,
                "cores": oracle_threads(), "kind": "oracle",
                "sample": f"{len(blocks)} seeded draft blocks x {w.Hq} heads of {w.name} "
                          f"({t:.1f} s), float64 numpy fwd+bwd"}
+        errors = oracle_errors(w, blocks, ref, outs)
 
     if d.rank == 0:
         line = {
@@ -401,7 +433,9 @@ def run_ours(args, d: Dist):
                              if args.config == 2 else "see workload",
                        "step": "plan + forward + backward"},
             "pct_of_peak": 100.0 * value / d.world / peak,
+            "plan": "contiguous" if args.contiguous else "lpt",
             "lpt_imbalance": {"fwd": st.fwd_lpt_imbalance, "bwd": st.bwd_lpt_imbalance},
+            "busy_imbalance": busy,
             "contiguous_imbalance": {"fwd": st.fwd_contig_imbalance, "bwd": st.bwd_contig_imbalance},
             "skip_rate": 1.0 - st.fwd_tiles / max(1, st.dense_tiles),
             "phase_ms": {"plan": plan_ms, "fwd": fwd_ms, "bwd": bwd_ms},
@@ -413,9 +447,118 @@ def run_ours(args, d: Dist):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "oracle_errors": errors,
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# Studies (one JSON line per workload)
+# ---------------------------------------------------------------------------
+def _setup(w, dev, flags, S, torch):
+    t32 = W.tensors(w, seed_offset=1)
+    gpu = {k: torch.from_numpy(t32[k]).to(torch.bfloat16).to(dev)
+           for k in ("Q", "Kc", "Vc", "Kd", "Vd", "dO")}
+    del t32
+    meta = [torch.from_numpy(a.astype(np.int32)).to(dev) for a in (w.cu_ctx, w.cu_anchor, w.anchors)]
+    kv = S.SplitKV(*meta, w.total_ctx, w.total_anchors, w.max_ctx, w.B, w.Hq, w.Hkv, w.d,
+                   w.chunk, w.scale, flags=flags)
+    outs = {"O": torch.empty_like(gpu["Q"]), "LSE": torch.empty(w.Hq, w.n_q, device=dev),
+            "dQ": torch.empty_like(gpu["Q"]), "dKc": torch.empty_like(gpu["Kc"]),
+            "dVc": torch.empty_like(gpu["Vc"]), "dKd": torch.empty_like(gpu["Kd"]),
+            "dVd": torch.empty_like(gpu["Vd"])}
+
+    def fwd():
+        kv.forward(gpu["Q"], gpu["Kc"], gpu["Vc"], gpu["Kd"], gpu["Vd"], outs["O"], outs["LSE"])
+
+    def bwd():
+        kv.backward(gpu["Q"], gpu["Kc"], gpu["Vc"], gpu["Kd"], gpu["Vd"], outs["O"], outs["LSE"],
+                    gpu["dO"], outs["dQ"], outs["dKc"], outs["dVc"], outs["dKd"], outs["dVd"])
+    return kv, (gpu, outs, meta), fwd, bwd
+
+
+def _event_ms(fn, n, torch):
+    """Mean device time of fn over n calls (3 untimed calls first)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def run_study(args, d):
+    """balance: the single-GPU analogue of the pages' balancing speedup — step
+    time (plan + fwd + bwd) with the LPT plan against the contiguous plan.
+    planner: planning time against the item count, next to the forward time."""
+    import torch
+    import block_sparse_cross_gb300 as S
+    if d.rank != 0:
+        return 0
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    n = max(3, min(args.steps, 10))
+    if args.study == "balance":
+        cases = [(3, 0), (3, 1), (3, 2)] + [(4, k) for k in range(5)]
+    else:
+        cases = [(1, 0), (2, 0), (3, 0)] + [(4, k) for k in range(5)]
+    for cfg, sweep in cases:
+        w = W.config(cfg, sweep)
+        line = {"study": args.study, "workload": workload_desc(w), "steps": n}
+        if args.study == "balance":
+            for mode, flags in (("lpt", 0), ("contiguous", S.SPLITKV_FLAG_CONTIGUOUS)):
+                kv, keep, fwd, bwd = _setup(w, dev, flags, S, torch)
+
+                def step():
+                    kv.plan()
+                    fwd()
+                    bwd()
+                ms = _event_ms(step, n, torch)
+                if kv.device_status() != S.SPLITKV_OK:
+                    raise RuntimeError(S.splitkv_status_string(kv.device_status()))
+                st = kv.stats()
+                line[mode] = {
+                    "ms_per_step": ms,
+                    "tflops": w.useful_flop(14) / (ms * 1e-3) / 1e12,
+                    "planned_imbalance": {
+                        "fwd": st.fwd_contig_imbalance if flags else st.fwd_lpt_imbalance,
+                        "bwd": st.bwd_contig_imbalance if flags else st.bwd_lpt_imbalance},
+                    "busy_imbalance": {k: v["imbalance"] for k, v in busy_imbalance(kv, S).items()},
+                }
+                del kv, keep
+                torch.cuda.empty_cache()
+            line["speedup_lpt_over_contiguous"] = line["contiguous"]["ms_per_step"] / line["lpt"]["ms_per_step"]
+        else:
+            kv, keep, fwd, bwd = _setup(w, dev, 0, S, torch)
+            plan_ms = _event_ms(kv.plan, n, torch)
+            fwd_ms = _event_ms(fwd, n, torch)
+            st = kv.stats()
+            line.update({"fwd_items": st.fwd_items, "bwd_items": st.bwd_items,
+                         "workers": st.workers, "plan_ms": plan_ms, "fwd_ms": fwd_ms,
+                         "plan_over_fwd": plan_ms / fwd_ms})
+            del kv, keep
+            torch.cuda.empty_cache()
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def busy_imbalance(kv, S):
+    """Measured load balance of the latest launch of each persistent attention
+    kernel: per-CTA busy time (end - start %globaltimer) max / mean - 1."""
+    out = {}
+    for name, kid in (("fwd_attention", S.SPLITKV_K_FWD_ATTN), ("bwd_dq", S.SPLITKV_K_BWD_DQ),
+                      ("bwd_dkdv", S.SPLITKV_K_BWD_DKDV)):
+        ns = kv.busy_ns(kid).astype(np.int64)
+        b = (ns[:, 1] - ns[:, 0]).astype(np.float64)
+        out[name] = {"imbalance": float(b.max() / b.mean() - 1.0), "busy_max_ms": float(b.max() * 1e-6),
+                     "busy_mean_ms": float(b.mean() * 1e-6),
+                     "span_ms": float((ns[:, 1].max() - ns[:, 0].min()) * 1e-6)}
+    return out
 
 
 def main():
@@ -430,12 +573,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-target-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    ap.add_argument("--contiguous", action="store_true",
+                    help="contiguous item assignment instead of LPT")
+    ap.add_argument("--study", choices=("balance", "planner"),
+                    help="balance: step time with LPT vs contiguous plans (configs 3, 4); "
+                         "planner: plan time vs item count next to the forward (configs 1-4)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     d = Dist()
     try:
-        rc = run_reference(args, d) if args.impl == "reference" else run_ours(args, d)
+        if args.study:
+            rc = run_study(args, d)
+        else:
+            rc = run_reference(args, d) if args.impl == "reference" else run_ours(args, d)
     finally:
         d.close()
     return rc

@@ -114,6 +114,8 @@ _SIGS = {
     "splitkv_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "splitkv_profile_read": ([_vp, _vp, ctypes.c_int], ctypes.c_int),
     "splitkv_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
+    "splitkv_busy_read": ([_P, _vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                           _vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -224,6 +226,15 @@ def splitkv_plan_stats(prob, plan_ws, stream=None):
     return st, out
 
 
+def splitkv_busy_read(prob, plan_ws, kernel_id, ns, stream=None):
+    """ns: host uint64 numpy array of length >= 2 * workers. Returns (status, workers)."""
+    w = ctypes.c_int(0)
+    st = _lib.splitkv_busy_read(ctypes.byref(prob), _ptr(plan_ws), int(kernel_id),
+                                ns.ctypes.data_as(ctypes.c_void_p), int(ns.size), ctypes.byref(w),
+                                _stream(stream))
+    return st, w.value
+
+
 def splitkv_device_status(prob, plan_ws, stream=None):
     s = ctypes.c_int(0)
     st = _lib.splitkv_device_status(ctypes.byref(prob), _ptr(plan_ws), ctypes.byref(s),
@@ -295,6 +306,15 @@ class SplitKV:
         st, out = splitkv_plan_stats(self.prob, self.plan_ws, self._stream())
         _check("splitkv_plan_stats", st)
         return out
+
+    def busy_ns(self, kernel_id: int):
+        """[workers][2] start / end %globaltimer stamps (ns) of the latest launch of
+        an attention kernel (SPLITKV_K_FWD_ATTN, _BWD_DQ or _BWD_DKDV)."""
+        import numpy as np
+        ns = np.zeros(2 * 4096, np.uint64)
+        st, w = splitkv_busy_read(self.prob, self.plan_ws, kernel_id, ns, self._stream())
+        _check("splitkv_busy_read", st)
+        return ns[:2 * w].reshape(w, 2)
 
     def device_status(self) -> int:
         st, s = splitkv_device_status(self.prob, self.plan_ws, self._stream())

@@ -232,6 +232,27 @@ int splitkv_profile_read(int32_t* launches, double* total_ms, int n) {
   return SPLITKV_OK;
 }
 
+int splitkv_busy_read(const splitkv_problem* prob, const void* plan_ws, int kernel_id,
+                      uint64_t* ns, int capacity, int* workers, splitkv_stream stream) {
+  Ctx c;
+  const int st = setup(prob, plan_ws, &c);
+  if (st) return st;
+  int slot;
+  switch (kernel_id) {
+    case SPLITKV_K_FWD_ATTN: slot = 0; break;
+    case SPLITKV_K_BWD_DQ: slot = 1; break;
+    case SPLITKV_K_BWD_DKDV: slot = 2; break;
+    default: return SPLITKV_EINVAL;
+  }
+  if (!ns || !workers || capacity < 0) return SPLITKV_EINVAL;
+  const int m = c.P.workers;
+  *workers = m;
+  if (capacity < 2 * m) return SPLITKV_EINVAL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
+  return cuda_status(cudaMemcpy(ns, c.pp.busy_ns + (size_t)slot * m * 2, sizeof(uint64_t) * 2 * m,
+                                cudaMemcpyDeviceToHost));
+}
+
 const char* splitkv_kernel_name(int kernel_id) {
   static const char* names[SPLITKV_NUM_KERNELS] = {
       "plan", "fwd_attention", "merge", "bwd_draft", "bwd_dq", "bwd_dkdv", "dq_reduce",

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
   float* ks = qT + D * kRows;          // [32][D]
   float* vs = ks + kSimtKeys * D;      // [32][D]
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 0, 0);
   const int w = blockIdx.x;
   const int r = threadIdx.x;
   const int q0 = pp.f_qoff[w], q1 = pp.f_qoff[w + 1];
@@ -98,6 +99,8 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
                                        acc[x + 3] * inv);
     wk.part_lse[slot * kRows + r] = l > 0.f ? m + logf(l) : -INFINITY;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) stamp_busy(P, pp, 0, 1);
 }
 
 template <typename T, int D>
@@ -113,6 +116,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
   float* ks = doT + D * kRows;         // [32][D]
   float* vs = ks + kSimtKeys * D;      // [32][D]
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 1, 0);
   const int w = blockIdx.x;
   const int r = threadIdx.x;
   const int q0 = pp.f_qoff[w], q1 = pp.f_qoff[w + 1];
@@ -176,6 +180,8 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
     for (int x = 0; x < D; x += 4)
       *(float4*)(po + x) = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) stamp_busy(P, pp, 1, 1);
 }
 
 constexpr int kRowBatch = 32;
@@ -202,6 +208,7 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
   float* d_s = lse_s + kRowBatch;      // [kRowBatch]
   int* anc_s = (int*)(d_s + kRowBatch);// [kRowBatch]
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 2, 0);
   const int w = blockIdx.x;
   const int tid = threadIdx.x;
   const int kl = tid >> 1, half = tid & 1;
@@ -289,6 +296,8 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
       }
     }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) stamp_busy(P, pp, 2, 1);
 }
 
 template <typename K>

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 0, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -468,7 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+    stamp_busy(P, pp, 0, 1);
+  }
 }
 
 // ===========================================================================
@@ -521,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 1, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -820,7 +825,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+    stamp_busy(P, pp, 1, 1);
+  }
 }
 
 // ===========================================================================
@@ -886,6 +894,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
   if (!plan_ok_cta(P, pp.hdr)) return;
+  if (threadIdx.x == 0) stamp_busy(P, pp, 2, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     // st_full takes one arrival from each of the two producer warps
@@ -1179,7 +1188,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
-  if (threadIdx.x == 0 && *abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) latch(pp.hdr, SPLITKV_ETIMEOUT);
+    stamp_busy(P, pp, 2, 1);
+  }
 }
 
 // ===========================================================================

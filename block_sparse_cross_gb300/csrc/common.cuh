@@ -35,6 +35,15 @@ __device__ __forceinline__ bool plan_ok_cta(const ProbDev& P, const PlanHeader* 
   return ok_flag != 0;
 }
 
+// Start (which = 0) or end (1) stamp of this worker's CTA in the plan's busy
+// table; slot 0 = forward, 1 = dQ, 2 = dK/dV attention launch.
+__device__ __forceinline__ void stamp_busy(const ProbDev& P, const PlanPtrs& pp, int slot,
+                                           int which) {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  pp.busy_ns[((size_t)slot * P.workers + blockIdx.x) * 2 + which] = t;
+}
+
 // Last index s in [0, n) with off[s] <= x (off non-decreasing, off[0] <= x).
 __device__ __forceinline__ int seg_of(const int32_t* off, int n, int64_t x) {
   int lo = 0, hi = n;

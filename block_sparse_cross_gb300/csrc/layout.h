@@ -92,6 +92,9 @@ struct PlanPtrs {
   QEntry* b_queue;
   int64_t* b_load_lpt;
   int64_t* b_load_contig;
+  // [3][workers][2] %globaltimer (ns) at the start and the end of every
+  // worker's CTA in the latest forward, dQ and dK/dV attention launch
+  uint64_t* busy_ns;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -140,6 +143,7 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   q.b_queue = (QEntry*)take(sizeof(QEntry) * (c.NCB * c.Hkv + 1));
   q.b_load_lpt = (int64_t*)take(8 * c.M);
   q.b_load_contig = (int64_t*)take(8 * c.M);
+  q.busy_ns = (uint64_t*)take(16 * 3 * c.M);
   if (p) *p = q;
   return align_up(off, 256);
 }

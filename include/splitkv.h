@@ -307,6 +307,25 @@ enum {
 };
 int splitkv_profile_enable(int on);
 int splitkv_profile_read(int32_t* launches, double* total_ms, int n);
+
+/*
+ * splitkv_busy_read — SYNCHRONISES `stream`. Measured load balance of the
+ * persistent attention kernels (the realised counterpart of the planned LPT
+ * loads; the paper claims balanced per-participant work, abstract and rit.work
+ * article, paragraph on anchor sampling and load imbalance). Every launch of
+ * the forward, dQ and dK/dV attention kernels with this plan stamps, per
+ * worker CTA, the %globaltimer value (ns) at its start and at its end into
+ * the plan workspace; this copies the stamps of the latest launch of
+ * `kernel_id` (SPLITKV_K_FWD_ATTN, SPLITKV_K_BWD_DQ or SPLITKV_K_BWD_DKDV)
+ * to the host array ns[2*w] = start, ns[2*w+1] = end of worker w.
+ *   capacity: length of ns; *workers receives the worker count (nothing is
+ *   written to ns unless capacity >= 2 * workers).
+ * Stamps of a kernel that has not run with this plan are undefined.
+ * Errors: EINVAL (other kernel ids, capacity too small), ECUDA, and the
+ * errors of an invalid problem / plan workspace.
+ */
+int splitkv_busy_read(const splitkv_problem* prob, const void* plan_ws, int kernel_id,
+                      uint64_t* ns, int capacity, int* workers, splitkv_stream stream);
 /* Name of a kernel family id (never NULL). */
 const char* splitkv_kernel_name(int kernel_id);
 

@@ -63,3 +63,26 @@ def test_status_strings():
     for code in range(10):
         assert S.splitkv_status_string(code) != "unknown status"
     assert S.splitkv_status_string(1234) == "unknown status"
+
+
+def test_busy_read_validates_on_the_host():
+    # explicit worker count: nothing below touches a device
+    import numpy as np
+    p = make_problem(num_workers=16)
+    dummy = ctypes.c_void_p(1 << 20)  # never dereferenced before the checks
+    ns = np.zeros(64, np.uint64)
+    w = ctypes.c_int(-1)
+    buf = ns.ctypes.data_as(ctypes.c_void_p)
+    # only the three attention kernel families have stamps
+    for kid in (S.SPLITKV_K_PLAN, S.SPLITKV_K_MERGE, S.SPLITKV_K_DQ_REDUCE, 99, -1):
+        assert S._lib.splitkv_busy_read(ctypes.byref(p), dummy, kid, buf, 64, ctypes.byref(w),
+                                        None) == S.SPLITKV_EINVAL
+    # capacity below 2 * workers: EINVAL, but the worker count is reported
+    assert S._lib.splitkv_busy_read(ctypes.byref(p), dummy, S.SPLITKV_K_FWD_ATTN, buf, 31,
+                                    ctypes.byref(w), None) == S.SPLITKV_EINVAL
+    assert w.value == 16
+    assert S._lib.splitkv_busy_read(ctypes.byref(p), None, S.SPLITKV_K_FWD_ATTN, buf, 64,
+                                    ctypes.byref(w), None) == S.SPLITKV_EINVAL
+    assert S._lib.splitkv_busy_read(ctypes.byref(make_problem(d=96, num_workers=16)), dummy,
+                                    S.SPLITKV_K_FWD_ATTN, buf, 64, ctypes.byref(w),
+                                    None) == S.SPLITKV_EUNSUPPORTED
