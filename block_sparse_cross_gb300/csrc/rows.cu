@@ -68,6 +68,46 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Reduce-scatter of 16 per-lane partial sums over the warp: afterwards lanes
+// 2k and 2k+1 both hold the warp total of value k (k = (lane >> 1) & 15).
+// Each halving step sends the half this lane gives up to its partner and
+// adds the half it keeps: 8 + 4 + 2 + 1 + 1 = 16 shuffles, against 5 per
+// value for a full all-reduce of each.
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+  float w[8];
+  {
+    const bool b = (lane >> 4) & 1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float keep = b ? v[i + 8] : v[i], send = b ? v[i] : v[i + 8];
+      w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool b = (lane >> 3) & 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float keep = b ? w[i + 4] : w[i], send = b ? w[i] : w[i + 4];
+      w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool b = (lane >> 2) & 1;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float keep = b ? w[i + 2] : w[i], send = b ? w[i] : w[i + 2];
+      w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  float x;
+  {
+    const bool b = (lane >> 1) & 1;
+    const float keep = b ? w[1] : w[0], send = b ? w[0] : w[1];
+    x = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  return x + __shfl_xor_sync(0xffffffffu, x, 1);
+}
+
 // One warp per (query n, head h); lane owns dims [lane*EPL, lane*EPL + EPL).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
@@ -93,44 +133,56 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
     q[i] *= P.scale;
     od[i] = 0.f;
   }
+  // Sixteen draft keys per pass: each lane pair ends with one key's score
+  // (reduce-scatter), the pass's maximum and sum combine over the 16 pairs,
+  // and each key's weight is broadcast from its pair to accumulate o_d.
   float md = -INFINITY, ld = 0.f;
-  constexpr int KT = 8;  // draft keys in flight
+  constexpr int KT = 16;
+  const int kl = (lane >> 1) & 15;  // the key this lane's pair holds
   for (int t0 = 0; t0 < P.B; t0 += KT) {
-    float kv[KT][EPL], vv[KT][EPL], sc[KT];
+    float sc[KT];
+    {
+      float kv[KT][EPL];
 #pragma unroll
-    for (int u = 0; u < KT; ++u) {
-      const int t = min(t0 + u, P.B - 1);
-      const size_t kro = ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0;
-      ld_vec<T, EPL>(Kd + kro, kv[u]);
-      ld_vec<T, EPL>(Vd + kro, vv[u]);
-    }
+      for (int u = 0; u < KT; ++u) {
+        const int t = min(t0 + u, P.B - 1);
+        ld_vec<T, EPL>(Kd + ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0, kv[u]);
+      }
 #pragma unroll
-    for (int u = 0; u < KT; ++u) {
-      float part = 0.f;
+      for (int u = 0; u < KT; ++u) {
+        float part = 0.f;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) part = fmaf(q[i], kv[u][i], part);
-      sc[u] = part;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int u = 0; u < KT; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], o);
-#pragma unroll
-    for (int u = 0; u < KT; ++u) {
-      if (t0 + u >= P.B) break;
-      if (sc[u] > md) {
-        const float f = expf(md - sc[u]);
-        ld = ld * f + 1.f;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) od[i] = fmaf(od[i], f, vv[u][i]);
-        md = sc[u];
-      } else {
-        const float p = expf(sc[u] - md);
-        ld += p;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) od[i] = fmaf(p, vv[u][i], od[i]);
+        for (int i = 0; i < EPL; ++i) part = fmaf(q[i], kv[u][i], part);
+        sc[u] = part;
       }
     }
+    const bool valid = t0 + kl < P.B;
+    const float s_all = reduce_scatter16(sc, lane);  // every lane takes part in the shuffles
+    const float s_mine = valid ? s_all : -INFINITY;
+    float mg = s_mine;
+#pragma unroll
+    for (int o = 2; o < 32; o <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+    const float m_new = fmaxf(md, mg);
+    const float f = (md == -INFINITY) ? 0.f : expf(md - m_new);
+    const float pm = valid ? expf(s_mine - m_new) : 0.f;
+    float lg = pm;
+#pragma unroll
+    for (int o = 2; o < 32; o <<= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);
+    ld = ld * f + lg;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) od[i] *= f;
+    // keys past B repeat the last key's values with weight 0
+    float vv[KT][EPL];
+#pragma unroll
+    for (int u = 0; u < KT; ++u)
+      ld_vec<T, EPL>(Vd + ((size_t)(j * P.B + min(t0 + u, P.B - 1)) * P.Hkv + g) * D + x0, vv[u]);
+#pragma unroll
+    for (int u = 0; u < KT; ++u) {
+      const float pu = __shfl_sync(0xffffffffu, pm, 2 * u);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) od[i] = fmaf(pu, vv[u][i], od[i]);
+    }
+    md = m_new;
   }
   const float lse_d = md + logf(ld);
   // pass 1: max and normaliser over chunk partials (+ draft)
@@ -225,7 +277,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, W
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
-  constexpr int KT = 8;  // draft keys in flight
+  // Sixteen draft keys per pass: the scores and dP values are reduce-scattered
+  // so that lane pair k holds key t0 + k; it computes P and dS, and dS is
+  // broadcast back for the draft term of dQ.
+  constexpr int KT = 16;
+  const int kl = (lane >> 1) & 15;
   for (int t0 = 0; t0 < P.B; t0 += KT) {
     float kd[KT][EPL], sp[KT], dp[KT];
 #pragma unroll
@@ -243,25 +299,21 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, W
         dp[u] = fmaf(dov[i], vd[i], dp[u]);
       }
     }
+    const float s_mine = reduce_scatter16(sp, lane);
+    const float dp_mine = reduce_scatter16(dp, lane);
+    const int t_mine = t0 + kl;
+    const bool valid = t_mine < P.B;
+    const float pt = valid ? expf(s_mine * P.scale - lse) : 0.f;
+    const float ds = pt * (dp_mine - Dr);
+    if (valid && (lane & 1) == 0) {
+      prow[t_mine] = pt;
+      srow[t_mine] = ds;
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
+    for (int u = 0; u < KT; ++u) {  // dS of keys past B is 0
+      const float du = __shfl_sync(0xffffffffu, ds, 2 * u);
 #pragma unroll
-      for (int u = 0; u < KT; ++u) {
-        sp[u] += __shfl_xor_sync(0xffffffffu, sp[u], o);
-        dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], o);
-      }
-#pragma unroll
-    for (int u = 0; u < KT; ++u) {
-      const int t = t0 + u;
-      if (t >= P.B) break;
-      const float pt = expf(sp[u] * P.scale - lse);
-      const float ds = pt * (dp[u] - Dr);
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) acc[i] = fmaf(ds, kd[u][i], acc[i]);
-      if (lane == (t & 31)) {
-        prow[t] = pt;
-        srow[t] = ds;
-      }
+      for (int i = 0; i < EPL; ++i) acc[i] = fmaf(du, kd[u][i], acc[i]);
     }
   }
   float* dqd = wk.dq_draft + row;
