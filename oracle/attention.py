@@ -21,6 +21,14 @@ Backward of the loss sum(dO * O):
 dK_j / dV_j are scattered back onto the Kc/Vc and Kd/Vd rows they came from
 and summed over the query heads of the kv group.
 
+Mask variants (the pages say other diffusion drafters -- DFlash, Domino,
+DSpark -- share this attention pattern, rit.work article, section "Когда метод
+меняет инфраструктурный план"; their exact masks are not given, so two plain
+variants are offered, selected by the workload's flags):
+
+    inclusive       the context keys are 0 <= k <= a_j (a_j + 1 keys)
+    causal block    query i of block j (row j*B + i) sees draft keys t <= i only
+
 Every input holds exactly the values the device sees (the compute-dtype
 rounding happens before); slices are upcast to float64 before any
 arithmetic, so float32 arrays of bf16-rounded values are accepted as well.
@@ -42,6 +50,21 @@ def _blocks(w) -> Iterable[Tuple[int, int, int]]:
     for s in range(w.num_samples):
         for j in range(int(w.cu_anchor[s]), int(w.cu_anchor[s + 1])):
             yield j, s, int(w.anchors[j])
+
+
+def _ctx_len(w, a: int) -> int:
+    """Number of context keys block with anchor a sees."""
+    return a + 1 if getattr(w, "mask_inclusive", False) else a
+
+
+def _mask_draft(w, S: np.ndarray, n_ctx: int) -> np.ndarray:
+    """Sets the scores of draft keys a causal block hides to -inf (in place).
+    S is B x (n_ctx + B) with the draft keys last."""
+    if getattr(w, "mask_causal_block", False):
+        B = w.B
+        hidden = np.triu(np.ones((B, B), bool), k=1)   # t > i
+        S[:, n_ctx:][hidden] = -np.inf
+    return S
 
 
 def _head_sets(w, heads: Optional[Sequence[int]]):
@@ -69,12 +92,13 @@ def forward(w, Q, Kc, Vc, Kd, Vd, blocks=None, heads=None):
         if sel is not None and j not in sel:
             continue
         c0 = int(w.cu_ctx[s])
+        na = _ctx_len(w, a)
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0).astype(np.float64)
-            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0).astype(np.float64)
+            keys = np.concatenate([Kc[c0:c0 + na, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0:c0 + na, g], Vd[rows, g]], axis=0).astype(np.float64)
             for h in hlist:
-                S = scale * (Q[rows, h].astype(np.float64) @ keys.T)
+                S = _mask_draft(w, scale * (Q[rows, h].astype(np.float64) @ keys.T), na)
                 lse = _logsumexp_rows(S)
                 P = np.exp(S - lse[:, None])
                 O[rows, h] = P @ vals
@@ -100,16 +124,17 @@ def backward(w, Q, Kc, Vc, Kd, Vd, dO, blocks=None, heads=None):
         if sel is not None and j not in sel:
             continue
         c0 = int(w.cu_ctx[s])
+        na = _ctx_len(w, a)
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + a, g], Kd[rows, g]], axis=0).astype(np.float64)
-            vals = np.concatenate([Vc[c0:c0 + a, g], Vd[rows, g]], axis=0).astype(np.float64)
+            keys = np.concatenate([Kc[c0:c0 + na, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0:c0 + na, g], Vd[rows, g]], axis=0).astype(np.float64)
             dK = np.zeros_like(keys)
             dV = np.zeros_like(vals)
             for h in hlist:
                 q = Q[rows, h].astype(np.float64)
                 do = dO[rows, h].astype(np.float64)
-                S = scale * (q @ keys.T)
+                S = _mask_draft(w, scale * (q @ keys.T), na)
                 lse = _logsumexp_rows(S)
                 P = np.exp(S - lse[:, None])
                 O = P @ vals
@@ -119,10 +144,10 @@ def backward(w, Q, Kc, Vc, Kd, Vd, dO, blocks=None, heads=None):
                 dS = P * (dP - D[:, None])
                 dQ[rows, h] = scale * (dS @ keys)
                 dK += scale * (dS.T @ q)
-            dKc[c0:c0 + a, g] += dK[:a]
-            dVc[c0:c0 + a, g] += dV[:a]
-            dKd[rows, g] += dK[a:]
-            dVd[rows, g] += dV[a:]
+            dKc[c0:c0 + na, g] += dK[:na]
+            dVc[c0:c0 + na, g] += dV[:na]
+            dKd[rows, g] += dK[na:]
+            dVd[rows, g] += dV[na:]
     return {"dQ": dQ, "dKc": dKc, "dVc": dVc, "dKd": dKd, "dVd": dVd}
 
 
@@ -147,12 +172,14 @@ def partial_forward(w, Q, Kc, Vc, Kd, Vd, lo: int, hi: int, draft: bool):
             if draft:
                 keys, vals = Kd[rows, g], Vd[rows, g]
             else:
-                k0, k1 = max(lo, 0), min(hi, a)
+                k0, k1 = max(lo, 0), min(hi, _ctx_len(w, a))
                 if k1 <= k0:
                     continue
                 keys, vals = Kc[c0 + k0:c0 + k1, g], Vc[c0 + k0:c0 + k1, g]
             keys = keys.astype(np.float64)
             S = scale * (Q[rows, h].astype(np.float64) @ keys.T)
+            if draft:
+                S = _mask_draft(w, S, 0)
             lse = _logsumexp_rows(S)
             lse_out[h, rows] = lse
             O_out[rows, h] = np.exp(S - lse[:, None]) @ vals.astype(np.float64)

@@ -12,7 +12,8 @@ realized masked work of chunk [cs, cs + cl) of a sample is the number of
     cost = sum over anchors a_j > cs of  min(cl, a_j - cs) * B
 
 (block j sees context keys [0, a_j), so it sees min(cl, a_j - cs) keys of
-the chunk, for each of its B query rows).
+the chunk, for each of its B query rows). With the inclusive mask variant
+(context [0, a_j]) the same formula runs on a_j + 1.
 
 Work items. The forward splits each chunk further by kv head g and by
 "slab" sigma: ``bps = 128 // (B * group)`` consecutive draft blocks of one
@@ -53,6 +54,13 @@ def blocks_per_slab(w) -> int:
     return TILE_ROWS // (w.B * group)
 
 
+def _sample_anchors(w, s: int) -> np.ndarray:
+    """End of the visible context of each block of sample s: a_j, or a_j + 1
+    when the context is inclusive ([0, a_j])."""
+    anc = np.asarray(w.anchors[int(w.cu_anchor[s]):int(w.cu_anchor[s + 1])], np.int64)
+    return anc + 1 if getattr(w, "mask_inclusive", False) else anc
+
+
 def fwd_items(w) -> List[Tuple[int, int, int, int, int, int]]:
     """(id, s, c, sigma, g, cost) for every forward item of positive cost."""
     bps = blocks_per_slab(w)
@@ -60,7 +68,7 @@ def fwd_items(w) -> List[Tuple[int, int, int, int, int, int]]:
     nid = 0
     for s in range(w.num_samples):
         L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
-        anc = w.anchors[int(w.cu_anchor[s]):int(w.cu_anchor[s + 1])]
+        anc = _sample_anchors(w, s)
         nch = -(-L // w.chunk)
         nsl = -(-len(anc) // bps)
         for c in range(nch):
@@ -81,7 +89,7 @@ def bwd_items(w) -> List[Tuple[int, int, int, int, int]]:
     nid = 0
     for s in range(w.num_samples):
         L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
-        anc = w.anchors[int(w.cu_anchor[s]):int(w.cu_anchor[s + 1])]
+        anc = _sample_anchors(w, s)
         for kt in range(-(-L // KEY_TILE)):
             ks = kt * KEY_TILE
             cost = chunk_cost(anc, ks, min(KEY_TILE, L - ks), w.B)

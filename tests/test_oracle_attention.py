@@ -8,6 +8,8 @@
   single-query textbook attention via scipy
 * invariants: exactness of any KV split merged by log-sum-exp (the property
   the Split-KV pages claim), strict prefix mask, GQA head map
+* the mask variants (inclusive context, causal draft block) through the same
+  brute-force, SDPA, finite-difference and split pins, plus their boundary keys
 """
 import json
 import math
@@ -50,12 +52,13 @@ def brute_force_forward(w, Q, Kc, Vc, Kd, Vd):
             g = h // group
             scores, vals = [], []
             for t in range(T):                       # every context row
-                visible = c0 <= t < c1 and (t - c0) < a
+                k = t - c0
+                visible = c0 <= t < c1 and (k <= a if w.mask_inclusive else k < a)
                 if visible:
                     scores.append(w.scale * sum(Q[n, h, x] * Kc[t, g, x] for x in range(d)))
                     vals.append(Vc[t, g])
             for t in range(nq):                      # every draft row
-                if t // w.B == j:
+                if t // w.B == j and (not w.mask_causal_block or t % w.B <= n % w.B):
                     scores.append(w.scale * sum(Q[n, h, x] * Kd[t, g, x] for x in range(d)))
                     vals.append(Vd[t, g])
             mx = max(scores)
@@ -78,8 +81,10 @@ def sdpa_reference(w, t):
         j = n // w.B
         s = block_sample[j]
         c0 = int(w.cu_ctx[s])
-        mask[n, c0:c0 + int(w.anchors[j])] = True
-        mask[n, T + j * w.B:T + (j + 1) * w.B] = True
+        mask[n, c0:c0 + int(w.anchors[j]) + (1 if w.mask_inclusive else 0)] = True
+        for u in range(w.B):
+            if not w.mask_causal_block or u <= n % w.B:
+                mask[n, T + j * w.B + u] = True
     q = torch.tensor(t["Q"]).permute(1, 0, 2).requires_grad_(True)
     kc = torch.tensor(t["Kc"]).requires_grad_(True)
     vc = torch.tensor(t["Vc"]).requires_grad_(True)
@@ -260,3 +265,99 @@ def test_subset_restriction_equals_masked_dO():
     g_full = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], dO)
     for k in ("dKc", "dVc", "dKd", "dVd"):
         np.testing.assert_allclose(g_sub[k], g_full[k], atol=1e-13, err_msg=k)
+
+
+MASKS = [(True, False), (False, True), (True, True)]
+
+
+@pytest.mark.parametrize("inclusive,causal", MASKS)
+def test_mask_variants_match_brute_force_loops(inclusive, causal):
+    w = tiny_workload(seed=17).with_mask(inclusive, causal)
+    t = _f64(W.tensors(w))
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    Ob, LSEb = brute_force_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    np.testing.assert_allclose(O, Ob, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(LSE, LSEb, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("inclusive,causal", MASKS)
+def test_mask_variants_match_torch_sdpa(inclusive, causal):
+    w = tiny_workload(seed=23, B=3).with_mask(inclusive, causal)
+    t = _f64(W.tensors(w))
+    ref = sdpa_reference(w, t)
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    g = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], t["dO"])
+    np.testing.assert_allclose(O, ref["O"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, ref["LSE"], rtol=0, atol=1e-12)
+    for k in ("dQ", "dKc", "dVc", "dKd", "dVd"):
+        np.testing.assert_allclose(g[k], ref[k], rtol=0, atol=1e-12, err_msg=k)
+
+
+def test_mask_variants_backward_matches_central_differences():
+    w = W.custom(31, lengths=[80], prompts=[30], counts=[3], B=4, Hq=2, Hkv=1, d=8,
+                 chunk=32).with_mask(True, True)
+    t = _f64(W.tensors(w))
+    g = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], t["dO"])
+    rng = np.random.default_rng(3)
+    h = 1e-6
+
+    def loss(tt):
+        O, _ = OA.forward(w, tt["Q"], tt["Kc"], tt["Vc"], tt["Kd"], tt["Vd"])
+        return float((O * tt["dO"]).sum())
+
+    for name, gname in (("Q", "dQ"), ("Kc", "dKc"), ("Vc", "dVc"), ("Kd", "dKd"), ("Vd", "dVd")):
+        arr = t[name]
+        flat_idx = rng.choice(arr.size, size=10, replace=False)
+        if name in ("Kc", "Vc"):  # the anchor rows themselves (visible only when inclusive)
+            flat_idx[:3] = [int(a) * w.d * w.Hkv for a in w.anchors]
+        for fi in flat_idx:
+            idx = np.unravel_index(fi, arr.shape)
+            tp = dict(t); tm = dict(t)
+            tp[name] = arr.copy(); tp[name][idx] += h
+            tm[name] = arr.copy(); tm[name][idx] -= h
+            fd = (loss(tp) - loss(tm)) / (2 * h)
+            assert abs(fd - g[gname][idx]) <= 1e-6 * max(1.0, abs(g[gname][idx])), (name, idx)
+
+
+@pytest.mark.parametrize("inclusive,causal", MASKS)
+def test_mask_variants_any_kv_split_merges_to_unsplit_result(inclusive, causal):
+    w = W.custom(140, lengths=[300, 170], prompts=[60, 20], counts=[5, 3], B=4, Hq=4, Hkv=2,
+                 d=8, chunk=64).with_mask(inclusive, causal)
+    t = _f64(W.tensors(w))
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    edges = [0, 37, 64, 128, 200, 300]
+    parts = [OA.partial_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], lo, hi, False)
+             for lo, hi in zip(edges[:-1], edges[1:])]
+    parts.append(OA.partial_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], 0, 0, True))
+    Om, LSEm = OA.merge(parts)
+    np.testing.assert_allclose(Om, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSEm, LSE, rtol=0, atol=1e-12)
+
+
+def test_inclusive_mask_sees_the_anchor_key_and_no_further():
+    w = W.custom(9, lengths=[50], prompts=[10], counts=[1], B=2, Hq=1, Hkv=1, d=4,
+                 chunk=16).with_mask(True, False)
+    t = _f64(W.tensors(w))
+    a = int(w.anchors[0])
+    base, _ = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    t2 = {k: v.copy() for k, v in t.items()}
+    t2["Vc"][a + 1] = 1e6                       # first invisible key
+    o2, _ = OA.forward(w, t2["Q"], t2["Kc"], t2["Vc"], t2["Kd"], t2["Vd"])
+    assert np.array_equal(base, o2)
+    t3 = {k: v.copy() for k, v in t.items()}
+    t3["Vc"][a] = 1e6                           # the anchor key is now visible
+    o3, _ = OA.forward(w, t3["Q"], t3["Kc"], t3["Vc"], t3["Kd"], t3["Vd"])
+    assert np.abs(o3 - base).max() > 1.0
+
+
+def test_causal_block_first_query_sees_one_draft_key():
+    """Query 0 of a causal block sees draft key 0 only; the last query sees all B."""
+    w = W.custom(12, lengths=[40], prompts=[8], counts=[1], B=4, Hq=1, Hkv=1, d=4,
+                 chunk=16).with_mask(False, True)
+    t = _f64(W.tensors(w))
+    base, _ = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    t2 = {k: v.copy() for k, v in t.items()}
+    t2["Vd"][1:4] = 1e6                         # draft keys 1..3
+    o2, _ = OA.forward(w, t2["Q"], t2["Kc"], t2["Vc"], t2["Kd"], t2["Vd"])
+    assert np.array_equal(base[0], o2[0])       # query 0: unchanged
+    assert np.abs(o2[3] - base[3]).max() > 1.0  # query 3 sees them

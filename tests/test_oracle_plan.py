@@ -25,7 +25,9 @@ def brute_mask_count(w, s, k0, k1):
     L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
     mask = np.zeros((len(anc) * B, L), bool)
     for j, a in enumerate(anc):
-        mask[j * B:(j + 1) * B, :a] = True
+        for k in range(L):  # the set rule, key by key
+            if k < a or (w.mask_inclusive and k == a):
+                mask[j * B:(j + 1) * B, k] = True
     return int(mask[:, k0:k1].sum())
 
 
@@ -132,3 +134,25 @@ def test_grouped_lpt_identity():
 def test_imbalance_definition():
     assert OP.imbalance([10, 10, 10]) == 0.0
     assert abs(OP.imbalance([14, 12, 12]) - (14 / (38 / 3) - 1)) < 1e-15
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_inclusive_items_equal_mask_count(seed):
+    """With the inclusive context [0, a_j] the forward items of every chunk and
+    the backward items of every key tile still sum to the mask count."""
+    rng = np.random.default_rng(50 + seed)
+    lengths = rng.integers(60, 400, size=3).tolist()
+    prompts = [int(rng.integers(0, L // 2)) for L in lengths]
+    counts = [int(rng.integers(1, 8)) for _ in lengths]
+    w = W.custom(seed, lengths, prompts, counts, B=4, Hq=8, Hkv=2, d=4,
+                 chunk=int(rng.choice([32, 64]))).with_mask(True, False)
+    fwd = OP.fwd_items(w)
+    bwd = OP.bwd_items(w)
+    for s in range(3):
+        L = lengths[s]
+        for c, cs in enumerate(range(0, L, w.chunk)):
+            got = sum(it[-1] for it in fwd if it[1] == s and it[2] == c)
+            assert got == brute_mask_count(w, s, cs, min(L, cs + w.chunk)) * w.Hkv
+        for kt, ks in enumerate(range(0, L, OP.KEY_TILE)):
+            got = sum(it[-1] for it in bwd if it[1] == s and it[2] == kt)
+            assert got == brute_mask_count(w, s, ks, min(L, ks + OP.KEY_TILE)) * w.Hkv

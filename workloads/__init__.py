@@ -45,6 +45,11 @@ class Workload:
     d: int
     chunk: int
     seed: int
+    # mask variants (the default is the strict prefix [0, a_j) plus all B
+    # draft keys): inclusive context [0, a_j]; draft keys causal within the
+    # block (query i of a block sees draft keys t <= i)
+    mask_inclusive: bool = False
+    mask_causal_block: bool = False
 
     @property
     def num_samples(self) -> int:
@@ -75,10 +80,19 @@ class Workload:
         """Sample index of every draft block (global block order)."""
         return np.repeat(np.arange(self.num_samples), np.diff(self.cu_anchor))
 
+    def with_mask(self, inclusive: bool = False, causal_block: bool = False) -> "Workload":
+        """The same draw with another mask variant."""
+        tag = ("_incl" if inclusive else "") + ("_causal" if causal_block else "")
+        return dataclasses.replace(self, name=self.name + tag, mask_inclusive=inclusive,
+                                   mask_causal_block=causal_block)
+
     def masked_pairs(self) -> int:
-        """(query, key) pairs per query head: sum over blocks of B*(a_j + B)."""
-        a = self.anchors.astype(np.int64)
-        return int((self.B * (a + self.B)).sum())
+        """(query, key) pairs per query head: sum over blocks of B*(a_j + B)
+        (B*(a_j + 1) context pairs when inclusive, B*(B+1)/2 draft pairs when
+        causal within the block)."""
+        a = self.anchors.astype(np.int64) + (1 if self.mask_inclusive else 0)
+        draft = self.B * (self.B + 1) // 2 if self.mask_causal_block else self.B * self.B
+        return int((self.B * a + draft).sum())
 
     def useful_flop(self, per_pair_per_dim: int = 14) -> int:
         """Useful FLOP of fwd+bwd: Hq * d * c * pairs (c=14: 4 fwd + 10 bwd)."""
