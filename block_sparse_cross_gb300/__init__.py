@@ -42,6 +42,8 @@ SPLITKV_BF16 = 0
 SPLITKV_FP32 = 1
 SPLITKV_FLAG_CUDA_CORE = 1
 SPLITKV_FLAG_CONTIGUOUS = 2
+SPLITKV_FLAG_MASK_INCLUSIVE = 4
+SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
 SPLITKV_NUM_KERNELS = 8
 SPLITKV_NOALLOC_SCRATCH_BYTES = 64 << 20
 (SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,

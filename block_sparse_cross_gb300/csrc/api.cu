@@ -14,7 +14,8 @@ using namespace skv;
 
 namespace {
 
-constexpr int kKnownFlags = SPLITKV_FLAG_CUDA_CORE | SPLITKV_FLAG_CONTIGUOUS;
+constexpr int kKnownFlags = SPLITKV_FLAG_CUDA_CORE | SPLITKV_FLAG_CONTIGUOUS |
+                            SPLITKV_FLAG_MASK_INCLUSIVE | SPLITKV_FLAG_MASK_CAUSAL_BLOCK;
 
 int check_problem(const splitkv_problem* p) {
   if (!p) return SPLITKV_EINVAL;
@@ -88,7 +89,9 @@ uint64_t problem_hash(const splitkv_problem* p, int m) {
   memcpy(&sbits, &p->scale, 4);
   mix(p->num_samples); mix(p->total_ctx); mix(p->total_anchors); mix(p->max_ctx);
   mix(p->B); mix(p->Hq); mix(p->Hkv); mix(p->d); mix(p->chunk); mix(p->dtype);
-  mix(m); mix(p->flags & SPLITKV_FLAG_CONTIGUOUS); mix(sbits);
+  mix(m); mix(sbits);
+  mix(p->flags & (SPLITKV_FLAG_CONTIGUOUS | SPLITKV_FLAG_MASK_INCLUSIVE |
+                  SPLITKV_FLAG_MASK_CAUSAL_BLOCK));
   return h;
 }
 
@@ -114,7 +117,8 @@ ProbDev make_dev(const splitkv_problem* p, int m) {
   P.hash = problem_hash(p, m);
   P.cu_ctx = p->cu_ctx;
   P.cu_anchor = p->cu_anchor;
-  P.anchors = p->anchors;
+  P.anchors = p->anchors;      // replaced by the plan's a_j + 1 table when inclusive
+  P.anchors_in = p->anchors;
   return P;
 }
 
@@ -146,6 +150,9 @@ int setup(const splitkv_problem* p, const void* plan_ws, Ctx* c) {
   c->caps = caps_of(p, kMaxWorkers);
   c->caps.M = kMaxWorkers;
   plan_layout(c->caps, (char*)plan_ws, &c->pp);
+  // every kernel after the planner's validation reads the end of each
+  // block's visible context from P.anchors
+  if (p->flags & SPLITKV_FLAG_MASK_INCLUSIVE) c->P.anchors = c->pp.anchor_end;
   return SPLITKV_OK;
 }
 

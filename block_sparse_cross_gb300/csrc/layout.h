@@ -92,6 +92,8 @@ struct PlanPtrs {
   QEntry* b_queue;
   int64_t* b_load_lpt;
   int64_t* b_load_contig;
+  // [NA] a_j + 1 (end of the visible context) when the mask is inclusive
+  int32_t* anchor_end;
   // [3][workers][2] %globaltimer (ns) at the start and the end of every
   // worker's CTA in the latest forward, dQ and dK/dV attention launch
   uint64_t* busy_ns;
@@ -143,6 +145,7 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   q.b_queue = (QEntry*)take(sizeof(QEntry) * (c.NCB * c.Hkv + 1));
   q.b_load_lpt = (int64_t*)take(8 * c.M);
   q.b_load_contig = (int64_t*)take(8 * c.M);
+  q.anchor_end = (int32_t*)take(4 * (c.NA + 1));
   q.busy_ns = (uint64_t*)take(16 * 3 * c.M);
   if (p) *p = q;
   return align_up(off, 256);
@@ -195,7 +198,8 @@ struct ProbDev {
   uint64_t hash;
   const int32_t* cu_ctx;
   const int32_t* cu_anchor;
-  const int32_t* anchors;
+  const int32_t* anchors;     // end of each block's visible context (a_j, or a_j + 1)
+  const int32_t* anchors_in;  // the caller's anchors (validated by the planner)
 };
 
 }  // namespace skv

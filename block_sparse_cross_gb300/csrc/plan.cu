@@ -126,10 +126,12 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
   for (int64_t i = tid; i < P.NA; i += blockDim.x) {
     const int s = seg_of(P.cu_anchor, S, i);
     const int L = P.cu_ctx[s + 1] - P.cu_ctx[s];
-    const int a = P.anchors[i];
+    const int a = P.anchors_in[i];
     if (a < 0 || a > L - P.B) latch(H, SPLITKV_EMETA);
-    if (i + 1 < P.NA && i + 1 < P.cu_anchor[s + 1] && P.anchors[i + 1] < a)
+    if (i + 1 < P.NA && i + 1 < P.cu_anchor[s + 1] && P.anchors_in[i + 1] < a)
       latch(H, SPLITKV_EMETA);
+    // inclusive context [0, a_j]: every later step works with its end a_j + 1
+    if (P.flags & SPLITKV_FLAG_MASK_INCLUSIVE) pp.anchor_end[i] = a + 1;
   }
   __syncthreads();
   if (read_status(H) != 0) return;

@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   const int j = n / P.B;
   const RowGeom G = row_geom(P, pp, n, h);
   const int x0 = lane * EPL;
-  // draft partial over the block's B draft keys (bidirectional within the block)
+  const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
+  // draft partial over the block's draft keys the row sees: all B
+  // (bidirectional within the block), or t <= n % B for a causal block
   float q[EPL], od[EPL], tmp[EPL];
   ld_vec<T, EPL>(Q + ((size_t)n * P.Hq + h) * D + x0, q);
 #pragma unroll
@@ -156,7 +158,9 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
         sc[u] = part;
       }
     }
-    const bool valid = t0 + kl < P.B;
+    // draft key t is visible to query i = n % B of its block (all t, or t <= i
+    // for a causal block)
+    const bool valid = t0 + kl < P.B && (!causal || t0 + kl <= n % P.B);
     const float s_all = reduce_scatter16(sc, lane);  // every lane takes part in the shuffles
     const float s_mine = valid ? s_all : -INFINITY;
     float mg = s_mine;
@@ -240,7 +244,8 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
 }
 
 // Backward prologue, one warp per (query n, head h):
-//   D = rowsum(dO * O); for each of the block's B draft keys t:
+//   D = rowsum(dO * O); for each of the block's B draft keys t the row sees
+//   (all B, or t <= n % B for a causal block):
 //   P_t = exp(scale q.kd_t - LSE), dS_t = P_t (dO.vd_t - D); the draft term
 //   of dQ = sum_t dS_t kd_t (fp32, unscaled). P_t and dS_t are kept for the
 //   draft key/value gradients.
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, W
   const int j = n / P.B;
   const int x0 = lane * EPL;
   const size_t row = ((size_t)n * P.Hq + h) * D + x0;
+  const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
   float q[EPL], dov[EPL], tmp[EPL];
   ld_vec<T, EPL>(Q + row, q);
   ld_vec<T, EPL>(dO + row, dov);
@@ -302,10 +308,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ProbDev P, PlanPtrs pp, W
     const float s_mine = reduce_scatter16(sp, lane);
     const float dp_mine = reduce_scatter16(dp, lane);
     const int t_mine = t0 + kl;
-    const bool valid = t_mine < P.B;
+    const bool valid = t_mine < P.B && (!causal || t_mine <= n % P.B);
     const float pt = valid ? expf(s_mine * P.scale - lse) : 0.f;
     const float ds = pt * (dp_mine - Dr);
-    if (valid && (lane & 1) == 0) {
+    if (t_mine < P.B && (lane & 1) == 0) {  // 0 for keys a causal block hides
       prow[t_mine] = pt;
       srow[t_mine] = ds;
     }

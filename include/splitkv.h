@@ -84,7 +84,16 @@ enum {
   SPLITKV_FLAG_CUDA_CORE = 1,
   /* Execute the naive contiguous assignment (worker w takes items
    * [floor(w n/m), floor((w+1) n/m)) in id order) instead of LPT. */
-  SPLITKV_FLAG_CONTIGUOUS = 2
+  SPLITKV_FLAG_CONTIGUOUS = 2,
+  /* Mask variants for drafters that share the pattern (the pages name DFlash,
+   * Domino and DSpark, rit.work article, section on when the method changes
+   * the infrastructure plan, without giving their masks):
+   * MASK_INCLUSIVE: block j sees context keys [0, a_j] instead of [0, a_j)
+   *   (chunk costs, tile skipping and masks all use a_j + 1);
+   * MASK_CAUSAL_BLOCK: query i of a block sees its draft keys t <= i only,
+   *   instead of all B. The flags may be combined. */
+  SPLITKV_FLAG_MASK_INCLUSIVE = 4,
+  SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
 };
 
 /*

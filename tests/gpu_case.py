@@ -18,9 +18,16 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
 
 
+def mask_flags(w):
+    """Problem flags of the workload's mask variant."""
+    return ((S.SPLITKV_FLAG_MASK_INCLUSIVE if w.mask_inclusive else 0) |
+            (S.SPLITKV_FLAG_MASK_CAUSAL_BLOCK if w.mask_causal_block else 0))
+
+
 class Case:
     def __init__(self, w, dtype="bf16", flags=0, num_workers=0, seed_offset=1):
         self.w = w
+        flags |= mask_flags(w)
         t = W.tensors(w, seed_offset)
         self.dtype = dtype
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
