@@ -170,26 +170,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer: Q and K (V comes from warp 15) ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       uint32_t nq = 0, nk = 0;
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, Lay::tile);
-        for (int i = 0; i < kSub; ++i)
-          tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+        if (nq > 0 && !(ok = warp_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
+        if (elect_one()) {
+          mbar_expect_tx(q_full, Lay::tile);
+          for (int i = 0; i < kSub; ++i)
+            tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+        }
+        __syncwarp();
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nk % kFwdNK, u = nk / kFwdNK;
           // stage s is free once S of tile nk - 3 is done
-          if (u > 0 && !(ok = mbar_wait(s_full + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = warp_wait(s_full + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
-          mbar_expect_tx(k_full + s, Lay::tile);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          if (elect_one()) {
+            mbar_expect_tx(k_full + s, Lay::tile);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          }
+          __syncwarp();
           ++nk;
         }
       }
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kVWarp) {
     // ---------------- V producer: its own warp, so that it runs in parallel
     // with the Q/K producer instead of taking turns with it ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
@@ -211,12 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nv % kFwdNV;
           // stage s is free once PV of tile nv - 2 is done
-          if (nv >= 2 && !(ok = mbar_wait(sfree + (nv - 2) % 3, ((nv - 2) / 3) & 1, abort_flag)))
+          if (nv >= 2 && !(ok = warp_wait(sfree + (nv - 2) % 3, ((nv - 2) / 3) & 1, abort_flag)))
             break;
           uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
-          mbar_expect_tx(v_full + s, Lay::tile);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          if (elect_one()) {
+            mbar_expect_tx(v_full + s, Lay::tile);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          }
+          __syncwarp();
           ++nv;
         }
       }
@@ -564,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer: Q, dO and K (V comes from warp 15) ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
@@ -572,20 +581,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (nq > 0 && !(ok = mbar_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, 2 * Lay::tile);
-        for (int i = 0; i < kSub; ++i) {
-          tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
-          tma_load_3d(smem + Lay::dO + i * kSubBytes, &tmdO, q_full, 64 * i, I.g * P.group, I.n0);
+        if (nq > 0 && !(ok = warp_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
+        if (elect_one()) {
+          mbar_expect_tx(q_full, 2 * Lay::tile);
+          for (int i = 0; i < kSub; ++i) {
+            tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+            tma_load_3d(smem + Lay::dO + i * kSubBytes, &tmdO, q_full, 64 * i, I.g * P.group, I.n0);
+          }
         }
+        __syncwarp();
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nk % kDqNK, u = nk / kDqNK;
-          if (u > 0 && !(ok = mbar_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = warp_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
-          mbar_expect_tx(k_full + s, Lay::tile);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          if (elect_one()) {
+            mbar_expect_tx(k_full + s, Lay::tile);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(kb + i * kSubBytes, &tmK, k_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          }
+          __syncwarp();
           ++nk;
         }
       }
@@ -597,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kVWarp) {
     // ---------------- V producer (its own warp) ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
@@ -605,11 +620,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nv % kDqNV, u = nv / kDqNV;
-          if (u > 0 && !(ok = mbar_wait(dp_full + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = warp_wait(dp_full + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
-          mbar_expect_tx(v_full + s, Lay::tile);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          if (elect_one()) {
+            mbar_expect_tx(v_full + s, Lay::tile);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(vb + i * kSubBytes, &tmV, v_full + s, 64 * i, I.g, I.row0 + t * kKeyTile);
+          }
+          __syncwarp();
           ++nv;
         }
       }
@@ -929,7 +947,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     // ---------------- producer: K/V per item, then Q and the slab's row table
     // (one bulk copy of the precomputed record) per slab; dO comes from
     // warp 10 ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
       tma_prefetch_desc(&tmK);
@@ -938,23 +956,29 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
       bool ok = true;
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
-        if (nkv > 0 && !(ok = mbar_wait(kv_empty, (nkv - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
-        for (int i = 0; i < kSub; ++i) {
-          tma_load_3d(smem + Lay::k + i * kSubBytes, &tmK, kv_full, 64 * i, I.g, I.c0 + I.ks0);
-          tma_load_3d(smem + Lay::v + i * kSubBytes, &tmV, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+        if (nkv > 0 && !(ok = warp_wait(kv_empty, (nkv - 1) & 1, abort_flag))) break;
+        if (elect_one()) {
+          mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
+          for (int i = 0; i < kSub; ++i) {
+            tma_load_3d(smem + Lay::k + i * kSubBytes, &tmK, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+            tma_load_3d(smem + Lay::v + i * kSubBytes, &tmV, kv_full, 64 * i, I.g, I.c0 + I.ks0);
+          }
         }
+        __syncwarp();
         ++nkv;
         for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
           const uint32_t s = nst % kNS, u = nst / kNS;
-          if (u > 0 && !(ok = mbar_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = warp_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
           const int n0 = pp.sl_first[sg] * P.B;
-          mbar_expect_tx(st_full + s, kSub * kSubBytes + kRowInfoFloats * 4);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(sb + i * kSubBytes, &tmQ, st_full + s, 64 * i, I.g * P.group, n0);
-          bulk_load(sb + Lay::info_off, wk.rowinfo + ((size_t)sg * P.Hkv + I.g) * kRowInfoFloats,
-                    kRowInfoFloats * 4, st_full + s);
+          if (elect_one()) {
+            mbar_expect_tx(st_full + s, kSub * kSubBytes + kRowInfoFloats * 4);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(sb + i * kSubBytes, &tmQ, st_full + s, 64 * i, I.g * P.group, n0);
+            bulk_load(sb + Lay::info_off, wk.rowinfo + ((size_t)sg * P.Hkv + I.g) * kRowInfoFloats,
+                      kRowInfoFloats * 4, st_full + s);
+          }
+          __syncwarp();
           ++nst;
         }
       }
@@ -967,7 +991,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   } else if (warp == kSoftmaxWarps + 2) {
     // ---------------- dO producer: its own warp, so that it runs in parallel
     // with the Q producer instead of taking turns with it ----------------
-    if (lane == 0) {
+    {  // the whole warp runs the loop and waits; one elected lane issues the copies
       tma_prefetch_desc(&tmdO);
       uint32_t nst = 0;
       bool ok = true;
@@ -975,12 +999,15 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
         for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
           const uint32_t s = nst % kNS, u = nst / kNS;
-          if (u > 0 && !(ok = mbar_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
+          if (u > 0 && !(ok = warp_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
           const int n0 = pp.sl_first[sg] * P.B;
-          mbar_expect_tx(st_full + s, kSub * kSubBytes);
-          for (int i = 0; i < kSub; ++i)
-            tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
+          if (elect_one()) {
+            mbar_expect_tx(st_full + s, kSub * kSubBytes);
+            for (int i = 0; i < kSub; ++i)
+              tma_load_3d(sb + (kSub + i) * kSubBytes, &tmdO, st_full + s, 64 * i, I.g * P.group, n0);
+          }
+          __syncwarp();
           ++nst;
         }
       }
