@@ -88,10 +88,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // ===========================================================================
 // Forward
 // ===========================================================================
-// K and V tiles sit in separate rings: a K tile is released as soon as the
-// S MMA that reads it completes, long before the PV MMA releases its V tile,
-// so K loads run further ahead of the MMAs than a shared K+V stage allows.
-constexpr int kFwdNK = 3, kFwdNV = 2;
+// Two 128-column S buffers and two O accumulators fill the 512 TMEM columns
+// at d = 128. Each softmax warp owns one 64-key half of every tile and keeps
+// its own running maximum, row sum and O accumulator (O_h += P_h V_h, the
+// keys of half h), so the two halves never meet during an item; the
+// epilogue combines (m_0, l_0, O_0) and (m_1, l_1, O_1) once per item. The K
+// stage, S buffer and V stage of tile t all have index t % 2.
+constexpr int kFwdNK = 2, kFwdNV = 2;
 
 template <int D>
 struct FwdLayout {
@@ -100,9 +103,8 @@ struct FwdLayout {
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k0 = tile;
   static constexpr uint32_t v0 = k0 + kFwdNK * tile;
-  static constexpr uint32_t xchg = v0 + kFwdNV * tile;  // [2 parity][2 half][128] floats
-  static constexpr uint32_t lm = xchg + 2048;  // [3][128] floats: l of each half, row max
-  static constexpr uint32_t bars = lm + 1536;
+  static constexpr uint32_t lm = v0 + kFwdNV * tile;  // [4][128] floats: l_0, l_1, m_0, m_1
+  static constexpr uint32_t bars = lm + 2048;
   static constexpr uint32_t total = bars + 512 + 1024;  // + alignment slack
 };
 
@@ -115,23 +117,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
-  // Tile t (counted over the CTA's items) uses S buffer, K stage and the
-  // barriers below at index t % 3, and V stage t % 2. S of tile t is issued
-  // once PV of tile t-3 (same buffer) is done; PV of tile t once its P is
-  // written. The K stage is free when S is done (s_full), the V stage when
-  // PV is done (sfree of that tile).
-  static_assert(kFwdNK == 3 && kFwdNV == 2, "ring sizes tied to the S buffers");
+  // Tile t (counted over the CTA's items) uses index b = t % 2. S of tile t
+  // is issued once both PV halves of tile t-2 are done (sfree); PV half h of
+  // tile t once that half's P is written (p_ready[b][h]). The K stage is
+  // free when S is done (s_full), the V stage when PV is done (sfree).
+  static_assert(kFwdNK == 2 && kFwdNV == 2, "ring sizes tied to the S buffers");
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;          // [3]
-  uint64_t* v_full = k_full + kFwdNK;   // [2]
-  uint64_t* s_full = v_full + kFwdNV;   // [3] S of tile t is in buffer t % 3
-  uint64_t* p_ready = s_full + 3;       // [3] its P (bf16) is written over it
-  uint64_t* sfree = p_ready + 3;        // [3] PV of tile t is done
-  uint64_t* o_free = sfree + 3;         // the epilogue has read O and the row sums
-  uint64_t* lm_ready = o_free + 1;      // the softmax has written the item's row sums
+  uint64_t* k_full = bars + 2;          // [2]
+  uint64_t* v_full = k_full + 2;        // [2]
+  uint64_t* s_full = v_full + 2;        // [2] S of tile t is in buffer t % 2
+  uint64_t* p_ready = s_full + 2;       // [2][2] P of half h written over its S half
+  uint64_t* sfree = p_ready + 4;        // [2] both PV halves of tile t are done
+  uint64_t* o_free = sfree + 2;         // the epilogue has read O_0, O_1 and the row sums
+  uint64_t* lm_ready = o_free + 1;      // the softmax has written the item's (m, l)
   uint64_t* mma_drain = lm_ready + 1;   // [2] one per issuing warp
-  uint64_t* xbar = mma_drain + 2;       // [4] row-max exchange per lane quadrant
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(xbar + q, 64);
-    for (int s = 0; s < kFwdNK; ++s) mbar_init(k_full + s, 1);
-    for (int s = 0; s < kFwdNV; ++s) mbar_init(v_full + s, 1);
-    for (int b = 0; b < 3; ++b) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(k_full + b, 1);
+      mbar_init(v_full + b, 1);
       mbar_init(s_full + b, 1);
-      mbar_init(p_ready + b, kSoftmaxWarps);
+      mbar_init(p_ready + 2 * b, kSoftmaxWarps / 2);
+      mbar_init(p_ready + 2 * b + 1, kSoftmaxWarps / 2);
       mbar_init(sfree + b, 1);
     }
     mbar_init(o_free, 4);
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 384;  // three 128-column S buffers, then O
+  const uint32_t tS = tmem, tO = tmem + 256;  // two S buffers, then O_0 and O_1 (D columns each)
   float* lm = (float*)(smem + Lay::lm);
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nk % kFwdNK, u = nk / kFwdNK;
-          // stage s is free once S of tile nk - 3 is done
+          // stage s is free once S of tile nk - 2 is done
           if (u > 0 && !(ok = warp_wait(s_full + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* kb = smem + Lay::k0 + s * Lay::tile;
           if (elect_one()) {
@@ -215,10 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qi = q0; qi < q1 && ok; ++qi) {
         const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
         for (int t = 0; t < I.ntiles; ++t) {
-          const uint32_t s = nv % kFwdNV;
-          // stage s is free once PV of tile nv - 2 is done
-          if (nv >= 2 && !(ok = warp_wait(sfree + (nv - 2) % 3, ((nv - 2) / 3) & 1, abort_flag)))
-            break;
+          const uint32_t s = nv % kFwdNV, u = nv / kFwdNV;
+          // stage s is free once both PV halves of tile nv - 2 are done
+          if (u > 0 && !(ok = warp_wait(sfree + s, (u - 1) & 1, abort_flag))) break;
           uint8_t* vb = smem + Lay::v0 + s * Lay::tile;
           if (elect_one()) {
             mbar_expect_tx(v_full + s, Lay::tile);
@@ -247,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
       if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
-        const uint32_t b = ns % 3;
-        if (!(ok = warp_wait(k_full + b, (ns / 3) & 1, abort_flag))) break;
-        if (ns >= 3 && !(ok = warp_wait(sfree + b, (ns / 3 - 1) & 1, abort_flag))) break;
+        const uint32_t b = ns & 1;
+        if (!(ok = warp_wait(k_full + b, (ns >> 1) & 1, abort_flag))) break;
+        if (ns >= 2 && !(ok = warp_wait(sfree + b, ((ns >> 1) - 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + b * Lay::tile));
         if (elect_one()) {
@@ -267,28 +266,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait_drain(mma_drain, 0, kDrainNs);
   } else if (warp == kSoftmaxWarps + 2) {
-    // ---------------- PV issuer ----------------
+    // ---------------- PV issuer: O_h += P_h V_h, half by half ----------------
     constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
     uint32_t np = 0, nit = 0;
     bool ok = true;
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      for (int t = 0; t < I.ntiles; ++t, ++np) {
-        const uint32_t b = np % 3, vs = np % kFwdNV;
-        if (!(ok = warp_wait(p_ready + b, (np / 3) & 1, abort_flag))) break;
+      for (int t = 0; t < I.ntiles && ok; ++t, ++np) {
+        const uint32_t b = np & 1;
+        if (!(ok = warp_wait(v_full + b, (np >> 1) & 1, abort_flag))) break;
         if (t == 0 && nit > 0 && !(ok = warp_wait(o_free, (nit - 1) & 1, abort_flag))) break;
-        if (!(ok = warp_wait(v_full + vs, (np / kFwdNV) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint64_t vd0 = desc_mnmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
+        const uint64_t vd0 = desc_mnmajor0(smem_u32(smem + Lay::v0 + b * Lay::tile));
         const uint32_t ta = tS + b * 128;
-        if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kKeyTile / 16; ++kk)
-            mma_ts(tO, ta + a_col(kk), vd0 + (mnmajor_off(kk) >> 4), kIdPV,
-                   (t == 0 && kk == 0) ? 0u : 1u);
-          mma_commit(sfree + b);
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = warp_wait(p_ready + 2 * b + h, (np >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+              mma_ts(tO + h * D, ta + a_col(kk), vd0 + (mnmajor_off(kk) >> 4), kIdPV,
+                     (t == 0 && kk == 4 * h) ? 0u : 1u);
+            if (h == 1) mma_commit(sfree + b);  // both halves; also frees V stage b
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     if (elect_one()) mma_commit(mma_drain + 1);
@@ -296,9 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
-    // Waits for the item's last PV and its row sums, loads O, releases it
-    // (and the row sums) to the next item, then writes the chunk partial
-    // (O / l, lse): the softmax warps never wait for it.
+    // Waits for the item's last PV and its (m, l) per half, combines the
+    // halves (O = sum_h 2^(m_h - m) O_h, l = sum_h 2^(m_h - m) l_h), releases
+    // the accumulators and writes the chunk partial (O / l, lse): the softmax
+    // warps never wait for it.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -309,56 +312,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       ns += I.ntiles;
       const uint32_t pt = ns - 1;  // the item's last tile
       if (!(ok = warp_wait(lm_ready, nit & 1, abort_flag))) break;
-      if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
+      if (!(ok = warp_wait(sfree + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      const float lt = lm[r] + lm[128 + r];  // column half 0, then half 1
-      const float m_run = lm[256 + r];
+      const float m0 = lm[256 + r], m1 = lm[384 + r];  // log2 units
+      const float m = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - m);
+      const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - m);
+      const float lt = lm[r] * w0 + lm[128 + r] * w1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float f0 = w0 * inv, f1 = w1 * inv;
       float* po = wk.part_o + (I.slot * kRows + r) * D;
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
-        uint32_t v[64];
-        tmem_ld_row<64>(tO + lane_base + 64 * h, v);
-        if (h == D / 64 - 1) {  // O and the row sums are in registers
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {  // 32 columns of each half at a time (register budget)
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tO + lane_base + 32 * c, v0);
+        tmem_ld32(tO + D + lane_base + 32 * c, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        if (c == D / 32 - 1) {  // O and the row statistics are in registers
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(o_free);
         }
 #pragma unroll
-        for (int i = 0; i < 64; i += 8)
-          st_global_v8(po + 64 * h + i, __uint_as_float(v[i]) * inv,
-                       __uint_as_float(v[i + 1]) * inv, __uint_as_float(v[i + 2]) * inv,
-                       __uint_as_float(v[i + 3]) * inv, __uint_as_float(v[i + 4]) * inv,
-                       __uint_as_float(v[i + 5]) * inv, __uint_as_float(v[i + 6]) * inv,
-                       __uint_as_float(v[i + 7]) * inv);
+        for (int i = 0; i < 32; i += 8) {
+          float o[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = fmaf(__uint_as_float(v0[i + k]), f0, __uint_as_float(v1[i + k]) * f1);
+          st_global_v8(po + 32 * c + i, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+        }
       }
-      wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+      wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
     }
   } else {
     // ---------------- softmax (warps 2..9) ----------------
-    // Warp w owns TMEM lane quadrant w % 4 (rows r) and column half hf of S;
-    // the two warps of a quadrant exchange their row maxima every tile
-    // through shared memory, paced by that quadrant's 64-thread mbarrier.
-    constexpr int OH = D / 2;
+    // Warp w owns TMEM lane quadrant w % 4 (rows r) and key half hf of every
+    // tile, with its own running maximum m_run (log2 units), row sum l and
+    // accumulator O_hf; lazy rescale keeps exponents <= 2^8.
     const int wq = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
-    float* xm = (float*)(smem + Lay::xchg);
-    uint32_t ns = 0, nx = 0;
+    const uint32_t tOh = tO + hf * D + lane_base;
+    uint32_t ns = 0;
     bool ok = true;
-    auto exchange = [&](float mine, float* other) -> bool {
-      float* buf = xm + (nx & 1) * 256;
-      buf[hf * 128 + r] = mine;
-      mbar_arrive(xbar + wq);
-      const bool got = warp_wait(xbar + wq, nx & 1, abort_flag);
-      *other = buf[(1 - hf) * 128 + r];
-      ++nx;
-      return got;
-    };
-    // The next item's record and row are loaded before this item's epilogue
-    // waits, so their dependent global loads overlap it.
+    // The next item's record and row are loaded before this item ends, so
+    // their dependent global loads overlap its last tile.
     FwdItem In{};
     RowInfo rin{};
     if (q0 < q1) {
@@ -368,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int qi = q0, nit = 0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = In;
       const RowInfo ri = rin;
-      float m_run = -INFINITY, l = 0.f;  // l: this half's partial row sum
+      float m_run = -INFINITY, l = 0.f;
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
-        const uint32_t sb = ns % 3;
-        if (!(ok = warp_wait(s_full + sb, (ns / 3) & 1, abort_flag))) break;
+        const uint32_t sb = ns & 1;
+        if (!(ok = warp_wait(s_full + sb, (ns >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         // padding rows (beyond the slab's blocks) compute on whatever Q rows the
         // tile box holds; their partials are never read
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (i >= lim) x[i] = __float_as_uint(-INFINITY);
         }
-        // row max: eight chains of three-input maxima
+        // row max of this half: eight chains of three-input maxima
         float mx[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
@@ -396,10 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx[k] = max3f(mx[k], __uint_as_float(x[i + k]), __uint_as_float(x[i + 8 + k]));
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[56 + k]));
-        const float mh = fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], max3f(mx[5], mx[6], mx[7])));
-        float mo;
-        if (!(ok = exchange(mh, &mo))) break;
-        const float mt = fmaxf(mh, mo) * sl2;
+        const float mt =
+            fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], max3f(mx[5], mx[6], mx[7]))) * sl2;
         const float m_new = fmaxf(m_run, mt);
         float fac = 1.f;
         bool resc = false;
@@ -437,38 +436,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = (t == 0) ? ls : l * fac + ls;
         tmem_st32(tS + lane_base + sb * 128 + 64 * hf, pk);  // packed P of this half: a_col()
         tmem_st_wait();
-        // O holds the PVs of tiles before t only once the PV of tile t-1 is
-        // done; wait for it only when O must be rescaled (rare).
-        if (t > 0 && __any_sync(0xffffffffu, resc)) {  // same decision in both halves
+        // O_hf holds the PVs of tiles before t only once the PV of tile t-1
+        // is done; wait for it only when O_hf must be rescaled (rare).
+        if (t > 0 && __any_sync(0xffffffffu, resc)) {
           const uint32_t pt = ns - 1;
-          if (!(ok = warp_wait(sfree + pt % 3, (pt / 3) & 1, abort_flag))) break;
+          if (!(ok = warp_wait(sfree + (pt & 1), (pt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
-          {
-            uint32_t v[OH];
-            tmem_ld_row<OH>(tO + lane_base + OH * hf, v);
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t v[64];
+            tmem_ld_row<64>(tOh + 64 * c, v);
 #pragma unroll
-            for (int i = 0; i < OH; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac);
-            if constexpr (OH == 64) {
-              tmem_st64(tO + lane_base + OH * hf, v);
-            } else {
-              tmem_st32(tO + lane_base + OH * hf, v);
-            }
+            for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * fac);
+            tmem_st64(tOh + 64 * c, v);
             tmem_st_wait();
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready + sb);
+        if (lane == 0) mbar_arrive(p_ready + 2 * sb + hf);
       }
       if (!ok) break;
       if (qi + 1 < q1) {
         In = fwd_item(P, pp, pp.f_queue[qi + 1]);
         rin = row_info(P, In.first, In.nblk, In.g, r);
       }
-      // hand the row sums to the epilogue once it has read the previous item's
+      // hand (m, l) of this half to the epilogue once it has read the previous item's
       if (nit > 0 && !(ok = warp_wait(o_free, (nit - 1) & 1, abort_flag))) break;
       lm[hf * 128 + r] = l;
-      if (hf == 0) lm[256 + r] = m_run;
+      lm[256 + hf * 128 + r] = m_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(lm_ready);
     }
