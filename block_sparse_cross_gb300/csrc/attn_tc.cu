@@ -483,6 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // dQ (same items as the forward)
 // ===========================================================================
+// Q and dO are constant over an item, so they are copied once per item from
+// their shared-memory tiles into TMEM and S = Q K^T, dP = dO V^T run as TS
+// MMAs: only K and V are read from shared memory (16 KB per k step instead
+// of 32 KB), which is what bounds these 128x128 products. TMEM: two
+// 128-column regions, tile t using region t % 2 for S, then dP (written over
+// S once the softmax has loaded it), then dS (bf16, over dP); the dQ
+// accumulator (D columns); Q and dO (D / 2 packed columns each).
 // K is read by S (early) and by dQ (late) of its tile, V only by dP: a ring
 // of three K tiles and a ring of two V tiles, each released after its last
 // reader.
@@ -500,6 +507,19 @@ struct DqLayout {
   static constexpr uint32_t total = bars + 512 + 1024;
 };
 
+// Row r of a [128 rows][64 bf16] sub-tile laid out by a 128-byte-swizzled TMA
+// box: its 16-byte chunk c sits at chunk c ^ (r % 8) of the row.
+__device__ __forceinline__ void lds_row_sw128(const uint8_t* sub, int r, uint32_t (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 x = *(const uint4*)(sub + r * 128 + ((c ^ (r & 7)) << 4));
+    v[4 * c] = x.x;
+    v[4 * c + 1] = x.y;
+    v[4 * c + 2] = x.z;
+    v[4 * c + 3] = x.w;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -510,22 +530,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
+  uint64_t* q_full = bars + 0;          // Q, dO of the item in shared memory
+  uint64_t* q_empty = bars + 1;         // ... copied to TMEM (4 arrivals)
   uint64_t* k_full = bars + 2;          // [kDqNK]
   uint64_t* k_empty = k_full + kDqNK;
   // V is read only by dP: V stage and dp_full of tile t are both t % 2, so
   // dP's commit frees the V stage.
   static_assert(kDqNV == 2, "V ring size tied to dp_full");
   uint64_t* v_full = k_empty + kDqNK;   // [kDqNV]
-  uint64_t* s_full = v_full + kDqNV;   // S of tile t is in TMEM
-  uint64_t* s_read = s_full + 1;       // softmax has loaded S: its region is free
-  uint64_t* dp_full = s_read + 1;      // [2] dP of tile t (alternating)
-  uint64_t* p_ready = dp_full + 2;     // [2] softmax wrote dS (bf16) over dP of tile t
-  uint64_t* rfree = p_ready + 2;       // [2] the dQ MMA of tile t has read its dS region
-  uint64_t* dq_done = rfree + 2;
+  uint64_t* s_full = v_full + kDqNV;    // S of tile t is in its region
+  uint64_t* s_read = s_full + 1;        // softmax has loaded S: dP may overwrite it
+  uint64_t* dp_full = s_read + 1;       // [2] dP of tile t (by tile parity)
+  uint64_t* p_ready = dp_full + 2;      // [2] softmax wrote dS (bf16) over dP of tile t
+  uint64_t* rfree = p_ready + 2;        // [2] the dQ MMA of tile t has read dS: region free
+  uint64_t* qt_ready = rfree + 2;       // Q, dO of the item are in TMEM (4 arrivals)
+  uint64_t* qt_empty = qt_ready + 1;    // the item's S and dP MMAs are done with them
+  uint64_t* dq_done = qt_empty + 1;
   uint64_t* dq_free = dq_done + 1;
-  uint64_t* mma_drain = dq_free + 1;   // [2] one per issuing warp
+  uint64_t* mma_drain = dq_free + 1;    // [2] one per issuing warp
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -534,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, 4);
     for (int s = 0; s < kDqNK; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -547,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_ready + b, kSoftmaxWarps);
       mbar_init(rfree + b, 1);
     }
+    mbar_init(qt_ready, 4);
+    mbar_init(qt_empty, 1);
     mbar_init(dq_done, 1);
     mbar_init(dq_free, 4);
     mbar_init(mma_drain, 1);
@@ -562,9 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM: S at columns 0..127 (released as soon as the softmax has loaded it),
-  // dP of tile t (then dS over it) at region 1 + t % 2, dQ at 384.
-  const uint32_t tdQ = tmem + 384;
+  // regions: tmem + 128 * (t % 2)
+  const uint32_t tdQ = tmem + 256;           // D columns
+  const uint32_t tQ = tdQ + D;               // D / 2 columns: Q, bf16 pairs
+  const uint32_t tdO = tQ + D / 2;           // D / 2 columns: dO
   const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
 
   if (warp == 0) {
@@ -634,42 +659,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- S and dP issuer (whole warp, one elected lane) ----------------
-    // dP of tile t lands on the region the dQ MMA of tile t-2 read: wait for
-    // that MMA (issued by the other warp) through rfree.
+    // S of tile t lands on the region the dQ MMA of tile t-2 read (rfree);
+    // dP of tile t lands on S once the softmax has loaded it (s_read).
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-    const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
-    const uint64_t dod0 = desc_kmajor0(smem_u32(smem + Lay::dO));
-    uint32_t gt = 0, nit = 0;  // gt: tiles issued (TMEM region, K and V ring index)
+    uint32_t gt = 0, nit = 0;  // gt: tiles issued (K and V ring index)
     bool ok = true;
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      if (!(ok = warp_wait(qt_ready, nit & 1, abort_flag))) break;
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
-        const uint32_t ks = gt % kDqNK, vs = gt % kDqNV;
+        const uint32_t ks = gt % kDqNK, vs = gt % kDqNV, b = gt & 1;
+        const uint32_t tR = tmem + 128 * b;
         if (!(ok = warp_wait(k_full + ks, (gt / kDqNK) & 1, abort_flag))) break;
-        if (!(ok = warp_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
-        if (gt > 0 && !(ok = warp_wait(s_read, (gt - 1) & 1, abort_flag))) break;
+        if (gt >= 2 && !(ok = warp_wait(rfree + b, ((gt >> 1) - 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t kd0 = desc_kmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
-        const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
-        const uint32_t rP = 1 + (gt & 1);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
-                   kk > 0 ? 1u : 0u);
+            mma_ts(tR, tQ + kk * 8, kd0 + (kmajor_off(kk) >> 4), kIdS, kk > 0 ? 1u : 0u);
           mma_commit(s_full);
         }
         __syncwarp();
-        if (gt >= 2 && !(ok = warp_wait(rfree + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(v_full + vs, (gt / kDqNV) & 1, abort_flag))) break;
+        if (!(ok = warp_wait(s_read, gt & 1, abort_flag))) break;
         tc_fence_after();
+        const uint64_t vd0 = desc_kmajor0(smem_u32(smem + Lay::v0 + vs * Lay::tile));
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + rP * 128, dod0 + (kmajor_off(kk) >> 4), vd0 + (kmajor_off(kk) >> 4),
-                   kIdS, kk > 0 ? 1u : 0u);
+            mma_ts(tR, tdO + kk * 8, vd0 + (kmajor_off(kk) >> 4), kIdS, kk > 0 ? 1u : 0u);
           mma_commit(dp_full + (gt & 1));  // also frees V stage vs == gt % 2
-          if (t == I.ntiles - 1) mma_commit(q_empty);  // Q and dO are read by S and dP only
+          if (t == I.ntiles - 1) mma_commit(qt_empty);  // Q and dO in TMEM are free
         }
         __syncwarp();
       }
@@ -685,18 +706,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
-        if (!(ok = warp_wait(p_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+        const uint32_t b = gt & 1;
+        if (!(ok = warp_wait(p_ready + b, (gt >> 1) & 1, abort_flag))) break;
         if (t == 0 && nit > 0 && !(ok = warp_wait(dq_free, (nit - 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t ks = gt % kDqNK;
         const uint64_t kd0 = desc_mnmajor0(smem_u32(smem + Lay::k0 + ks * Lay::tile));
-        const uint32_t ta = tmem + (1 + (gt & 1)) * 128;
+        const uint32_t tR = tmem + 128 * b;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk)
-            mma_ts(tdQ, ta + a_col(kk), kd0 + (mnmajor_off(kk) >> 4), kIdQ,
+            mma_ts(tdQ, tR + a_col(kk), kd0 + (mnmajor_off(kk) >> 4), kIdQ,
                    (t == 0 && kk == 0) ? 0u : 1u);
-          mma_commit(rfree + (gt & 1));
+          mma_commit(rfree + b);
           mma_commit(k_empty + ks);
           if (t == I.ntiles - 1) mma_commit(dq_done);
         }
@@ -707,17 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-    // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
-    // Loads the item's dQ partial once its last dQ MMA is done, releases the
-    // accumulator to the next item and writes the partial.
+    // ---------------- Q/dO copy and epilogue (warps 11..14): one lane quadrant each ----------------
+    // Per item: copy the rows of Q and dO from their swizzled shared-memory
+    // tiles into TMEM (once the previous item's S and dP are done with
+    // them); then write the previous item's dQ partial once its last dQ MMA
+    // is done, releasing the accumulator right after loading it.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     bool ok = true;
-    uint32_t nit = 0;
-    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      if (!(ok = warp_wait(dq_done, nit & 1, abort_flag))) break;
+    auto write_dq = [&](const FwdItem& I, uint32_t it) -> bool {
+      if (!warp_wait(dq_done, it & 1, abort_flag)) return false;
       tc_fence_after();
       float* po = wk.part_o + (I.slot * kRows + r) * D;
 #pragma unroll 1
@@ -736,10 +758,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                        __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
                        __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
       }
+      return true;
+    };
+    FwdItem Iprev{};
+    uint32_t nit = 0;
+    for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
+      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      if (nit > 0 && !(ok = warp_wait(qt_empty, (nit - 1) & 1, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {  // Q, then dO
+        const uint8_t* tile = smem + (which == 0 ? Lay::q : Lay::dO);
+        const uint32_t tcol = (which == 0 ? tQ : tdO) + lane_base;
+#pragma unroll 1
+        for (int sub = 0; sub < kSub; ++sub) {
+          uint32_t v[32];
+          lds_row_sw128(tile + sub * kSubBytes, r, v);
+          tmem_st32(tcol + 32 * sub, v);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(qt_ready);
+        mbar_arrive(q_empty);  // the shared-memory tiles may take the next item
+      }
+      if (nit > 0 && !(ok = write_dq(Iprev, nit - 1))) break;
+      Iprev = I;
     }
+    if (ok && nit > 0) write_dq(Iprev, nit - 1);
   } else {
     // softmax (warps 2..9): lane quadrant warp % 4, column half hf
-    constexpr int OH = D / 2;
     const int wq = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
@@ -748,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gt = 0, nit = 0;
     bool ok = true;
     // The next item's record, row and row statistics are loaded before this
-    // item's epilogue waits, so their dependent global loads overlap it.
+    // item's last tile ends, so their dependent global loads overlap it.
     FwdItem In{};
     RowInfo rin{};
     float nl2n = -INFINITY, Drn = 0.f;
@@ -773,15 +824,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int lim =
             (ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile)) - 64 * hf;
-        const uint32_t sa = tmem + lane_base + 64 * hf;
-        const uint32_t pa = tmem + lane_base + (1 + (gt & 1)) * 128 + 64 * hf;
+        // S, then dP, then dS of this tile: region gt % 2, this half's columns
+        const uint32_t sa = tmem + 128 * (gt & 1) + lane_base + 64 * hf;
+        const uint32_t pa = sa;
         // phase 1 (while dP of this tile and dQ of the previous one run):
         // P = exp(S * scale - LSE) on the row's visible keys, kept as bf16
         uint32_t pk[32];
         {
           uint32_t sv[64];
           tmem_ld_row<64>(sa, sv);
-          tc_fence_before();  // S is in registers: let the next S overwrite it
+          tc_fence_before();  // S is in registers: dP may overwrite it
           __syncwarp();
           if (lane == 0) mbar_arrive(s_read);
           if (__all_sync(0xffffffffu, lim >= 64)) {
