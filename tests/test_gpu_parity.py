@@ -49,6 +49,9 @@ FUZZ = [
     ([1500], [200], [33], 1, 4, 1, 128, 384),
     ([513, 900], [0, 0], [5, 17], 8, 4, 2, 64, 512),
     ([4096, 130], [1000, 0], [21, 3], 16, 32, 8, 128, 1024),
+    # one draft block per 128-row slab (B * group = 128), B up to 128
+    ([2500, 700], [100, 0], [11, 4], 32, 8, 2, 128, 512),
+    ([3000], [500], [6], 128, 2, 2, 64, 1024),
 ]
 
 
