@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
   // draft partial over the block's draft keys the row sees: all B
   // (bidirectional within the block), or t <= n % B for a causal block
-  float q[EPL], od[EPL], tmp[EPL];
+  float q[EPL], od[EPL];
   ld_vec<T, EPL>(Q + ((size_t)n * P.Hq + h) * D + x0, q);
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -380,6 +380,166 @@ __global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp,
   }
 }
 
+// The whole backward of one draft block's B x B self-attention block for one
+// kv head, in one CTA (blocks with B <= 32 and B * group <= 64 rows): the
+// block's draft keys and values are staged once in shared memory; warp w
+// takes rows w, w + 8, ...: D = rowsum(dO * O), the B scores and dP values
+// (reduce-scattered over the lanes), P = exp(scale q.kd_t - LSE) (0 for keys
+// a causal block hides), dS = P (dP - D), and the row's draft term of dQ =
+// sum_t dS_t kd_t (fp32, unscaled); then one thread per (head dim, key
+// group) sums dVd[t] = sum_r P_t(r) dO_r and dKd[t] = scale * sum_r dS_t(r)
+// q_r over the rows in fixed order.
+constexpr int kDraftBM = 32, kDraftRM = 64;
+
+// EPL consecutive floats of shared memory (16- or 8-byte aligned) in one load.
+template <int EPL>
+__device__ __forceinline__ void lds_vec(const float* p, float (&v)[EPL]) {
+  if constexpr (EPL == 4) {
+    const float4 t = *(const float4*)p;
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    static_assert(EPL == 2, "head dim 64 or 128");
+    const float2 t = *(const float2*)p;
+    v[0] = t.x; v[1] = t.y;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                              const T* __restrict__ Q,
+                                                              const T* __restrict__ Kd,
+                                                              const T* __restrict__ Vd,
+                                                              const T* __restrict__ O,
+                                                              const float* __restrict__ LSE,
+                                                              const T* __restrict__ dO,
+                                                              T* __restrict__ dKd,
+                                                              T* __restrict__ dVd) {
+  constexpr int EPL = D / 32;
+  extern __shared__ float sm[];
+  float* kd_s = sm;                      // [B][D]
+  float* vd_s = kd_s + kDraftBM * D;     // [B][D]
+  float* ps = vd_s + kDraftBM * D;       // [R][kDraftBM]  P
+  float* dss = ps + kDraftRM * kDraftBM; // [R][kDraftBM]  dS
+  if (read_status(pp.hdr) != 0) return;
+  const int B = P.B, G = P.group, R = B * G;
+  const int j = blockIdx.x, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
+  for (int i = threadIdx.x; i < B * D; i += blockDim.x) {
+    const size_t o = ((size_t)(j * B + i / D) * P.Hkv + g) * D + i % D;
+    kd_s[i] = ld_f(Kd + o);
+    vd_s[i] = ld_f(Vd + o);
+  }
+  __syncthreads();
+  const int x0 = lane * EPL;
+  const int kl = (lane >> 1) & 15;  // the key this lane's pair holds after a reduce-scatter
+  // rows are prefetched one step ahead: their loads overlap the previous row
+  auto row_of = [&](int rr) {
+    return ((size_t)(j * B + rr / G) * P.Hq + g * G + rr % G) * D + x0;
+  };
+  float qn[EPL], don[EPL], onx[EPL];
+  if (warp < R) {
+    ld_vec<T, EPL>(Q + row_of(warp), qn);
+    ld_vec<T, EPL>(dO + row_of(warp), don);
+    ld_vec<T, EPL>(O + row_of(warp), onx);
+  }
+  for (int r = warp; r < R; r += 8) {
+    const int n = j * B + r / G, h = g * G + r % G;
+    const size_t row = ((size_t)n * P.Hq + h) * D + x0;
+    float q[EPL], dov[EPL], ov[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      q[i] = qn[i];
+      dov[i] = don[i];
+      ov[i] = onx[i];
+    }
+    if (r + 8 < R) {
+      ld_vec<T, EPL>(Q + row_of(r + 8), qn);
+      ld_vec<T, EPL>(dO + row_of(r + 8), don);
+      ld_vec<T, EPL>(O + row_of(r + 8), onx);
+    }
+    float dd = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) dd = fmaf(dov[i], ov[i], dd);
+    const float Dr = warp_sum(dd);
+    const float lse = LSE[(size_t)h * P.NQ + n];
+    if (lane == 0) wk.dvec[(size_t)h * P.NQ + n] = Dr;
+    float acc[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+    for (int t0 = 0; t0 < B; t0 += 16) {
+      float sp[16], dp[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int t = min(t0 + u, B - 1);
+        float kr[EPL], vr[EPL];
+        lds_vec<EPL>(kd_s + t * D + x0, kr);
+        lds_vec<EPL>(vd_s + t * D + x0, vr);
+        sp[u] = 0.f;
+        dp[u] = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          sp[u] = fmaf(q[i], kr[i], sp[u]);
+          dp[u] = fmaf(dov[i], vr[i], dp[u]);
+        }
+      }
+      const float s_mine = reduce_scatter16(sp, lane);
+      const float dp_mine = reduce_scatter16(dp, lane);
+      const int t_mine = t0 + kl;
+      const bool valid = t_mine < B && (!causal || t_mine <= n % B);
+      const float pt = valid ? expf(s_mine * P.scale - lse) : 0.f;
+      const float ds = pt * (dp_mine - Dr);
+      if (t_mine < B && (lane & 1) == 0) {  // 0 for keys a causal block hides
+        ps[r * kDraftBM + t_mine] = pt;
+        dss[r * kDraftBM + t_mine] = ds;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {  // dS of keys past B is 0
+        const float du = __shfl_sync(0xffffffffu, ds, 2 * u);
+        float kr[EPL];
+        lds_vec<EPL>(kd_s + min(t0 + u, B - 1) * D + x0, kr);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc[i] = fmaf(du, kr[i], acc[i]);
+      }
+    }
+    float* dqd = wk.dq_draft + row;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) dqd[i] = acc[i];
+  }
+  __syncthreads();
+  // dVd and dKd: thread (x, key group); groups of 16 keys at a time
+  constexpr int KG = 256 / D;  // key groups (2 at d = 128, 4 at d = 64)
+  const int x = threadIdx.x % D, kg = threadIdx.x / D;
+  for (int t0 = kg * 16; t0 < B; t0 += KG * 16) {
+    float av[16], ak[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) av[k] = ak[k] = 0.f;
+#pragma unroll 4
+    for (int r = 0; r < R; ++r) {
+      const int n = j * B + r / G, h = g * G + r % G;
+      const size_t o = ((size_t)n * P.Hq + h) * D + x;
+      const float dv = ld_f(dO + o), qv = ld_f(Q + o);
+      const float* pr = ps + r * kDraftBM + t0;
+      const float* sr = dss + r * kDraftBM + t0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (t0 + k < B) {
+          av[k] = fmaf(pr[k], dv, av[k]);
+          ak[k] = fmaf(sr[k], qv, ak[k]);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (t0 + k < B) {
+        const size_t o = ((size_t)(j * B + t0 + k) * P.Hkv + g) * D + x;
+        st_f(dVd + o, av[k]);
+        st_f(dKd + o, ak[k] * P.scale);
+      }
+    }
+  }
+}
+
 // Row table of every (slab, kv head) for the dK/dV kernel, which streams it
 // with the slab's Q / dO tiles: -LSE*log2(e) (-inf on padding rows, so their
 // P is 0 without masking), D, and the row's anchor.
@@ -481,16 +641,27 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
     constexpr int D = decltype(dtag)::value;
     const int64_t warps = P.NQ * P.Hq;
     if (warps == 0) return cudaSuccess;
-    bwd_prep_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-        P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O, LSE, (const T*)dO);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    const size_t smem = sizeof(float) * 2 * (size_t)P.B * P.group * P.B;
-    auto k = bwd_draft_kv_kernel<T, D>;
-    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
+    cudaError_t err;
     dim3 grid((unsigned)P.NA, (unsigned)P.Hkv);
-    k<<<grid, D, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)dO, (T*)dKd, (T*)dVd);
+    if (P.B <= kDraftBM && P.B * P.group <= kDraftRM) {
+      // one CTA per (draft block, kv head) does the whole draft-block backward
+      const size_t smem = sizeof(float) * (2 * kDraftBM * D + 2 * kDraftRM * kDraftBM);
+      auto k = bwd_draft_block_kernel<T, D>;
+      err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      k<<<grid, 256, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O,
+                                 LSE, (const T*)dO, (T*)dKd, (T*)dVd);
+    } else {  // larger blocks: one warp per row, then one CTA per (block, kv head)
+      bwd_prep_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+          P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (const T*)O, LSE, (const T*)dO);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+      const size_t smem = sizeof(float) * 2 * (size_t)P.B * P.group * P.B;
+      auto k = bwd_draft_kv_kernel<T, D>;
+      err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      k<<<grid, D, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)dO, (T*)dKd, (T*)dVd);
+    }
     err = cudaGetLastError();
     if (err != cudaSuccess || nsl_cap == 0) return err;
     slab_rowinfo_kernel<<<dim3((unsigned)nsl_cap, (unsigned)P.Hkv), kRows, 0, st>>>(P, pp, wk, LSE);
