@@ -108,21 +108,31 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
   return x + __shfl_xor_sync(0xffffffffu, x, 1);
 }
 
-// One warp per (query n, head h); lane owns dims [lane*EPL, lane*EPL + EPL).
-template <typename T, int D>
-__global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
-                                                    const T* __restrict__ Q,
-                                                    const T* __restrict__ Kd,
-                                                    const T* __restrict__ Vd,
-                                                    T* __restrict__ O, float* __restrict__ LSE) {
+constexpr int kDraftBM = 32, kDraftRM = 64;
+
+// EPL consecutive floats of shared memory (16- or 8-byte aligned) in one load.
+template <int EPL>
+__device__ __forceinline__ void lds_vec(const float* p, float (&v)[EPL]) {
+  if constexpr (EPL == 4) {
+    const float4 t = *(const float4*)p;
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    static_assert(EPL == 2, "head dim 64 or 128");
+    const float2 t = *(const float2*)p;
+    v[0] = t.x; v[1] = t.y;
+  }
+}
+
+// Merge of one (query n, head h) row by one warp; lane owns dims
+// [lane*EPL, lane*EPL + EPL). kd_row / vd_row(t, v) fetch this lane's dims of
+// draft key / value t of the row's block (from global memory or shared).
+template <typename T, int D, typename KF, typename VF>
+__device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                                          const T* __restrict__ Q, T* __restrict__ O,
+                                          float* __restrict__ LSE, int n, int h, int lane,
+                                          KF kd_row, VF vd_row) {
   constexpr int EPL = D / 32;
-  if (read_status(pp.hdr) != 0) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (wid >= P.NQ * P.Hq) return;
-  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
   const int g = h / P.group;
-  const int j = n / P.B;
   const RowGeom G = row_geom(P, pp, n, h);
   const int x0 = lane * EPL;
   const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
@@ -146,10 +156,7 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
     {
       float kv[KT][EPL];
 #pragma unroll
-      for (int u = 0; u < KT; ++u) {
-        const int t = min(t0 + u, P.B - 1);
-        ld_vec<T, EPL>(Kd + ((size_t)(j * P.B + t) * P.Hkv + g) * D + x0, kv[u]);
-      }
+      for (int u = 0; u < KT; ++u) kd_row(min(t0 + u, P.B - 1), kv[u]);
 #pragma unroll
       for (int u = 0; u < KT; ++u) {
         float part = 0.f;
@@ -178,8 +185,7 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
     // keys past B repeat the last key's values with weight 0
     float vv[KT][EPL];
 #pragma unroll
-    for (int u = 0; u < KT; ++u)
-      ld_vec<T, EPL>(Vd + ((size_t)(j * P.B + min(t0 + u, P.B - 1)) * P.Hkv + g) * D + x0, vv[u]);
+    for (int u = 0; u < KT; ++u) vd_row(min(t0 + u, P.B - 1), vv[u]);
 #pragma unroll
     for (int u = 0; u < KT; ++u) {
       const float pu = __shfl_sync(0xffffffffu, pm, 2 * u);
@@ -241,6 +247,58 @@ __global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, Work
   for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wd, od[i], acc[i]);
   st_vec<T, EPL>(O + ((size_t)n * P.Hq + h) * D + x0, acc);
   if (lane == 0) LSE[(size_t)h * P.NQ + n] = M + logf(Ls);
+}
+
+// One warp per (query n, head h), draft keys and values read from global
+// memory (any B).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                    const T* __restrict__ Q,
+                                                    const T* __restrict__ Kd,
+                                                    const T* __restrict__ Vd,
+                                                    T* __restrict__ O, float* __restrict__ LSE) {
+  constexpr int EPL = D / 32;
+  if (read_status(pp.hdr) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= P.NQ * P.Hq) return;
+  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
+  const size_t kv0 = ((size_t)(n / P.B) * P.B * P.Hkv + h / P.group) * D + lane * EPL;
+  const size_t kvs = (size_t)P.Hkv * D;  // between draft rows
+  merge_row<T, D>(P, pp, wk, Q, O, LSE, n, h, lane,
+                  [&](int t, float (&v)[EPL]) { ld_vec<T, EPL>(Kd + kv0 + t * kvs, v); },
+                  [&](int t, float (&v)[EPL]) { ld_vec<T, EPL>(Vd + kv0 + t * kvs, v); });
+}
+
+// One CTA per (draft block j, kv head g) for B <= kDraftBM: the block's draft
+// keys and values are staged in shared memory once, and the eight warps
+// merge the block's B * group rows in turn.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_block_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+                                                          const T* __restrict__ Q,
+                                                          const T* __restrict__ Kd,
+                                                          const T* __restrict__ Vd,
+                                                          T* __restrict__ O,
+                                                          float* __restrict__ LSE) {
+  constexpr int EPL = D / 32;
+  extern __shared__ float sm[];
+  float* kd_s = sm;                   // [B][D]
+  float* vd_s = kd_s + kDraftBM * D;  // [B][D]
+  if (read_status(pp.hdr) != 0) return;
+  const int B = P.B, Gs = P.group, R = B * Gs;
+  const int j = blockIdx.x, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < B * D; i += blockDim.x) {
+    const size_t o = ((size_t)(j * B + i / D) * P.Hkv + g) * D + i % D;
+    kd_s[i] = ld_f(Kd + o);
+    vd_s[i] = ld_f(Vd + o);
+  }
+  __syncthreads();
+  const int x0 = lane * EPL;
+  for (int r = warp; r < R; r += 8)
+    merge_row<T, D>(P, pp, wk, Q, O, LSE, j * B + r / Gs, g * Gs + r % Gs, lane,
+                    [&](int t, float (&v)[EPL]) { lds_vec<EPL>(kd_s + t * D + x0, v); },
+                    [&](int t, float (&v)[EPL]) { lds_vec<EPL>(vd_s + t * D + x0, v); });
 }
 
 // Backward prologue, one warp per (query n, head h):
@@ -389,21 +447,6 @@ __global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp,
 // sum_t dS_t kd_t (fp32, unscaled); then one thread per (head dim, key
 // group) sums dVd[t] = sum_r P_t(r) dO_r and dKd[t] = scale * sum_r dS_t(r)
 // q_r over the rows in fixed order.
-constexpr int kDraftBM = 32, kDraftRM = 64;
-
-// EPL consecutive floats of shared memory (16- or 8-byte aligned) in one load.
-template <int EPL>
-__device__ __forceinline__ void lds_vec(const float* p, float (&v)[EPL]) {
-  if constexpr (EPL == 4) {
-    const float4 t = *(const float4*)p;
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  } else {
-    static_assert(EPL == 2, "head dim 64 or 128");
-    const float2 t = *(const float2*)p;
-    v[0] = t.x; v[1] = t.y;
-  }
-}
-
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                               const T* __restrict__ Q,
@@ -626,8 +669,14 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
     constexpr int D = decltype(dtag)::value;
     const int64_t warps = P.NQ * P.Hq;
     if (warps == 0) return cudaSuccess;
-    merge_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
-        P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (T*)O, LSE);
+    if (P.B <= kDraftBM) {
+      const size_t smem = sizeof(float) * 2 * kDraftBM * D;
+      merge_block_kernel<T, D><<<dim3((unsigned)P.NA, (unsigned)P.Hkv), 256, smem, st>>>(
+          P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (T*)O, LSE);
+    } else {
+      merge_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+          P, pp, wk, (const T*)Q, (const T*)Kd, (const T*)Vd, (T*)O, LSE);
+    }
     return cudaGetLastError();
   });
 }
