@@ -20,6 +20,13 @@ What it computes, and the passages it follows:
 * ``attention.partial_forward`` / ``attention.merge``: attention restricted to
   a key subset, plus the log-sum-exp merge of such partials. Used only to
   check that any split merges back to ``forward`` (the exactness property).
+* ``projection``: the drafter layer's input projections (Q, K, V of the
+  draft tokens and K, V of the context through one stacked weight) and
+  output projection around the attention, forward and backward, as plain
+  float64 matrix products; ``layer_forward`` / ``layer_backward`` compose
+  them with ``attention``. The pages name the layer (diffusion drafters whose
+  draft blocks cross-attend to the target's context) but not its
+  projections; the plain linear maps are the reading taken.
 * ``plan``: the realized-attention cost of a KV chunk and the
   longest-processing-time-first assignment (sort by cost, most expensive
   first; give each to the least-loaded worker) that the abstract and the
@@ -31,4 +38,4 @@ is pinned by mathematics instead: brute force on tiny inputs, a library
 special case, finite differences, closed forms, invariants and Graham's
 bound (see ``tests/test_oracle_*.py``).
 """
-from . import attention, plan  # noqa: F401
+from . import attention, plan, projection  # noqa: F401

@@ -255,6 +255,38 @@ def tensors(w: Workload, seed_offset: int = 1, dtype=np.float32,
     return out
 
 
+def default_hidden(w: Workload) -> int:
+    """Model width of the drafter layer around the attention: Hq * d (the
+    pages give none; this is the usual width of an attention layer whose
+    heads tile the model dimension, e.g. 32 x 128 = 4096)."""
+    return w.Hq * w.d
+
+
+def layer_tensors(w: Workload, hidden: Optional[int] = None, seed_offset: int = 7,
+                  dtype=np.float32) -> dict:
+    """Inputs of the drafter layer's projections, from their own PCG64 stream.
+
+    Xd [N_q, hidden] and Xc [T, hidden] (hidden states of the draft tokens and
+    of the context) and dY [N_q, hidden] (upstream gradient of the layer
+    output) are N(0,1); the stacked input weight Wqkv [(Hq + 2 Hkv) d, hidden]
+    is N(0, 1/hidden) and the output weight Wo [hidden, Hq d] N(0, 1/(Hq d)),
+    so that the projected Q, K, V and the output have unit variance like the
+    attention's own N(0,1) draws.
+    """
+    H = default_hidden(w) if hidden is None else int(hidden)
+    rng = _rng(w.seed + seed_offset * 1_000_003)
+    nq, T = w.n_q, w.total_ctx
+    rows = (w.Hq + 2 * w.Hkv) * w.d
+    return {
+        "Xd": rng.standard_normal((nq, H), dtype=dtype),
+        "Xc": rng.standard_normal((T, H), dtype=dtype),
+        "Wqkv": (rng.standard_normal((rows, H), dtype=dtype) / np.float32(math.sqrt(H))),
+        "Wo": (rng.standard_normal((H, w.Hq * w.d), dtype=dtype) /
+               np.float32(math.sqrt(w.Hq * w.d))),
+        "dY": rng.standard_normal((nq, H), dtype=dtype),
+    }
+
+
 def subset(w: Workload, n_heads: int, n_anchors: int, seed: int) -> tuple:
     """Seeded subset (query heads, global block indices) for spot checks."""
     rng = _rng(seed)
