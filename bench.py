@@ -547,6 +547,114 @@ def run_study(args, d):
     return 0
 
 
+def proj_flop(w, H):
+    """FLOP of the drafter layer's projections (2 per multiply-add)."""
+    nq, T = w.n_q, w.total_ctx
+    qd, kd = w.Hq * w.d, w.Hkv * w.d
+    in_fwd = 2 * nq * H * (qd + 2 * kd) + 2 * T * H * 2 * kd
+    out_fwd = 2 * nq * H * qd
+    return {"in_fwd": in_fwd, "in_bwd": 2 * in_fwd, "out_fwd": out_fwd, "out_bwd": 2 * out_fwd}
+
+
+def run_projection_study(args, d):
+    """The drafter layer's projections (splitkv_proj_*) at configs 1 and 2
+    with hidden = Hq d: each call's device time and TFLOP/s against the
+    measured burst bf16 peak, the same products through torch.matmul
+    (cuBLAS) for context, and the whole layer step (projections + plan +
+    attention forward and backward)."""
+    import torch
+    import block_sparse_cross_gb300 as S
+    if d.rank != 0:
+        return 0
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    n = max(3, min(args.steps, 20))
+    for cfg in (1, 2):
+        w = W.config(cfg)
+        H = W.default_hidden(w)
+        kv, keep, fwd, bwd = _setup(w, dev, 0, S, torch)
+        t = W.layer_tensors(w, H)
+        x = {k: torch.from_numpy(v).to(dev).to(torch.bfloat16) for k, v in t.items()}
+        del t
+        nq, T = w.n_q, w.total_ctx
+        qd, kd = w.Hq * w.d, w.Hkv * w.d
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        gpu, outs, _ = keep
+        a = {k: gpu[k] for k in ("Q", "Kc", "Vc", "Kd", "Vd")}
+        O, LSE = outs["O"], outs["LSE"]
+        Y = torch.empty(nq, H, **bf)
+        dO = torch.empty(nq, w.Hq, w.d, **bf)
+        g = {k: torch.empty_like(v) for k, v in a.items()}
+        dXd = torch.empty(nq, H, **bf)
+        dXc = torch.empty(T, H, **bf)
+        dW = torch.empty(qd + 2 * kd, H, device=dev)
+        dWo = torch.empty(H, qd, device=dev)
+        calls = {
+            "in_fwd": lambda: kv.proj_in_forward(H, x["Xd"], x["Xc"], x["Wqkv"], a["Q"], a["Kc"],
+                                                 a["Vc"], a["Kd"], a["Vd"]),
+            "out_fwd": lambda: kv.proj_out_forward(H, O, x["Wo"], Y),
+            "out_bwd": lambda: kv.proj_out_backward(H, O, x["Wo"], x["dY"], dO, dWo),
+            "in_bwd": lambda: kv.proj_in_backward(H, x["Xd"], x["Xc"], x["Wqkv"], g["Q"], g["Kc"],
+                                                  g["Vc"], g["Kd"], g["Vd"], dXd, dXc, dW),
+        }
+        fl = proj_flop(w, H)
+        line = {"study": "projection", "workload": workload_desc(w), "hidden": H, "steps": n,
+                "peak": peak, "peak_source": f"bf16_tflops (burst) of {src}",
+                "l2": "context hidden states and their gradient are larger than L2; "
+                      "the draft-side operands stay L2-resident between calls"}
+        for name, fn in calls.items():
+            S.splitkv_profile_enable(True)
+            ms = _event_ms(fn, n, torch)
+            S.splitkv_profile_enable(False)
+            _, kt = S.splitkv_profile_read()
+            tf = fl[name] / (ms * 1e-3) / 1e12
+            line[name] = {"ms": ms, "tflops": tf, "frac": tf / peak,
+                          "launches_per_call": kt["projection"][0] / (n + 3)}
+        st, ds = S.splitkv_proj_status(clear=True)
+        if st != S.SPLITKV_OK or ds != S.SPLITKV_OK:
+            raise RuntimeError("projection status " + S.splitkv_status_string(ds))
+        # the same products through torch.matmul (cuBLAS), operands pre-packed
+        Wkv = x["Wqkv"][qd:]
+        gq = torch.randn(nq, qd + 2 * kd, **bf)
+        gc = torch.randn(T, 2 * kd, **bf)
+        Of = O.reshape(nq, qd)
+        cub = {
+            "in_fwd": lambda: (x["Xd"] @ x["Wqkv"].t(), x["Xc"] @ Wkv.t()),
+            "out_fwd": lambda: Of @ x["Wo"].t(),
+            "out_bwd": lambda: (x["dY"] @ x["Wo"], x["dY"].t() @ Of),
+            "in_bwd": lambda: (gq @ x["Wqkv"], gc @ Wkv, gq.t() @ x["Xd"], gc.t() @ x["Xc"]),
+        }
+        line["cublas"] = {}
+        for name, fn in cub.items():
+            ms = _event_ms(fn, n, torch)
+            line["cublas"][name] = {"ms": ms, "tflops": fl[name] / (ms * 1e-3) / 1e12}
+        del gq, gc
+
+        def layer():
+            calls["in_fwd"]()
+            kv.plan()
+            kv.forward(a["Q"], a["Kc"], a["Vc"], a["Kd"], a["Vd"], O, LSE)
+            calls["out_fwd"]()
+            calls["out_bwd"]()
+            kv.backward(a["Q"], a["Kc"], a["Vc"], a["Kd"], a["Vd"], O, LSE, dO, g["Q"], g["Kc"],
+                        g["Vc"], g["Kd"], g["Vd"])
+            calls["in_bwd"]()
+        ms = _event_ms(layer, n, torch)
+        if kv.device_status() != S.SPLITKV_OK:
+            raise RuntimeError(S.splitkv_status_string(kv.device_status()))
+        attn = w.useful_flop(14)
+        proj = sum(fl.values())
+        line["layer"] = {"ms": ms, "useful_tflop": (attn + proj) / 1e12,
+                         "attention_tflop": attn / 1e12, "projection_tflop": proj / 1e12,
+                         "tflops": (attn + proj) / (ms * 1e-3) / 1e12}
+        print(json.dumps(line), flush=True)
+        del kv, keep, gpu, outs, x, a, g
+        torch.cuda.empty_cache()
+    return 0
+
+
 def busy_imbalance(kv, S):
     """Measured load balance of the latest launch of each persistent attention
     kernel: per-CTA busy time (end - start %globaltimer) max / mean - 1."""
@@ -575,15 +683,19 @@ def main():
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--contiguous", action="store_true",
                     help="contiguous item assignment instead of LPT")
-    ap.add_argument("--study", choices=("balance", "planner"),
+    ap.add_argument("--study", choices=("balance", "planner", "projection"),
                     help="balance: step time with LPT vs contiguous plans (configs 3, 4); "
-                         "planner: plan time vs item count next to the forward (configs 1-4)")
+                         "planner: plan time vs item count next to the forward (configs 1-4); "
+                         "projection: the drafter layer's projection GEMMs and the whole "
+                         "layer step (configs 1, 2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     d = Dist()
     try:
-        if args.study:
+        if args.study == "projection":
+            rc = run_projection_study(args, d)
+        elif args.study:
             rc = run_study(args, d)
         else:
             rc = run_reference(args, d) if args.impl == "reference" else run_ours(args, d)

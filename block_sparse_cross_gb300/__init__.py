@@ -44,10 +44,10 @@ SPLITKV_FLAG_CUDA_CORE = 1
 SPLITKV_FLAG_CONTIGUOUS = 2
 SPLITKV_FLAG_MASK_INCLUSIVE = 4
 SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
-SPLITKV_NUM_KERNELS = 8
+SPLITKV_NUM_KERNELS = 9
 SPLITKV_NOALLOC_SCRATCH_BYTES = 64 << 20
 (SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,
- SPLITKV_K_BWD_DKDV, SPLITKV_K_DQ_REDUCE, SPLITKV_K_ZERO) = range(8)
+ SPLITKV_K_BWD_DKDV, SPLITKV_K_DQ_REDUCE, SPLITKV_K_ZERO, SPLITKV_K_PROJ) = range(9)
 
 
 class splitkv_problem(ctypes.Structure):
@@ -118,6 +118,11 @@ _SIGS = {
     "splitkv_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
     "splitkv_busy_read": ([_P, _vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                            _vp], ctypes.c_int),
+    "splitkv_proj_in_fwd": ([_P, ctypes.c_int] + [_vp] * 8 + [_vp], ctypes.c_int),
+    "splitkv_proj_in_bwd": ([_P, ctypes.c_int] + [_vp] * 11 + [_vp], ctypes.c_int),
+    "splitkv_proj_out_fwd": ([_P, ctypes.c_int, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "splitkv_proj_out_bwd": ([_P, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "splitkv_proj_status": ([ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -260,6 +265,37 @@ def splitkv_plan_export(prob, plan_ws, kind: int, capacity: int, stream=None):
     return st, ids[:n], costs[:n], worker[:n], pos[:n]
 
 
+def splitkv_proj_in_fwd(prob, hidden: int, Xd, Xc, Wqkv, Q, Kc, Vc, Kd, Vd, stream=None) -> int:
+    return _lib.splitkv_proj_in_fwd(ctypes.byref(prob), int(hidden), _ptr(Xd), _ptr(Xc),
+                                    _ptr(Wqkv), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(Kd), _ptr(Vd),
+                                    _stream(stream))
+
+
+def splitkv_proj_in_bwd(prob, hidden: int, Xd, Xc, Wqkv, dQ, dKc, dVc, dKd, dVd, dXd, dXc,
+                        dWqkv, stream=None) -> int:
+    return _lib.splitkv_proj_in_bwd(ctypes.byref(prob), int(hidden), _ptr(Xd), _ptr(Xc),
+                                    _ptr(Wqkv), _ptr(dQ), _ptr(dKc), _ptr(dVc), _ptr(dKd),
+                                    _ptr(dVd), _ptr(dXd), _ptr(dXc), _ptr(dWqkv),
+                                    _stream(stream))
+
+
+def splitkv_proj_out_fwd(prob, hidden: int, O, Wo, Y, stream=None) -> int:
+    return _lib.splitkv_proj_out_fwd(ctypes.byref(prob), int(hidden), _ptr(O), _ptr(Wo), _ptr(Y),
+                                     _stream(stream))
+
+
+def splitkv_proj_out_bwd(prob, hidden: int, O, Wo, dY, dO, dWo, stream=None) -> int:
+    return _lib.splitkv_proj_out_bwd(ctypes.byref(prob), int(hidden), _ptr(O), _ptr(Wo),
+                                     _ptr(dY), _ptr(dO), _ptr(dWo), _stream(stream))
+
+
+def splitkv_proj_status(clear: bool = False, stream=None):
+    """Returns (status, device status of the projection kernels)."""
+    s = ctypes.c_int(0)
+    st = _lib.splitkv_proj_status(ctypes.byref(s), 1 if clear else 0, _stream(stream))
+    return st, s.value
+
+
 # ---- convenience wrapper over torch tensors --------------------------------
 class SplitKV:
     """One problem (metadata resident on the device) plus its workspaces.
@@ -317,6 +353,25 @@ class SplitKV:
         st, w = splitkv_busy_read(self.prob, self.plan_ws, kernel_id, ns, self._stream())
         _check("splitkv_busy_read", st)
         return ns[:2 * w].reshape(w, 2)
+
+    # ---- projections of the drafter layer (splitkv_proj_*) ----
+    def proj_in_forward(self, hidden: int, Xd, Xc, Wqkv, Q, Kc, Vc, Kd, Vd) -> None:
+        _check("splitkv_proj_in_fwd", splitkv_proj_in_fwd(self.prob, hidden, Xd, Xc, Wqkv, Q, Kc,
+                                                          Vc, Kd, Vd, self._stream()))
+
+    def proj_in_backward(self, hidden: int, Xd, Xc, Wqkv, dQ, dKc, dVc, dKd, dVd, dXd, dXc,
+                         dWqkv) -> None:
+        _check("splitkv_proj_in_bwd", splitkv_proj_in_bwd(self.prob, hidden, Xd, Xc, Wqkv, dQ, dKc,
+                                                          dVc, dKd, dVd, dXd, dXc, dWqkv,
+                                                          self._stream()))
+
+    def proj_out_forward(self, hidden: int, O, Wo, Y) -> None:
+        _check("splitkv_proj_out_fwd", splitkv_proj_out_fwd(self.prob, hidden, O, Wo, Y,
+                                                            self._stream()))
+
+    def proj_out_backward(self, hidden: int, O, Wo, dY, dO, dWo) -> None:
+        _check("splitkv_proj_out_bwd", splitkv_proj_out_bwd(self.prob, hidden, O, Wo, dY, dO, dWo,
+                                                            self._stream()))
 
     def device_status(self) -> int:
         st, s = splitkv_device_status(self.prob, self.plan_ws, self._stream())

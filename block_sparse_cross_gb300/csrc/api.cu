@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -209,6 +210,61 @@ cudaError_t timed(int kernel, int launches, cudaStream_t st, F&& f) {
   return e;
 }
 
+// ---- projections ------------------------------------------------------------
+int check_proj(const splitkv_problem* p, int hidden) {
+  const int st = check_problem(p);
+  if (st) return st;
+  if (hidden <= 0) return SPLITKV_EINVAL;
+  if (p->dtype != SPLITKV_BF16 || hidden % 64 || hidden >= (1 << 24)) return SPLITKV_EUNSUPPORTED;
+  return SPLITKV_OK;
+}
+
+bool all_aligned(std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return false;
+  return true;
+}
+
+// One-segment product C = A B with the given operand forms.
+ProjSpec proj_one(int64_t M, int64_t N, int a_mn, int b_mn, ProjOperand a, ProjOperand b,
+                  int64_t b_off, int64_t klen, int out_f32) {
+  ProjSpec s;
+  memset(&s, 0, sizeof(s));
+  s.M = M;
+  s.N = N;
+  s.a_mn = a_mn;
+  s.b_mn = b_mn;
+  s.b_off = b_off;
+  s.nseg = 1;
+  s.a[0] = a;
+  s.b[0] = b;
+  s.klen[0] = klen;
+  s.ksplit = 1;
+  s.out_f32 = out_f32;
+  return s;
+}
+
+void add_seg(ProjSpec* s, ProjOperand a, ProjOperand b, int64_t k0_b, int64_t klen) {
+  const int j = s->nseg++;
+  s->a[j] = a;
+  s->b[j] = b;
+  s->k0_b[j] = k0_b;
+  s->klen[j] = klen;
+}
+
+void add_dst(ProjSpec* s, void* ptr, int col0, int ncols, int64_t ld) {
+  ProjDst& d = s->dst[s->ndst++];
+  d.ptr = ptr;
+  d.col0 = col0;
+  d.ncols = ncols;
+  d.ld = ld;
+}
+
+int run_proj(const ProjSpec* parts, int n, cudaStream_t s) {
+  if (n == 0) return SPLITKV_OK;
+  return cuda_status(timed(SPLITKV_K_PROJ, 1, s, [&] { return launch_proj(parts, n, s); }));
+}
+
 }  // namespace
 
 extern "C" {
@@ -263,7 +319,7 @@ int splitkv_busy_read(const splitkv_problem* prob, const void* plan_ws, int kern
 const char* splitkv_kernel_name(int kernel_id) {
   static const char* names[SPLITKV_NUM_KERNELS] = {
       "plan", "fwd_attention", "merge", "bwd_draft", "bwd_dq", "bwd_dkdv", "dq_reduce",
-      "zero_uncovered"};
+      "zero_uncovered", "projection"};
   return (kernel_id >= 0 && kernel_id < SPLITKV_NUM_KERNELS) ? names[kernel_id] : "unknown";
 }
 
@@ -467,6 +523,139 @@ int splitkv_plan_export(const splitkv_problem* prob, const void* plan_ws, int ki
     }
   }
   return SPLITKV_OK;
+}
+
+int splitkv_proj_in_fwd(const splitkv_problem* prob, int hidden, const void* Xd, const void* Xc,
+                        const void* Wqkv, void* Q, void* Kc, void* Vc, void* Kd, void* Vd,
+                        splitkv_stream stream) {
+  int st = check_proj(prob, hidden);
+  if (st) return st;
+  const int64_t NQ = prob->total_anchors * prob->B, T = prob->total_ctx, H = hidden;
+  const int qd = prob->Hq * prob->d, kd = prob->Hkv * prob->d;
+  const bool draft = NQ > 0, ctx = T > 0 && Xc;
+  if (!Wqkv || (draft && (!Xd || !Q || !Kd || !Vd)) || (ctx && (!Kc || !Vc)))
+    return SPLITKV_EINVAL;
+  if (!all_aligned({Xd, Xc, Wqkv, Q, Kc, Vc, Kd, Vd})) return SPLITKV_EINVAL;
+  const ProjOperand W{Wqkv, qd + 2 * kd, H};
+  ProjSpec parts[2];
+  int n = 0;
+  if (draft) {  // [Q | Kd | Vd] = Xd Wqkv^T
+    ProjSpec& p = parts[n++];
+    p = proj_one(NQ, qd + 2 * kd, 0, 0, {Xd, NQ, H}, W, 0, H, 0);
+    add_dst(&p, Q, 0, qd, qd);
+    add_dst(&p, Kd, qd, kd, kd);
+    add_dst(&p, Vd, qd + kd, kd, kd);
+  }
+  if (ctx) {  // [Kc | Vc] = Xc Wkv^T: rows [qd, qd + 2 kd) of Wqkv
+    ProjSpec& p = parts[n++];
+    p = proj_one(T, 2 * kd, 0, 0, {Xc, T, H}, W, qd, H, 0);
+    add_dst(&p, Kc, 0, kd, kd);
+    add_dst(&p, Vc, kd, kd, kd);
+  }
+  return run_proj(parts, n, (cudaStream_t)stream);
+}
+
+int splitkv_proj_in_bwd(const splitkv_problem* prob, int hidden, const void* Xd, const void* Xc,
+                        const void* Wqkv, const void* dQ, const void* dKc, const void* dVc,
+                        const void* dKd, const void* dVd, void* dXd, void* dXc, float* dWqkv,
+                        splitkv_stream stream) {
+  int st = check_proj(prob, hidden);
+  if (st) return st;
+  const int64_t NQ = prob->total_anchors * prob->B, T = prob->total_ctx, H = hidden;
+  const int qd = prob->Hq * prob->d, kd = prob->Hkv * prob->d;
+  const bool draft = NQ > 0, ctx = T > 0 && Xc;
+  if (!Wqkv || !dWqkv || (draft && (!Xd || !dQ || !dKd || !dVd || !dXd)) ||
+      (ctx && (!dKc || !dVc || !dXc)))
+    return SPLITKV_EINVAL;
+  if (!all_aligned({Xd, Xc, Wqkv, dQ, dKc, dVc, dKd, dVd, dXd, dXc, dWqkv})) return SPLITKV_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  const ProjOperand W{Wqkv, qd + 2 * kd, H};  // read MN-major: [out rows = K][hidden = N]
+  // activation gradients (bf16)
+  ProjSpec parts[3];
+  int n = 0;
+  if (draft) {  // dXd = dQ Wq + dKd Wk + dVd Wv
+    ProjSpec& p = parts[n++];
+    p = proj_one(NQ, H, 0, 1, {dQ, NQ, qd}, W, 0, qd, 0);
+    add_seg(&p, {dKd, NQ, kd}, W, qd, kd);
+    add_seg(&p, {dVd, NQ, kd}, W, qd + kd, kd);
+    add_dst(&p, dXd, 0, (int)H, H);
+  }
+  if (ctx) {  // dXc = dKc Wk + dVc Wv
+    ProjSpec& p = parts[n++];
+    p = proj_one(T, H, 0, 1, {dKc, T, kd}, W, 0, kd, 0);
+    p.k0_b[0] = qd;
+    add_seg(&p, {dVc, T, kd}, W, qd + kd, kd);
+    add_dst(&p, dXc, 0, (int)H, H);
+  }
+  if ((st = run_proj(parts, n, s))) return st;
+  // weight gradients (fp32): rows of dWqkv = (dY_part)^T X, summed over the
+  // draft rows and then the context rows
+  const int64_t kb_ctx = ctx ? (T + 63) / 64 : 0, kb_d = (NQ + 63) / 64;
+  const int ksplit = (int)std::min<int64_t>(64, std::max<int64_t>(1, (kb_d + kb_ctx) / 128));
+  if (ksplit > 1 || !draft) {  // atomics add into it, or dWq has no terms
+    if (cudaMemsetAsync(dWqkv, 0, sizeof(float) * (size_t)(qd + 2 * kd) * H, s) != cudaSuccess)
+      return SPLITKV_ECUDA;
+  }
+  n = 0;
+  if (draft) {  // dWq = dQ^T Xd
+    ProjSpec& p = parts[n++];
+    p = proj_one(qd, H, 1, 1, {dQ, NQ, qd}, {Xd, NQ, H}, 0, NQ, 1);
+    add_dst(&p, dWqkv, 0, (int)H, H);
+  }
+  for (int kv = 0; kv < 2 && (draft || ctx); ++kv) {  // dWk, dWv
+    ProjSpec& p = parts[n++];
+    memset(&p, 0, sizeof(p));
+    p.M = kd;
+    p.N = H;
+    p.a_mn = p.b_mn = 1;
+    p.out_f32 = 1;
+    p.ksplit = ksplit;
+    if (draft) add_seg(&p, {kv ? dVd : dKd, NQ, kd}, {Xd, NQ, H}, 0, NQ);
+    if (ctx) add_seg(&p, {kv ? dVc : dKc, T, kd}, {Xc, T, H}, 0, T);
+    add_dst(&p, dWqkv + (size_t)(qd + kv * kd) * H, 0, (int)H, H);
+  }
+  return run_proj(parts, n, s);
+}
+
+int splitkv_proj_out_fwd(const splitkv_problem* prob, int hidden, const void* O, const void* Wo,
+                         void* Y, splitkv_stream stream) {
+  int st = check_proj(prob, hidden);
+  if (st) return st;
+  const int64_t NQ = prob->total_anchors * prob->B, H = hidden;
+  const int qd = prob->Hq * prob->d;
+  if (NQ > 0 && (!O || !Wo || !Y)) return SPLITKV_EINVAL;
+  if (!all_aligned({O, Wo, Y})) return SPLITKV_EINVAL;
+  if (NQ == 0) return SPLITKV_OK;
+  ProjSpec p = proj_one(NQ, H, 0, 0, {O, NQ, qd}, {Wo, H, qd}, 0, qd, 0);
+  add_dst(&p, Y, 0, (int)H, H);
+  return run_proj(&p, 1, (cudaStream_t)stream);
+}
+
+int splitkv_proj_out_bwd(const splitkv_problem* prob, int hidden, const void* O, const void* Wo,
+                         const void* dY, void* dO, float* dWo, splitkv_stream stream) {
+  int st = check_proj(prob, hidden);
+  if (st) return st;
+  const int64_t NQ = prob->total_anchors * prob->B, H = hidden;
+  const int qd = prob->Hq * prob->d;
+  if (!dWo || (NQ > 0 && (!O || !Wo || !dY || !dO))) return SPLITKV_EINVAL;
+  if (!all_aligned({O, Wo, dY, dO, dWo})) return SPLITKV_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (NQ == 0)
+    return cuda_status(cudaMemsetAsync(dWo, 0, sizeof(float) * (size_t)H * qd, s));
+  ProjSpec parts[2];
+  // dO = dY Wo: Wo read MN-major ([hidden rows = K][Hq d = N])
+  parts[0] = proj_one(NQ, qd, 0, 1, {dY, NQ, H}, {Wo, H, qd}, 0, H, 0);
+  add_dst(&parts[0], dO, 0, qd, qd);
+  // dWo = dY^T O: both MN-major ([N_q rows = K])
+  parts[1] = proj_one(H, qd, 1, 1, {dY, NQ, H}, {O, NQ, qd}, 0, NQ, 1);
+  add_dst(&parts[1], dWo, 0, qd, qd);
+  return run_proj(parts, 2, s);
+}
+
+int splitkv_proj_status(int* status, int clear, splitkv_stream stream) {
+  if (!status) return SPLITKV_EINVAL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
+  return cuda_status(proj_status(status, clear != 0));
 }
 
 const char* splitkv_status_string(int status) {

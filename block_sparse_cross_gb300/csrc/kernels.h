@@ -43,4 +43,59 @@ cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,
                                   cudaStream_t st);
 
+// proj.cu — grouped tcgen05 GEMM of the drafter layer's projections.
+constexpr int kProjMaxParts = 3, kProjMaxSegs = 3, kProjMaxDst = 3;
+
+// Columns [col0, col0 + ncols) of a product go to ptr[row * ld + (c - col0)].
+struct ProjDst {
+  void* ptr;
+  int col0, ncols;
+  int64_t ld;
+};
+
+// A row-major [rows][cols] bf16 tensor read by one segment.
+struct ProjOperand {
+  const void* ptr;
+  int64_t rows, cols;
+};
+
+// One product C[M, N] = sum over segments s of A_s B_s (host description).
+//   K-major A: a[s] is [M rows][K cols]; MN-major A: [K rows][M cols];
+//   likewise B with N. The part's first row of C is row a_off of A's M
+//   extent and its first column is b_off of B's N extent; segment s covers
+//   K coordinates [k0_a[s], k0_a[s] + klen[s]) of a[s] and [k0_b[s], ...) of
+//   b[s]. A segment whose K range ends inside its tensor must have
+//   klen % 64 == 0 (the last k block is padded with the tensor's zero fill).
+//   ksplit > 1 splits K into that many slices added with fp32 atomics
+//   (out_f32 only; the output must be zeroed first).
+struct ProjSpec {
+  int64_t M, N;
+  int a_mn, b_mn;
+  int64_t a_off, b_off;
+  int nseg;
+  ProjOperand a[kProjMaxSegs], b[kProjMaxSegs];
+  int64_t k0_a[kProjMaxSegs], k0_b[kProjMaxSegs], klen[kProjMaxSegs];
+  int ksplit, out_f32, ndst;
+  ProjDst dst[kProjMaxDst];
+};
+
+// Device form of a part (built by launch_proj).
+struct ProjSeg {
+  int kb0, a_k, b_k;
+};
+struct ProjPart {
+  int M, N, mt, nt, a_mn, b_mn, a_off, b_off, nseg, nkb, ksplit, kb_per_split, unit0, out_f32,
+      ndst;
+  ProjSeg seg[kProjMaxSegs];
+  ProjDst dst[kProjMaxDst];
+};
+struct ProjGroup {
+  int nparts, units;
+  ProjPart part[kProjMaxParts];
+};
+
+cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st);
+// Reads (and optionally clears) the projections' device status word.
+cudaError_t proj_status(int* status, bool clear);
+
 }  // namespace skv

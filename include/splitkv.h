@@ -312,7 +312,8 @@ enum {
   SPLITKV_K_BWD_DKDV = 5,    /* dK/dV of 128-key tiles (persistent) */
   SPLITKV_K_DQ_REDUCE = 6,   /* dQ = scale * sum of partials */
   SPLITKV_K_ZERO = 7,        /* zero dK/dV rows no block sees */
-  SPLITKV_NUM_KERNELS = 8
+  SPLITKV_K_PROJ = 8,        /* projection GEMMs (splitkv_proj_*) */
+  SPLITKV_NUM_KERNELS = 9
 };
 int splitkv_profile_enable(int on);
 int splitkv_profile_read(int32_t* launches, double* total_ms, int n);
@@ -335,6 +336,61 @@ int splitkv_profile_read(int32_t* launches, double* total_ms, int n);
  */
 int splitkv_busy_read(const splitkv_problem* prob, const void* plan_ws, int kernel_id,
                       uint64_t* ns, int capacity, int* workers, splitkv_stream stream);
+/*
+ * Projections of the drafter layer around the attention (the fused
+ * projection epilogue). The pages name the layer the attention sits in — a
+ * diffusion drafter whose draft blocks cross-attend to the target model's
+ * context (Split-KV abstract; rit.work article, section on when the method
+ * changes the infrastructure plan) — but give no projections. Reading taken:
+ * the bias-free linear maps of an attention layer, weights in a linear
+ * layer's [out, in] row-major layout, the context keys/values projected by
+ * the same Wk, Wv as the draft tokens:
+ *     [Q | Kd | Vd] = Xd Wqkv^T      Xd   [N_q, hidden]  draft-token hidden states
+ *     [Kc | Vc]     = Xc Wkv^T       Xc   [T, hidden]    context hidden states
+ *     Y             = O Wo^T         Wqkv [(Hq + 2 Hkv) d, hidden] = [Wq; Wk; Wv]
+ *                                    Wkv  = rows [Hq d, (Hq + 2 Hkv) d) of Wqkv
+ *                                    Wo   [hidden, Hq d];   Y, dY [N_q, hidden]
+ * Q, Kd, Vd, Kc, Vc, O have the layouts of splitkv_fwd ([rows, heads, d] is
+ * [rows, heads * d]). Every product is a tcgen05 GEMM (bf16 in, fp32
+ * accumulate) whose epilogue writes those layouts directly: one launch over
+ * Wqkv produces Q, Kd and Vd (and Kc, Vc), and the backward sums the three
+ * terms dQ Wq + dKd Wk + dVd Wv of dXd in one accumulator.
+ * Requirements: the problem passes splitkv_plan's checks (no plan is needed),
+ * prob->dtype == SPLITKV_BF16, hidden a positive multiple of 64, all
+ * pointers 16-byte aligned. Activations and their gradients are bf16; the
+ * weight gradients dWqkv, dWo are fp32 and are overwritten (not accumulated
+ * into). dWk, dWv sum over N_q + T rows; when T is large that sum is split
+ * into slices added with fp32 atomics, so the last bits of dWqkv's k/v rows
+ * can differ between runs; every other output is deterministic.
+ * Errors: EINVAL (null or misaligned pointer, hidden <= 0), EUNSUPPORTED
+ * (dtype, hidden % 64, the problem's shape), ECUDA. A device pipeline wait
+ * that times out stops the kernel and is reported by splitkv_proj_status.
+ */
+/* Forward of the input projections. Xc may be NULL: the context projection
+ * is skipped and Kc, Vc (then allowed NULL) are left untouched. */
+int splitkv_proj_in_fwd(const splitkv_problem* prob, int hidden, const void* Xd, const void* Xc,
+                        const void* Wqkv, void* Q, void* Kc, void* Vc, void* Kd, void* Vd,
+                        splitkv_stream stream);
+/* Backward of the input projections: dXd = dQ Wq + dKd Wk + dVd Wv,
+ * dXc = dKc Wk + dVc Wv, dWqkv = [dQ^T Xd; dKd^T Xd + dKc^T Xc; dVd^T Xd + dVc^T Xc]
+ * (fp32). With Xc NULL the context terms are left out (dXc, dKc, dVc may be
+ * NULL). */
+int splitkv_proj_in_bwd(const splitkv_problem* prob, int hidden, const void* Xd, const void* Xc,
+                        const void* Wqkv, const void* dQ, const void* dKc, const void* dVc,
+                        const void* dKd, const void* dVd, void* dXd, void* dXc, float* dWqkv,
+                        splitkv_stream stream);
+/* Forward of the output projection: Y = O Wo^T. */
+int splitkv_proj_out_fwd(const splitkv_problem* prob, int hidden, const void* O, const void* Wo,
+                         void* Y, splitkv_stream stream);
+/* Backward of the output projection: dO = dY Wo (bf16, the input of
+ * splitkv_bwd), dWo = dY^T O (fp32). One launch. */
+int splitkv_proj_out_bwd(const splitkv_problem* prob, int hidden, const void* O, const void* Wo,
+                         const void* dY, void* dO, float* dWo, splitkv_stream stream);
+/* SYNCHRONISES `stream`; *status = the first device error of any projection
+ * launch in this process (SPLITKV_OK or SPLITKV_ETIMEOUT); clear != 0 resets
+ * it. Errors: EINVAL, ECUDA. */
+int splitkv_proj_status(int* status, int clear, splitkv_stream stream);
+
 /* Name of a kernel family id (never NULL). */
 const char* splitkv_kernel_name(int kernel_id);
 

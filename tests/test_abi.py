@@ -86,3 +86,27 @@ def test_busy_read_validates_on_the_host():
     assert S._lib.splitkv_busy_read(ctypes.byref(make_problem(d=96, num_workers=16)), dummy,
                                     S.SPLITKV_K_FWD_ATTN, buf, 64, ctypes.byref(w),
                                     None) == S.SPLITKV_EUNSUPPORTED
+
+
+def test_projection_entry_points_validate_on_the_host():
+    # every call below returns before any CUDA runtime call
+    p = make_problem()
+    dummy = 1 << 20           # 16-byte aligned, never dereferenced
+    odd = (1 << 20) + 8
+    u, inval = S.SPLITKV_EUNSUPPORTED, S.SPLITKV_EINVAL
+    assert S.splitkv_proj_out_fwd(p, 100, dummy, dummy, dummy) == u       # hidden % 64
+    assert S.splitkv_proj_out_fwd(p, 0, dummy, dummy, dummy) == inval     # hidden <= 0
+    assert S.splitkv_proj_out_fwd(make_problem(dtype=S.SPLITKV_FP32), 128, dummy, dummy,
+                                  dummy) == u
+    assert S.splitkv_proj_out_fwd(p, 128, odd, dummy, dummy) == inval      # misaligned
+    assert S.splitkv_proj_out_fwd(p, 128, None, dummy, dummy) == inval
+    assert S.splitkv_proj_out_bwd(p, 128, dummy, dummy, dummy, dummy, None) == inval
+    assert S.splitkv_proj_in_fwd(p, 128, dummy, dummy, None, dummy, dummy, dummy, dummy,
+                                 dummy) == inval                           # no weight
+    assert S.splitkv_proj_in_fwd(p, 128, dummy, dummy, dummy, dummy, None, dummy, dummy,
+                                 dummy) == inval                           # Xc given, no Kc
+    assert S.splitkv_proj_in_bwd(p, 128, dummy, dummy, dummy, dummy, dummy, dummy, dummy,
+                                 dummy, dummy, dummy, None) == inval       # no dWqkv
+    assert S.splitkv_proj_in_bwd(make_problem(d=96), 128, *([dummy] * 11)) == u
+    assert S._lib.splitkv_proj_status(None, 0, None) == inval
+    assert S.splitkv_kernel_name(S.SPLITKV_K_PROJ) == "projection"
