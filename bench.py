@@ -384,27 +384,95 @@ def run_ours(args, d: Dist):
     plan_ms = kernels.get("plan", {}).get("ms_total", 0.0) / args.steps
 
     # ---- end to end through the public API with host buffers ----
-    e2e = None
+    # Every step copies its inputs from pinned host memory and its outputs
+    # back. Pipelined (the `e2e` key): two device buffer sets; step i's inputs
+    # are copied on an H2D stream while step i-1 computes, and its outputs on
+    # a D2H stream while step i+1 computes, each copy ordered against the
+    # compute that last used its buffer set by CUDA events. Serial
+    # (`e2e_serial`): copy in, compute, copy out on one stream.
+    e2e = e2e_serial = None
     if not args.no_e2e:
         h2d = sum(v.numel() * v.element_size() for v in pinned.values()) + \
             sum(m.numel() * m.element_size() for m in meta_host)
         d2h = sum(v.numel() * v.element_size() for v in outs.values())
-        d.barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
+        # each buffer set has its own metadata copy and its own problem handle
+        # (plan and work workspaces), so a copy never writes what a running
+        # step reads
+        meta2 = [torch.empty_like(m) for m in meta]
+        kv2 = S.SplitKV(*meta2, w.total_ctx, w.total_anchors, w.max_ctx, w.B, w.Hq, w.Hkv, w.d,
+                        w.chunk, w.scale, flags=flags)
+        sets = [(gpu, outs, meta, kv),
+                ({k: torch.empty_like(v) for k, v in gpu.items()},
+                 {k: torch.empty_like(v) for k, v in outs.items()}, meta2, kv2)]
+
+        def step_on(g, o, kvb):
+            kvb.plan()
+            kvb.forward(g["Q"], g["Kc"], g["Vc"], g["Kd"], g["Vd"], o["O"], o["LSE"])
+            kvb.backward(g["Q"], g["Kc"], g["Vc"], g["Kd"], g["Vd"], o["O"], o["LSE"],
+                         g["dO"], o["dQ"], o["dKc"], o["dVc"], o["dKd"], o["dVd"])
+
+        def copy_in(g, m):
             for k in names_in:
-                gpu[k].copy_(pinned[k], non_blocking=True)
-            for m, mh in zip(meta, meta_host):
-                m.copy_(mh, non_blocking=True)
-            step()
-            for k in outs:
-                out_host[k].copy_(outs[k], non_blocking=True)
-        torch.cuda.synchronize()
-        t_e2e = d.max(time.perf_counter() - t0)
-        e2e = {"value": d.sum(flop_step) * args.steps / t_e2e / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": 1e3 * t_e2e / args.steps}
+                g[k].copy_(pinned[k], non_blocking=True)
+            for dm, mh in zip(m, meta_host):
+                dm.copy_(mh, non_blocking=True)
+
+        def copy_out(o):
+            for k in o:
+                out_host[k].copy_(o[k], non_blocking=True)
+
+        def run_pipelined(steps):
+            comp = torch.cuda.current_stream()
+            s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+            done = [None, None]    # compute that last read / wrote set b
+            copied = [None, None]  # D2H that last read set b's outputs
+            for i in range(steps):
+                b = i % 2
+                g, o, m, kvb = sets[b]
+                with torch.cuda.stream(s_in):
+                    if done[b] is not None:
+                        s_in.wait_event(done[b])
+                    copy_in(g, m)
+                    ready = torch.cuda.Event()
+                    ready.record(s_in)
+                comp.wait_event(ready)
+                if copied[b] is not None:
+                    comp.wait_event(copied[b])
+                step_on(g, o, kvb)
+                done[b] = torch.cuda.Event()
+                done[b].record(comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[b])
+                    copy_out(o)
+                    copied[b] = torch.cuda.Event()
+                    copied[b].record(s_out)
+            torch.cuda.synchronize()
+
+        def run_serial(steps):
+            for _ in range(steps):
+                copy_in(gpu, meta)
+                step_on(gpu, outs, kv)
+                copy_out(outs)
+            torch.cuda.synchronize()
+
+        res = {}
+        for name, fn in (("pipelined", run_pipelined), ("serial", run_serial)):
+            fn(2)  # warm-up (streams, events)
+            d.barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn(args.steps)
+            t = d.max(time.perf_counter() - t0)
+            res[name] = {"value": d.sum(flop_step) * args.steps / t / 1e12, "unit": UNIT,
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                         "ms_per_step": 1e3 * t / args.steps}
+        e2e = dict(res["pipelined"], overlap="two device buffer sets; step i's kernels overlap "
+                   "the H2D copy of step i+1 and the D2H copy of step i-1 (own streams)")
+        e2e_serial = res["serial"]
+        for kvb in (kv, kv2):
+            if kvb.device_status() != S.SPLITKV_OK:
+                raise RuntimeError("device status " + S.splitkv_status_string(kvb.device_status()))
+        del sets, kv2, meta2
 
     # ---- CPU oracle baseline (rank 0, N = 1), and the errors of the GPU
     # outputs against it on the same sampled rows ----
@@ -446,6 +514,7 @@ def run_ours(args, d: Dist):
             "gpu_launches": launches_total,
             "clocks": clocks,
             "e2e": e2e,
+            "e2e_serial": e2e_serial,
             "cpu_baseline": cpu,
             "oracle_errors": errors,
         }
@@ -571,7 +640,7 @@ def run_projection_study(args, d):
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
     n = max(3, min(args.steps, 20))
-    for cfg in (1, 2):
+    for cfg in [int(c) for c in args.proj_configs.split(",")]:
         w = W.config(cfg)
         H = W.default_hidden(w)
         kv, keep, fwd, bwd = _setup(w, dev, 0, S, torch)
@@ -688,6 +757,8 @@ def main():
                          "planner: plan time vs item count next to the forward (configs 1-4); "
                          "projection: the drafter layer's projection GEMMs and the whole "
                          "layer step (configs 1, 2)")
+    ap.add_argument("--proj-configs", default="1,2",
+                    help="configs of --study projection (comma-separated)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
