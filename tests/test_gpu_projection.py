@@ -194,3 +194,38 @@ def test_whole_layer_matches_oracle(w, hidden):
     for k, t in (("dXd", dXd), ("dXc", dXc), ("dWqkv", dW), ("dWo", dWo)):
         err = rel_l2(_np(t), ref[k])
         assert err < 1e-2, (k, err)
+
+
+def test_no_draft_queries_and_no_context():
+    """Problems without anchors (only the context projection and its
+    gradients; dWq and dWo are zero) and calls without context hidden states."""
+    w = W.custom(34, lengths=[2000], prompts=[100], counts=[0], B=16, Hq=32, Hkv=8, d=128,
+                 chunk=1024)
+    assert w.n_q == 0
+    L = Layer(w, 192)
+    d = L.dev
+    L.kv.proj_in_forward(L.H, None, d["Xc"], d["Wqkv"], None, L.Kc, L.Vc, None, None)
+    T = w.total_ctx
+    rng = np.random.Generator(np.random.PCG64(79))
+    g32 = {k: W.round_to_bf16(rng.standard_normal((T, w.Hkv, w.d), dtype=np.float32))
+           for k in ("dKc", "dVc")}
+    dXc = torch.empty(T, L.H, dtype=torch.bfloat16, device="cuda")
+    dW = torch.full(((w.Hq + 2 * w.Hkv) * w.d, L.H), float("nan"), device="cuda")
+    L.kv.proj_in_backward(L.H, None, d["Xc"], d["Wqkv"], None, _bf16(g32["dKc"]),
+                          _bf16(g32["dVc"]), None, None, None, dXc, dW)
+    dWo = torch.full((L.H, w.Hq * w.d), float("nan"), device="cuda")
+    L.kv.proj_out_backward(L.H, None, d["Wo"], None, None, dWo)
+    torch.cuda.synchronize()
+    _check_status()
+    h = L.host
+    qd, kd = w.Hq * w.d, w.Hkv * w.d
+    Wk, Wv = h["Wqkv"][qd:qd + kd], h["Wqkv"][qd + kd:]
+    assert rel_l2(_np(L.Kc).reshape(T, -1), h["Xc"] @ Wk.T) < BF16_REL
+    assert rel_l2(_np(L.Vc).reshape(T, -1), h["Xc"] @ Wv.T) < BF16_REL
+    gk, gv = g32["dKc"].reshape(T, -1).astype(np.float64), g32["dVc"].reshape(T, -1).astype(np.float64)
+    assert rel_l2(_np(dXc), gk @ Wk + gv @ Wv) < BF16_REL
+    got = _np(dW)
+    assert (got[:qd] == 0).all()
+    assert rel_l2(got[qd:qd + kd], gk.T @ h["Xc"]) < F32_REL
+    assert rel_l2(got[qd + kd:], gv.T @ h["Xc"]) < F32_REL
+    assert (_np(dWo) == 0).all()
