@@ -363,8 +363,11 @@ def run_ours(args, d: Dist):
     for name, (launches, tot) in ktimes.items():
         if launches == 0:
             continue
-        per_launch = tot / launches if name != "plan" else tot / (launches / 3)
-        entry = {"launches": launches, "ms_total": tot, "ms_per_launch": per_launch}
+        # the planner and the draft-block prologue are several launches per
+        # call: their figure per step is the one to compare
+        per_launch = tot / launches
+        entry = {"launches": launches, "ms_total": tot, "ms_per_launch": per_launch,
+                 "ms_per_step": tot / args.steps}
         if name in KERNEL_FLOP_PER_PAIR_DIM:
             f = KERNEL_FLOP_PER_PAIR_DIM[name] * w.d * w.Hq * cp
             entry["tflops"] = f / (per_launch * 1e-3) / 1e12

@@ -401,7 +401,7 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   WorkPtrs wk;
   work_layout(c.caps.NCF * prob->Hkv, c.P.NQ, prob->Hq, prob->d, prob->B,
               c.caps.NSL * prob->Hkv, (char*)work, &wk);
-  e = timed(SPLITKV_K_BWD_DRAFT, 1, s, [&] {
+  e = timed(SPLITKV_K_BWD_DRAFT, bwd_draft_launches(c.P, c.caps.NSL), s, [&] {
     return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, c.caps.NSL, s);
   });
   if (e != cudaSuccess) return SPLITKV_ECUDA;

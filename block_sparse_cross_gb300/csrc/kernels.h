@@ -38,6 +38,8 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
                              const void* Q, const void* Kd, const void* Vd, const void* O,
                              const float* LSE, const void* dO, void* dKd, void* dVd,
                              int64_t nsl_cap, cudaStream_t st);
+// Kernel launches launch_bwd_draft makes for this problem.
+int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap);
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
                              cudaStream_t st);
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,

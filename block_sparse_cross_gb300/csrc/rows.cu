@@ -681,6 +681,12 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
   });
 }
 
+int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap) {
+  if (P.NQ * P.Hq == 0) return 0;
+  const bool fused = P.B <= kDraftBM && P.B * P.group <= kDraftRM;
+  return (fused ? 1 : 2) + (nsl_cap > 0 ? 1 : 0);
+}
+
 cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                              const void* Q, const void* Kd, const void* Vd, const void* O,
                              const float* LSE, const void* dO, void* dKd, void* dVd,
