@@ -108,6 +108,15 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def aggregate(d: "Dist", flop_step: float, steps: int, ms_local: float):
+    """Whole-job throughput of a weak-scaling run: every rank times its own
+    `steps` steps (ms_local per step); the job's step time is the slowest
+    rank's, and the value is the FLOP all ranks did over that time.
+    Returns (TFLOP/s, ms per step)."""
+    ms = d.max(ms_local)
+    return d.sum(flop_step) * steps / (ms * steps * 1e-3) / 1e12, ms
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled during the timed region."""
 
@@ -348,12 +357,10 @@ def run_ours(args, d: Dist):
     clocks = sampler.stop()
     d.barrier()
     ms_local = e0.elapsed_time(e1) / args.steps
-    ms = d.max(ms_local)
+    flop_step = w.useful_flop(14)
+    value, ms = aggregate(d, flop_step, args.steps, ms_local)
     pst, ktimes = S.splitkv_profile_read()
     busy = busy_imbalance(kv, S)
-
-    flop_step = w.useful_flop(14)
-    value = d.sum(flop_step) * args.steps / (ms * args.steps * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
 
