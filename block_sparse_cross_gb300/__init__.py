@@ -123,6 +123,7 @@ _SIGS = {
     "splitkv_proj_out_fwd": ([_P, ctypes.c_int, _vp, _vp, _vp, _vp], ctypes.c_int),
     "splitkv_proj_out_bwd": ([_P, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "splitkv_proj_status": ([ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp], ctypes.c_int),
+    "splitkv_selftest_wait_timeout": ([ctypes.POINTER(ctypes.c_int), _vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -293,6 +294,14 @@ def splitkv_proj_status(clear: bool = False, stream=None):
     """Returns (status, device status of the projection kernels)."""
     s = ctypes.c_int(0)
     st = _lib.splitkv_proj_status(ctypes.byref(s), 1 if clear else 0, _stream(stream))
+    return st, s.value
+
+
+def splitkv_selftest_wait_timeout(stream=None):
+    """Returns (status, what the probe kernel reported): SPLITKV_ETIMEOUT
+    when its unsatisfiable bounded wait gave up as designed."""
+    s = ctypes.c_int(-1)
+    st = _lib.splitkv_selftest_wait_timeout(ctypes.byref(s), _stream(stream))
     return st, s.value
 
 

@@ -658,6 +658,11 @@ int splitkv_proj_status(int* status, int clear, splitkv_stream stream) {
   return cuda_status(proj_status(status, clear != 0));
 }
 
+int splitkv_selftest_wait_timeout(int* status, splitkv_stream stream) {
+  if (!status) return SPLITKV_EINVAL;
+  return cuda_status(run_wait_probe(status, (cudaStream_t)stream));
+}
+
 const char* splitkv_status_string(int status) {
   switch (status) {
     case SPLITKV_OK: return "ok";

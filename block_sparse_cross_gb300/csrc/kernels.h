@@ -97,6 +97,10 @@ struct ProjGroup {
 };
 
 cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st);
+
+// selftest.cu — a wait that nothing satisfies; *status = what the kernel
+// reported (SPLITKV_ETIMEOUT when the bounded wait gave up). Synchronises st.
+cudaError_t run_wait_probe(int* status, cudaStream_t st);
 // Reads (and optionally clears) the projections' device status word.
 cudaError_t proj_status(int* status, bool clear);
 

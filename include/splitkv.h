@@ -391,6 +391,18 @@ int splitkv_proj_out_bwd(const splitkv_problem* prob, int hidden, const void* O,
  * it. Errors: EINVAL, ECUDA. */
 int splitkv_proj_status(int* status, int clear, splitkv_stream stream);
 
+/*
+ * splitkv_selftest_wait_timeout — diagnostic of the device-side failure path.
+ *   SYNCHRONISES `stream`. Runs one small kernel whose mbarrier wait nothing
+ *   can satisfy, with the same bounded-wait routine every pipeline uses: the
+ *   wait gives up after its limit (about 1 s), raises the CTA's abort flag
+ *   (a second waiting warp stops on it) and the kernel reports the outcome;
+ *   *status = SPLITKV_ETIMEOUT when that happened, SPLITKV_OK if the wait
+ *   returned without timing out. The context stays usable.
+ * Errors: EINVAL (null status), ECUDA.
+ */
+int splitkv_selftest_wait_timeout(int* status, splitkv_stream stream);
+
 /* Name of a kernel family id (never NULL). */
 const char* splitkv_kernel_name(int kernel_id);
 

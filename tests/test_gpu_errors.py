@@ -7,8 +7,9 @@ import pytest
 import torch
 
 import block_sparse_cross_gb300 as S
+import oracle.attention as OA
 import workloads as W
-from gpu_case import Case
+from gpu_case import TOL, Case, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -71,3 +72,22 @@ def test_workspace_too_small_and_null_pointers():
                          case.LSE, kv.work, kv.work_bytes) == S.SPLITKV_EINVAL
     assert S.splitkv_fwd(kv.prob, kv.plan_ws, d["Q"].data_ptr() + 2, d["Kc"], d["Vc"], d["Kd"],
                          d["Vd"], case.O, case.LSE, kv.work, kv.work_bytes) == S.SPLITKV_EINVAL
+
+
+@pytest.mark.gpu
+def test_bounded_wait_times_out_and_the_context_survives():
+    """A wait that nothing satisfies gives up after its limit and reports
+    SPLITKV_ETIMEOUT (no trap, no hang); the same process then runs the
+    whole path correctly."""
+    import time
+    t0 = time.perf_counter()
+    st, s = S.splitkv_selftest_wait_timeout()
+    dt = time.perf_counter() - t0
+    assert st == S.SPLITKV_OK
+    assert s == S.SPLITKV_ETIMEOUT
+    assert 0.5 < dt < 30.0
+    c = Case(W.config(0)).plan().forward()
+    torch.cuda.synchronize()
+    assert c.kv.device_status() == S.SPLITKV_OK
+    O, LSE = OA.forward(c.w, c.host["Q"], c.host["Kc"], c.host["Vc"], c.host["Kd"], c.host["Vd"])
+    assert rel_l2(c.O.float().cpu().numpy(), O) < TOL["O_rel"]
