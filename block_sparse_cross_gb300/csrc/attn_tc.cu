@@ -49,25 +49,46 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 100000000ull;
 
-struct FwdItem {
-  int n0, g, row0, cs, ntiles, first, nblk;
-  size_t slot;
-};
+using FwdItem = FwdRec;
 
-__device__ __forceinline__ FwdItem fwd_item(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
-  FwdItem I;
-  I.first = pp.sl_first[e.slab];
-  I.nblk = pp.sl_nblk[e.slab];
-  const int c0 = P.cu_ctx[e.s], L = P.cu_ctx[e.s + 1] - c0;
-  const int amax = P.anchors[I.first + I.nblk - 1];
-  I.cs = e.c * P.chunk;
-  const int ke = min(min(I.cs + P.chunk, L), amax);
-  I.ntiles = (ke - I.cs + kKeyTile - 1) / kKeyTile;
-  I.row0 = c0 + I.cs;
-  I.n0 = I.first * P.B;
-  I.g = e.g;
-  I.slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
-  return I;
+// The planner's decoded record of queue position p (read-only here). The
+// loads are volatile asm so that they stay where they are written: every
+// role issues the next item's record load when the current item starts and
+// uses it one item later, off the item boundary's critical path.
+__device__ __forceinline__ FwdRec ld_rec(const FwdRec* p) {
+  FwdRec R;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(R.n0), "=r"(R.g), "=r"(R.row0), "=r"(R.cs)
+               : "l"(p));
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4 + 16];"
+               : "=r"(R.ntiles), "=r"(R.first), "=r"(R.nblk), "=r"(R.slot)
+               : "l"(p));
+  return R;
+}
+__device__ __forceinline__ int ld_int_early(const int* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_float_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// Row r of an item (as row_info), with the anchor load issued now.
+__device__ __forceinline__ RowInfo row_info_early(const ProbDev& P, const FwdRec& I, int r) {
+  RowInfo ri;
+  const int per_blk = P.B * P.group;
+  const int b = r / per_blk;
+  if (b >= I.nblk) {
+    ri.n = -1; ri.h = 0; ri.anchor = 0;
+    return ri;
+  }
+  ri.n = (I.first + b) * P.B + (r / P.group) % P.B;
+  ri.h = I.g * P.group + r % P.group;
+  ri.anchor = ld_int_early(P.anchors + I.first + b);
+  return ri;
 }
 
 // TMEM column of the packed bf16 A operand (P, dS, P^T, dS^T) for k step kk
@@ -100,8 +121,8 @@ template <int D>
 struct FwdLayout {
   static constexpr int kSub = D / 64;
   static constexpr uint32_t tile = kSub * kSubBytes;  // one 128 x D bf16 tile
-  static constexpr uint32_t q = 0;
-  static constexpr uint32_t k0 = tile;
+  static constexpr uint32_t q = 0;  // two Q tiles: item i uses i % 2
+  static constexpr uint32_t k0 = 2 * tile;
   static constexpr uint32_t v0 = k0 + kFwdNK * tile;
   static constexpr uint32_t lm = v0 + kFwdNV * tile;  // [4][128] floats: l_0, l_1, m_0, m_1
   static constexpr uint32_t bars = lm + 2048;
@@ -120,11 +141,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Tile t (counted over the CTA's items) uses index b = t % 2. S of tile t
   // is issued once both PV halves of tile t-2 are done (sfree); PV half h of
   // tile t once that half's P is written (p_ready[b][h]). The K stage is
-  // free when S is done (s_full), the V stage when PV is done (sfree).
+  // free when S is done (s_full), the V stage when PV is done (sfree). Item
+  // i's Q is in buffer i % 2, so the next item's Q lands while this item's
+  // last tiles run.
   static_assert(kFwdNK == 2 && kFwdNV == 2, "ring sizes tied to the S buffers");
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;          // [2]
+  uint64_t* q_full = bars + 0;          // [2]
+  uint64_t* q_empty = bars + 2;         // [2] the item's last S is done
+  uint64_t* k_full = bars + 4;          // [2]
   uint64_t* v_full = k_full + 2;        // [2]
   uint64_t* s_full = v_full + 2;        // [2] S of tile t is in buffer t % 2
   uint64_t* p_ready = s_full + 2;       // [2][2] P of half h written over its S half
@@ -139,9 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) stamp_busy(P, pp, 0, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(q_full + b, 1);
+      mbar_init(q_empty + b, 1);
       mbar_init(k_full + b, 1);
       mbar_init(v_full + b, 1);
       mbar_init(s_full + b, 1);
@@ -175,13 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       uint32_t nq = 0, nk = 0;
       bool ok = true;
+      FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-        if (nq > 0 && !(ok = warp_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
+        const FwdItem I = In;
+        if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
+        const uint32_t qb = nq & 1;
+        // buffer qb is free once the last S of item nq - 2 is done
+        if (nq >= 2 && !(ok = warp_wait(q_empty + qb, ((nq >> 1) - 1) & 1, abort_flag))) break;
         if (elect_one()) {
-          mbar_expect_tx(q_full, Lay::tile);
+          mbar_expect_tx(q_full + qb, Lay::tile);
           for (int i = 0; i < kSub; ++i)
-            tma_load_3d(smem + Lay::q + i * kSubBytes, &tmQ, q_full, 64 * i, I.g * P.group, I.n0);
+            tma_load_3d(smem + Lay::q + qb * Lay::tile + i * kSubBytes, &tmQ, q_full + qb, 64 * i,
+                        I.g * P.group, I.n0);
         }
         __syncwarp();
         ++nq;
@@ -200,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {  // let every copy in flight land before the CTA exits
-        if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, kDrainNs);
+        for (uint32_t j = nq > 2u ? nq - 2 : 0; j < nq; ++j)
+          mbar_wait_drain(q_full + (j & 1), (j >> 1) & 1, kDrainNs);
         for (uint32_t j = nk > (uint32_t)kFwdNK ? nk - kFwdNK : 0; j < nk; ++j)
           mbar_wait_drain(k_full + j % kFwdNK, (j / kFwdNK) & 1, kDrainNs);
       }
@@ -212,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
+      FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        const FwdItem I = In;
+        if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nv % kFwdNV, u = nv / kFwdNV;
           // stage s is free once both PV halves of tile nv - 2 are done
@@ -239,12 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S and PV are issued by two warps: while one waits on its commit the
     // other keeps the tensor pipe fed.
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-    const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q));
     uint32_t ns = 0, nit = 0;
     bool ok = true;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
-      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
+      const uint32_t qb = nit & 1;
+      if (!(ok = warp_wait(q_full + qb, (nit >> 1) & 1, abort_flag))) break;
+      const uint64_t qd0 = desc_kmajor0(smem_u32(smem + Lay::q + qb * Lay::tile));
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
         const uint32_t b = ns & 1;
         if (!(ok = warp_wait(k_full + b, (ns >> 1) & 1, abort_flag))) break;
@@ -257,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tS + b * 128, qd0 + (kmajor_off(kk) >> 4), kd0 + (kmajor_off(kk) >> 4), kIdS,
                    kk > 0 ? 1u : 0u);
           mma_commit(s_full + b);  // also frees K stage b
-          if (t == I.ntiles - 1) mma_commit(q_empty);
+          if (t == I.ntiles - 1) mma_commit(q_empty + qb);
         }
         __syncwarp();
       }
@@ -270,8 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
     uint32_t np = 0, nit = 0;
     bool ok = true;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
       for (int t = 0; t < I.ntiles && ok; ++t, ++np) {
         const uint32_t b = np & 1;
         if (!(ok = warp_wait(v_full + b, (np >> 1) & 1, abort_flag))) break;
@@ -307,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     uint32_t ns = 0, nit = 0;
     bool ok = true;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
       ns += I.ntiles;
       const uint32_t pt = ns - 1;  // the item's last tile
       if (!(ok = warp_wait(lm_ready, nit & 1, abort_flag))) break;
@@ -321,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = lm[r] * w0 + lm[128 + r] * w1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float f0 = w0 * inv, f1 = w1 * inv;
-      float* po = wk.part_o + (I.slot * kRows + r) * D;
+      float* po = wk.part_o + ((size_t)I.slot * kRows + r) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {  // 32 columns of each half at a time (register budget)
         uint32_t v0[32], v1[32];
@@ -343,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_global_v8(po + 32 * c + i, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
         }
       }
-      wk.part_lse[I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+      wk.part_lse[(size_t)I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
     }
   } else {
     // ---------------- softmax (warps 2..9) ----------------
@@ -358,17 +396,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tOh = tO + hf * D + lane_base;
     uint32_t ns = 0;
     bool ok = true;
-    // The next item's record and row are loaded before this item ends, so
-    // their dependent global loads overlap its last tile.
+    // The next item's record is loaded when an item starts and the row's
+    // anchor once its first tile is done, so neither load is waited for at
+    // the item boundary.
     FwdItem In{};
     RowInfo rin{};
     if (q0 < q1) {
-      In = fwd_item(P, pp, pp.f_queue[q0]);
-      rin = row_info(P, In.first, In.nblk, In.g, r);
+      In = ld_rec(pp.f_rec + q0);
+      rin = row_info_early(P, In, r);
     }
     for (int qi = q0, nit = 0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = In;
       const RowInfo ri = rin;
+      bool row_next = qi + 1 >= q1;  // the next item's row is loaded (or not needed)
+      if (!row_next) In = ld_rec(pp.f_rec + qi + 1);
       float m_run = -INFINITY, l = 0.f;
       for (int t = 0; t < I.ntiles; ++t, ++ns) {
         const uint32_t sb = ns & 1;
@@ -455,12 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_ready + 2 * sb + hf);
+        if (!row_next) {
+          rin = row_info_early(P, In, r);
+          row_next = true;
+        }
       }
       if (!ok) break;
-      if (qi + 1 < q1) {
-        In = fwd_item(P, pp, pp.f_queue[qi + 1]);
-        rin = row_info(P, In.first, In.nblk, In.g, r);
-      }
       // hand (m, l) of this half to the epilogue once it has read the previous item's
       if (nit > 0 && !(ok = warp_wait(o_free, (nit - 1) & 1, abort_flag))) break;
       lm[hf * 128 + r] = l;
@@ -600,8 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       uint32_t nq = 0, nk = 0;
       bool ok = true;
+      FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        const FwdItem I = In;
+        if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
         if (nq > 0 && !(ok = warp_wait(q_empty, (nq - 1) & 1, abort_flag))) break;
         if (elect_one()) {
           mbar_expect_tx(q_full, 2 * Lay::tile);
@@ -637,8 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       uint32_t nv = 0;
       bool ok = true;
+      FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+        const FwdItem I = In;
+        if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
         for (int t = 0; t < I.ntiles; ++t) {
           const uint32_t s = nv % kDqNV, u = nv / kDqNV;
           if (u > 0 && !(ok = warp_wait(dp_full + s, (u - 1) & 1, abort_flag))) break;
@@ -664,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
     uint32_t gt = 0, nit = 0;  // gt: tiles issued (K and V ring index)
     bool ok = true;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
       if (!(ok = warp_wait(qt_ready, nit & 1, abort_flag))) break;
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         const uint32_t ks = gt % kDqNK, vs = gt % kDqNV, b = gt & 1;
@@ -703,8 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
     uint32_t gt = 0, nit = 0;
     bool ok = true;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         const uint32_t b = gt & 1;
         if (!(ok = warp_wait(p_ready + b, (gt >> 1) & 1, abort_flag))) break;
@@ -741,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto write_dq = [&](const FwdItem& I, uint32_t it) -> bool {
       if (!warp_wait(dq_done, it & 1, abort_flag)) return false;
       tc_fence_after();
-      float* po = wk.part_o + (I.slot * kRows + r) * D;
+      float* po = wk.part_o + ((size_t)I.slot * kRows + r) * D;
 #pragma unroll 1
       for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
         uint32_t v[64];
@@ -762,8 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     FwdItem Iprev{};
     uint32_t nit = 0;
+    FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const FwdItem I = fwd_item(P, pp, pp.f_queue[qi]);
+      const FwdItem I = In;
+      if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
       if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
       if (nit > 0 && !(ok = warp_wait(qt_empty, (nit - 1) & 1, abort_flag))) break;
       tc_fence_after();
@@ -798,20 +849,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = P.scale_log2;
     uint32_t gt = 0, nit = 0;
     bool ok = true;
-    // The next item's record, row and row statistics are loaded before this
-    // item's last tile ends, so their dependent global loads overlap it.
+    // The next item's record, row and row statistics are loaded after this
+    // item's last tile (two dependent loads: the decoded record, then the
+    // row's anchor, LSE and D; keeping them across the tiles would cost the
+    // registers this role does not have).
     FwdItem In{};
     RowInfo rin{};
     float nl2n = -INFINITY, Drn = 0.f;
     auto load_next = [&](int qn) {
-      In = fwd_item(P, pp, pp.f_queue[qn]);
-      rin = row_info(P, In.first, In.nblk, In.g, r);
+      In = ld_rec(pp.f_rec + qn);
+      rin = row_info_early(P, In, r);
       // padding rows: -inf exponent offset makes their P exactly 0
       nl2n = -INFINITY;
       Drn = 0.f;
       if (rin.n >= 0) {
-        nl2n = -LSE[(size_t)rin.h * P.NQ + rin.n] * kLog2e;
-        Drn = wk.dvec[(size_t)rin.h * P.NQ + rin.n];
+        nl2n = -ld_float_early(LSE + (size_t)rin.h * P.NQ + rin.n) * kLog2e;
+        Drn = ld_float_early(wk.dvec + (size_t)rin.h * P.NQ + rin.n);
       }
     };
     if (q0 < q1) load_next(q0);
@@ -912,26 +965,17 @@ struct KvLayout {
   static constexpr uint32_t total = bars + 512 + 1024;
 };
 
-struct KvItem {
-  int s, g, c0, L, ks0, sl_lo, sl_hi;
-};
+using KvItem = BwdRec;
 
-__device__ __forceinline__ KvItem kv_item(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
-  KvItem I;
-  I.s = e.s;
-  I.g = e.g;
-  I.c0 = P.cu_ctx[e.s];
-  I.L = P.cu_ctx[e.s + 1] - I.c0;
-  I.ks0 = e.c * kKeyTile;
-  const int sl0 = pp.s_slab_off[e.s], sl1 = pp.s_slab_off[e.s + 1];
-  int lo = sl0, hi = sl1;
-  while (lo < hi) {  // first slab whose last anchor exceeds the tile start
-    const int mid = (lo + hi) >> 1;
-    if (P.anchors[pp.sl_first[mid] + pp.sl_nblk[mid] - 1] > I.ks0) hi = mid; else lo = mid + 1;
-  }
-  I.sl_lo = lo;
-  I.sl_hi = sl1;
-  return I;
+__device__ __forceinline__ BwdRec ld_brec(const BwdRec* p) {
+  BwdRec R;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(R.s), "=r"(R.g), "=r"(R.c0), "=r"(R.L)
+               : "l"(p));
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4 + 16];"
+               : "=r"(R.ks0), "=r"(R.sl_lo), "=r"(R.sl_hi), "=r"(R.pad)
+               : "l"(p));
+  return R;
 }
 
 template <int D>
@@ -1002,8 +1046,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
       tma_prefetch_desc(&tmV);
       uint32_t nkv = 0, nst = 0;
       bool ok = true;
+      KvItem In = q0 < q1 ? ld_brec(pp.b_rec + q0) : KvItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+        const KvItem I = In;
+        if (qi + 1 < q1) In = ld_brec(pp.b_rec + qi + 1);  // lands during this item
         if (nkv > 0 && !(ok = warp_wait(kv_empty, (nkv - 1) & 1, abort_flag))) break;
         if (elect_one()) {
           mbar_expect_tx(kv_full, 2 * kSub * kSubBytes);
@@ -1043,8 +1089,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
       tma_prefetch_desc(&tmdO);
       uint32_t nst = 0;
       bool ok = true;
+      KvItem In = q0 < q1 ? ld_brec(pp.b_rec + q0) : KvItem{};
       for (int qi = q0; qi < q1 && ok; ++qi) {
-        const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+        const KvItem I = In;
+        if (qi + 1 < q1) In = ld_brec(pp.b_rec + qi + 1);  // lands during this item
         for (int sg = I.sl_lo; sg < I.sl_hi; ++sg) {
           const uint32_t s = nst % kNS, u = nst / kNS;
           if (u > 0 && !(ok = warp_wait(st_empty + s, (u - 1) & 1, abort_flag))) break;
@@ -1090,8 +1138,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     };
     uint32_t nst = 0, nit = 0;
     bool ok = true;
+    KvItem In = q0 < q1 ? ld_brec(pp.b_rec + q0) : KvItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+      const KvItem I = In;
+      if (qi + 1 < q1) In = ld_brec(pp.b_rec + qi + 1);  // lands during this item
       if (!(ok = warp_wait(kv_full, nit & 1, abort_flag))) break;
       if (!(ok = warp_wait(st_full + nst % kNS, (nst / kNS) & 1, abort_flag))) break;
       tc_fence_after();
@@ -1155,8 +1205,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     const float sl2 = P.scale_log2;
     uint32_t nst = 0, nit = 0;
     bool ok = true;
+    KvItem In = q0 < q1 ? ld_brec(pp.b_rec + q0) : KvItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
-      const KvItem I = kv_item(P, pp, pp.b_queue[qi]);
+      const KvItem I = In;
+      if (qi + 1 < q1) In = ld_brec(pp.b_rec + qi + 1);  // lands during this item
       const int key = I.ks0 + r;
       for (int sg = I.sl_lo; sg < I.sl_hi; ++sg, ++nst) {
         const uint32_t s = nst % kNS;

@@ -49,6 +49,27 @@ struct __align__(16) QEntry {
   int32_t s, c, slab, g;
 };
 
+// A forward / dQ queue entry decoded once by the planner, so that a kernel
+// role reads an item with one 32-byte load instead of chasing the slab and
+// anchor tables at every item boundary.
+//   n0      first query row of the slab      g      kv head
+//   row0    first context row of the chunk   cs     chunk start (sample-local)
+//   ntiles  128-key tiles below the slab's last visible key
+//   first   first draft block of the slab    nblk   blocks in the slab
+//   slot    partial slot of (slab, chunk, kv head)
+struct __align__(16) FwdRec {
+  int32_t n0, g, row0, cs, ntiles, first, nblk, slot;
+};
+
+// A dK/dV queue entry decoded once by the planner:
+//   s, g     sample, kv head          c0, L   first context row, length of s
+//   ks0      the key tile's first key (sample-local)
+//   sl_lo    first slab whose last visible key lies beyond ks0
+//   sl_hi    end of the sample's slabs
+struct __align__(16) BwdRec {
+  int32_t s, g, c0, L, ks0, sl_lo, sl_hi, pad;
+};
+
 struct PlanCaps {
   int64_t S, NA, NSL, NCF, NCB, M, Hkv;
 };
@@ -78,6 +99,7 @@ struct PlanPtrs {
   int32_t* f_pos;          // [NCF]   queue position of rank r
   int32_t* f_qoff;         // [M+1]
   QEntry* f_queue;         // [NCF*Hkv]
+  FwdRec* f_rec;           // [NCF*Hkv] the same entries, decoded
   int64_t* f_load_lpt;     // [M]
   int64_t* f_load_contig;  // [M]
   // backward
@@ -90,6 +112,7 @@ struct PlanPtrs {
   int32_t* b_pos;
   int32_t* b_qoff;
   QEntry* b_queue;
+  BwdRec* b_rec;           // [NCB*Hkv] the same entries, decoded
   int64_t* b_load_lpt;
   int64_t* b_load_contig;
   // [NA] a_j + 1 (end of the visible context) when the mask is inclusive
@@ -132,6 +155,7 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   q.f_pos = (int32_t*)take(4 * (c.NCF + 1));
   q.f_qoff = (int32_t*)take(4 * (c.M + 1));
   q.f_queue = (QEntry*)take(sizeof(QEntry) * (c.NCF * c.Hkv + 1));
+  q.f_rec = (FwdRec*)take(sizeof(FwdRec) * (c.NCF * c.Hkv + 1));
   q.f_load_lpt = (int64_t*)take(8 * c.M);
   q.f_load_contig = (int64_t*)take(8 * c.M);
   q.b_cost = (int64_t*)take(8 * (c.NCB + 1));
@@ -143,6 +167,7 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   q.b_pos = (int32_t*)take(4 * (c.NCB + 1));
   q.b_qoff = (int32_t*)take(4 * (c.M + 1));
   q.b_queue = (QEntry*)take(sizeof(QEntry) * (c.NCB * c.Hkv + 1));
+  q.b_rec = (BwdRec*)take(sizeof(BwdRec) * (c.NCB * c.Hkv + 1));
   q.b_load_lpt = (int64_t*)take(8 * c.M);
   q.b_load_contig = (int64_t*)take(8 * c.M);
   q.anchor_end = (int32_t*)take(4 * (c.NA + 1));

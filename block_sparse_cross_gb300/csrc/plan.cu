@@ -373,6 +373,46 @@ __device__ __forceinline__ QEntry decode_fwd(const ProbDev& P, const PlanPtrs& p
   return e;
 }
 
+// The decoded form of forward entry e (see FwdRec): the chunk's tiles end at
+// the slab's last visible key (its largest anchor end) or the chunk end.
+__device__ __forceinline__ FwdRec fwd_rec(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
+  FwdRec R;
+  R.first = pp.sl_first[e.slab];
+  R.nblk = pp.sl_nblk[e.slab];
+  const int c0 = P.cu_ctx[e.s], L = P.cu_ctx[e.s + 1] - c0;
+  const int amax = P.anchors[R.first + R.nblk - 1];
+  R.cs = e.c * P.chunk;
+  const int ke = min(min(R.cs + P.chunk, L), amax);
+  R.ntiles = (ke - R.cs + kKeyTile - 1) / kKeyTile;
+  R.row0 = c0 + R.cs;
+  R.n0 = R.first * P.B;
+  R.g = e.g;
+  R.slot = (pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
+  return R;
+}
+
+// The decoded form of backward entry e (see BwdRec): the slabs that see the
+// key tile start at the first one whose last visible key lies beyond the
+// tile start (anchors, hence slabs' last anchors, rise within a sample).
+__device__ __forceinline__ BwdRec bwd_rec(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
+  BwdRec R;
+  R.s = e.s;
+  R.g = e.g;
+  R.c0 = P.cu_ctx[e.s];
+  R.L = P.cu_ctx[e.s + 1] - R.c0;
+  R.ks0 = e.c * kKeyTile;
+  const int sl0 = pp.s_slab_off[e.s], sl1 = pp.s_slab_off[e.s + 1];
+  int lo = sl0, hi = sl1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (P.anchors[pp.sl_first[mid] + pp.sl_nblk[mid] - 1] > R.ks0) hi = mid; else lo = mid + 1;
+  }
+  R.sl_lo = lo;
+  R.sl_hi = sl1;
+  R.pad = 0;
+  return R;
+}
+
 __device__ __forceinline__ QEntry decode_bwd(const ProbDev& P, const PlanPtrs& pp, int cand,
                                              int g) {
   const int s = seg_of(pp.s_bcand_off, P.S, cand);
@@ -436,9 +476,23 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
       for (int r = tid; r < n; r += blockDim.x) {
         const int cand = item[sorted[r]];
         const int Gr = grp[r], p = pos[r];
+        // the record of replica g differs from replica 0's only in g (and slot)
+        QEntry e = kind == 0 ? decode_fwd(P, pp, cand, 0) : decode_bwd(P, pp, cand, 0);
+        FwdRec fr;
+        BwdRec br;
+        if (kind == 0) fr = fwd_rec(P, pp, e); else br = bwd_rec(P, pp, e);
         for (int g = 0; g < Hkv; ++g) {
-          QEntry e = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
-          queue[qoff[Gr * Hkv + g] + p] = e;
+          const int at = qoff[Gr * Hkv + g] + p;
+          e.g = g;
+          queue[at] = e;
+          if (kind == 0) {
+            fr.g = g;
+            pp.f_rec[at] = fr;
+            ++fr.slot;
+          } else {
+            br.g = g;
+            pp.b_rec[at] = br;
+          }
         }
       }
     } else {
@@ -447,6 +501,8 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
         const int cand = item[x / Hkv];
         const int g = (int)(x % Hkv);
         queue[x] = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
+        if (kind == 0) pp.f_rec[x] = fwd_rec(P, pp, queue[x]);
+        else pp.b_rec[x] = bwd_rec(P, pp, queue[x]);
       }
     }
     __syncthreads();

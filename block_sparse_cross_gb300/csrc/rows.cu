@@ -635,18 +635,22 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
 template <typename T>
 __global__ void zero_uncovered_kernel(ProbDev P, PlanPtrs pp, T* __restrict__ dKc,
                                       T* __restrict__ dVc) {
+  // CTA (x, y) takes samples y, y + gridDim.y, ...: the rows of sample s
+  // from the end of its last visible key's tile to the sample's end, in
+  // 16-byte stores, strided over the x CTAs
   if (read_status(pp.hdr) != 0) return;
-  const int64_t row_elems = (int64_t)P.Hkv * P.d;
-  for (int64_t t = blockIdx.x; t < P.T; t += gridDim.x) {
-    const int s = seg_of(P.cu_ctx, P.S, t);
-    const int local = (int)(t - P.cu_ctx[s]);
+  const size_t row16 = (size_t)P.Hkv * P.d * sizeof(T) / 16;  // d in {64, 128}: whole 16 B units
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int s = blockIdx.y; s < P.S; s += gridDim.y) {
+    const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
     const int a0 = P.cu_anchor[s], a1 = P.cu_anchor[s + 1];
     const int alast = a1 > a0 ? P.anchors[a1 - 1] : 0;
-    const int covered = (alast + kKeyTile - 1) / kKeyTile * kKeyTile;
-    if (local < covered) continue;
-    for (int64_t x = threadIdx.x; x < row_elems; x += blockDim.x) {
-      st_f(dKc + t * row_elems + x, 0.f);
-      st_f(dVc + t * row_elems + x, 0.f);
+    const int covered = min(L, (alast + kKeyTile - 1) / kKeyTile * kKeyTile);
+    const size_t lo = (size_t)(c0 + covered) * row16, hi = (size_t)(c0 + L) * row16;
+    for (size_t i = lo + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi;
+         i += (size_t)gridDim.x * blockDim.x) {
+      ((uint4*)dKc)[i] = z;
+      ((uint4*)dVc)[i] = z;
     }
   }
 }
@@ -739,7 +743,8 @@ cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,
                                   cudaStream_t st) {
   if (P.T == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(P.T < 4096 ? P.T : 4096);
+  const int ys = P.S < 2048 ? P.S : 2048;
+  const dim3 grid((unsigned)(2048 / ys < 64 ? 2048 / ys : 64), (unsigned)ys);
   if (P.dtype == SPLITKV_FP32)
     zero_uncovered_kernel<float><<<grid, 256, 0, st>>>(P, pp, (float*)dKc, (float*)dVc);
   else
