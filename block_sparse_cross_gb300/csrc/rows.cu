@@ -195,43 +195,49 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
     md = m_new;
   }
   const float lse_d = md + logf(ld);
-  // pass 1: max and normaliser over chunk partials (+ draft)
+  // One pass over the chunk partials in ascending chunk order, then the
+  // draft partial: a running maximum Mr and normaliser Sr, the weighted sum
+  // rescaled when the maximum grows. Lane c of each group of 32 chunks holds
+  // chunk c's lse; the group's lse values and its first eight partial rows
+  // are loaded together, eight rows in flight per step.
   const size_t slot0 = (size_t)pp.sl_slot[G.slab];
   const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + G.r;  // chunk c at c * Hkv * 128
   const size_t cstride = (size_t)P.Hkv * kRows;
-  float M = lse_d;
-  for (int c = lane; c < G.nact; c += 32) M = fmaxf(M, plse[c * cstride]);
-  M = warp_max(M);
-  float Ls = 0.f;
-  for (int c = lane; c < G.nact; c += 32) Ls += expf(plse[c * cstride] - M);
-  Ls = warp_sum(Ls) + expf(lse_d - M);
-  const float invL = 1.f / Ls;
-  // pass 2: weighted sum in ascending chunk order, then the draft partial.
-  // Lane c of each group of 32 chunks holds chunk c's weight; eight rows are
-  // in flight per step.
+  const float* pbase = wk.part_o + (slot0 * P.Hkv + g) * kRows * D + (size_t)G.r * D + x0;
+  const size_t ostride = cstride * D;
+  constexpr int U = 8;
+  auto load_rows = [&](int cb, int c0, int nc, float (&v)[U][EPL]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = min(c0 + u, nc - 1);  // clamped rows get weight 0
+      const float* po = pbase + (size_t)(cb + c) * ostride;
+      if constexpr (EPL == 4) {  // 16-byte aligned: row * D * 4 and lane * 16 bytes
+        const float4 t = *(const float4*)po;
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) v[u][i] = po[i];
+      }
+    }
+  };
   float acc[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
-  const float* pbase = wk.part_o + (slot0 * P.Hkv + g) * kRows * D + (size_t)G.r * D + x0;
-  const size_t ostride = cstride * D;
+  float Mr = -INFINITY, Sr = 0.f;
   for (int cb = 0; cb < G.nact; cb += 32) {
     const int nc = min(32, G.nact - cb);
-    const float e = lane < nc ? expf(plse[(cb + lane) * cstride] - M) * invL : 0.f;
-    constexpr int U = 8;
+    const float lc = lane < nc ? plse[(cb + lane) * cstride] : -INFINITY;
+    float v[U][EPL];
+    load_rows(cb, 0, nc, v);
+    const float Mn = fmaxf(Mr, warp_max(lc));
+    const float f = Mr == -INFINITY ? 0.f : expf(Mr - Mn);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[i] *= f;
+    const float e = lc == -INFINITY ? 0.f : expf(lc - Mn);  // this lane's chunk weight
+    Sr = Sr * f + warp_sum(e);
+    Mr = Mn;
     for (int c0 = 0; c0 < nc; c0 += U) {
-      float v[U][EPL];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = min(c0 + u, nc - 1);  // clamped rows get weight 0 below
-        const float* po = pbase + (size_t)(cb + c) * ostride;
-        if constexpr (EPL == 4) {  // 16-byte aligned: row * D * 4 and lane * 16 bytes
-          const float4 t = *(const float4*)po;
-          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-        } else {
-#pragma unroll
-          for (int i = 0; i < EPL; ++i) v[u][i] = po[i];
-        }
-      }
+      if (c0 > 0) load_rows(cb, c0, nc, v);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float wgt = __shfl_sync(0xffffffffu, e, min(c0 + u, 31));
@@ -242,9 +248,20 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
       }
     }
   }
-  const float wd = expf(lse_d - M) * invL / ld;
+  {  // the draft partial (its lse is finite: every row sees a draft key)
+    const float Mn = fmaxf(Mr, lse_d);
+    const float f = Mr == -INFINITY ? 0.f : expf(Mr - Mn);
+    const float ed = expf(lse_d - Mn);
+    Sr = Sr * f + ed;
+    Mr = Mn;
+    const float wd = ed / ld;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wd, od[i], acc[i]);
+    for (int i = 0; i < EPL; ++i) acc[i] = fmaf(wd, od[i], acc[i] * f);
+  }
+  const float invS = 1.f / Sr;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) acc[i] *= invS;
+  const float M = Mr, Ls = Sr;
   st_vec<T, EPL>(O + ((size_t)n * P.Hq + h) * D + x0, acc);
   if (lane == 0) LSE[(size_t)h * P.NQ + n] = M + logf(Ls);
 }
@@ -480,11 +497,13 @@ __global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtr
   auto row_of = [&](int rr) {
     return ((size_t)(j * B + rr / G) * P.Hq + g * G + rr % G) * D + x0;
   };
-  float qn[EPL], don[EPL], onx[EPL];
+  auto lse_of = [&](int rr) { return LSE[(size_t)(g * G + rr % G) * P.NQ + j * B + rr / G]; };
+  float qn[EPL], don[EPL], onx[EPL], lsen = 0.f;
   if (warp < R) {
     ld_vec<T, EPL>(Q + row_of(warp), qn);
     ld_vec<T, EPL>(dO + row_of(warp), don);
     ld_vec<T, EPL>(O + row_of(warp), onx);
+    lsen = lse_of(warp);
   }
   for (int r = warp; r < R; r += 8) {
     const int n = j * B + r / G, h = g * G + r % G;
@@ -496,16 +515,17 @@ __global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtr
       dov[i] = don[i];
       ov[i] = onx[i];
     }
+    const float lse = lsen;
     if (r + 8 < R) {
       ld_vec<T, EPL>(Q + row_of(r + 8), qn);
       ld_vec<T, EPL>(dO + row_of(r + 8), don);
       ld_vec<T, EPL>(O + row_of(r + 8), onx);
+      lsen = lse_of(r + 8);
     }
     float dd = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) dd = fmaf(dov[i], ov[i], dd);
     const float Dr = warp_sum(dd);
-    const float lse = LSE[(size_t)h * P.NQ + n];
     if (lane == 0) wk.dvec[(size_t)h * P.NQ + n] = Dr;
     float acc[EPL];
 #pragma unroll
