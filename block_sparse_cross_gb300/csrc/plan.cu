@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
     H->n_slot_base = (int32_t)nslot;
   }
   // ---- D: candidate costs -------------------------------------------------
+  unsigned long long my_tiles = 0;  // summed per warp, one shared atomic per warp
   for (int id = tid; id < ncand; id += blockDim.x) {
     const int s = seg_of(pp.s_cand_off, S, id);
     const int local = id - pp.s_cand_off[s];
@@ -187,11 +188,10 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
     int ke;
     const int64_t cost = fwd_item_cost(P, s, c, sigma, &ke);
     pp.f_cost[id] = cost;
-    if (cost > 0) {
-      const int cs = c * P.chunk;
-      atomicAdd(&tiles_acc, (unsigned long long)((ke - cs + kKeyTile - 1) / kKeyTile));
-    }
+    if (cost > 0) my_tiles += (unsigned long long)((ke - c * P.chunk + kKeyTile - 1) / kKeyTile);
   }
+  for (int o = 16; o > 0; o >>= 1) my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
+  if ((tid & 31) == 0 && my_tiles) atomicAdd(&tiles_acc, my_tiles);
   for (int id = tid; id < nbcand; id += blockDim.x) {
     const int s = seg_of(pp.s_bcand_off, S, id);
     pp.b_cost[id] = bwd_item_cost(P, s, id - pp.s_bcand_off[s]);
@@ -280,27 +280,39 @@ __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32
   // fits 32 bits when that cost is < 2^26, and a single warp min-reduction
   // finds the least-loaded group with the lowest id.
   if (G <= 32 && (n == 0 || scost[0] < (1LL << 26))) {
-    int64_t load = 0, base = 0;
+    // rel = this lane's load minus the running minimum (< 2^26), so every
+    // step is 32-bit and branch-free: the group that takes item t is the
+    // warp-uniform minimum m & 31; lane t keeps item t's (group, position)
+    // and stores them once per 32 items.
+    uint32_t rel = 0;
+    int64_t base = 0;
     int32_t cnt = 0;
     for (int r0 = 0; r0 < n; r0 += 32) {
       const int32_t mine = (r0 + lane < n) ? (int32_t)scost[r0 + lane] : 0;
       const int lim = min(32, n - r0);
+      int32_t my_grp = 0, my_pos = 0;
       for (int t = 0; t < lim; ++t) {
-        const int32_t c = __shfl_sync(0xffffffffu, mine, t);
-        const uint32_t key =
-            lane < G ? ((uint32_t)(load - base) << 5) | (uint32_t)lane : 0xffffffffu;
+        const uint32_t c = (uint32_t)__shfl_sync(0xffffffffu, mine, t);
+        const uint32_t key = lane < G ? (rel << 5) | (uint32_t)lane : 0xffffffffu;
         const uint32_t m = __reduce_min_sync(0xffffffffu, key);
-        if ((int)(m & 31u) == lane) {
-          grp[r0 + t] = lane;
-          pos[r0 + t] = cnt;
-          cnt += 1;
-          load += c;
+        const int gsel = (int)(m & 31u);
+        const bool take = gsel == lane;
+        const int32_t p = __shfl_sync(0xffffffffu, cnt, gsel);
+        if (lane == t) {
+          my_grp = gsel;
+          my_pos = p;
         }
+        rel = rel - (m >> 5) + (take ? c : 0u);
+        cnt += take ? 1 : 0;
         base += (int64_t)(m >> 5);
+      }
+      if (lane < lim) {
+        grp[r0 + lane] = my_grp;
+        pos[r0 + lane] = my_pos;
       }
     }
     if (lane < G) {
-      gload[lane] = load;
+      gload[lane] = base + (int64_t)rel;
       gcount[lane] = cnt;
     }
     return;
