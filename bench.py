@@ -234,6 +234,9 @@ def sample_flop(w, blocks) -> int:
 
 
 def oracle_threads() -> int:
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -734,6 +737,60 @@ def run_projection_study(args, d):
     return 0
 
 
+def _oracle_line(w, host, blocks, seconds, full: bool) -> dict:
+    f_sample = sample_flop(w, blocks)
+    f_total = w.useful_flop(14)
+    return {"workload": workload_desc(w), "threads": oracle_threads(),
+            "blocks": f"{len(blocks)} of {w.total_anchors}", "seconds": seconds,
+            "tflops": f_sample / seconds / 1e12,
+            "full_seconds": seconds if full else seconds * f_total / f_sample,
+            "full": "measured" if full else "linear extrapolation by masked-pair count"}
+
+
+def run_oracle_study(args, d):
+    """The float64 oracle timed on this machine's host cores (a reported
+    baseline only): the whole problem for configs 0 and 1, a seeded block
+    sample with a labelled linear extrapolation by masked-pair count for
+    configs 2, 3 and 4 (L = 16k and 256k), and single-thread times for
+    configs 0 and 1 (a child process with one BLAS thread)."""
+    if d.rank != 0:
+        return 0
+    if args.study == "oracle-1t":  # the child: one case, BLAS limited to one thread
+        w = W.config(args.config)
+        host = host_inputs(w)
+        if args.config == 0:
+            blocks = np.arange(w.total_anchors)
+            t = oracle_sample_seconds(w, host, blocks)
+        else:
+            blocks, t = calibrate_blocks(w, host, 8.0, w.seed + 99)
+        print(json.dumps(_oracle_line(w, host, blocks, t, args.config == 0)), flush=True)
+        return 0
+    cases = [(0, 0, True), (1, 0, True), (2, 0, False), (3, 0, False), (4, 0, False), (4, 4, False)]
+    for cfg, sweep, full in cases:
+        w = W.config(cfg, sweep)
+        host = host_inputs(w)
+        if full:
+            blocks = np.arange(w.total_anchors)
+            oracle_sample_seconds(w, host, blocks[:1])  # warm
+            t = oracle_sample_seconds(w, host, blocks)
+        else:
+            blocks, t = calibrate_blocks(w, host, 8.0, w.seed + 99)
+        line = {"study": "oracle"}
+        line.update(_oracle_line(w, host, blocks, t, full))
+        if cfg <= 1:
+            env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1",
+                       MKL_NUM_THREADS="1")
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--study", "oracle-1t",
+                                "--config", str(cfg)], env=env, capture_output=True, text=True,
+                               timeout=600)
+            if r.returncode == 0 and r.stdout.strip():
+                one = json.loads(r.stdout.strip().splitlines()[-1])
+                line["single_thread"] = {k: one[k] for k in ("threads", "blocks", "seconds",
+                                                             "tflops", "full_seconds", "full")}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def busy_imbalance(kv, S):
     """Measured load balance of the latest launch of each persistent attention
     kernel: per-CTA busy time (end - start %globaltimer) max / mean - 1."""
@@ -762,11 +819,12 @@ def main():
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--contiguous", action="store_true",
                     help="contiguous item assignment instead of LPT")
-    ap.add_argument("--study", choices=("balance", "planner", "projection"),
+    ap.add_argument("--study", choices=("balance", "planner", "projection", "oracle", "oracle-1t"),
                     help="balance: step time with LPT vs contiguous plans (configs 3, 4); "
                          "planner: plan time vs item count next to the forward (configs 1-4); "
                          "projection: the drafter layer's projection GEMMs and the whole "
-                         "layer step (configs 1, 2)")
+                         "layer step (configs 1, 2); oracle: the float64 oracle on the host "
+                         "cores, whole problems and extrapolated samples, one thread and all")
     ap.add_argument("--proj-configs", default="1,2",
                     help="configs of --study projection (comma-separated)")
     args = ap.parse_args()
@@ -776,6 +834,8 @@ def main():
     try:
         if args.study == "projection":
             rc = run_projection_study(args, d)
+        elif args.study in ("oracle", "oracle-1t"):
+            rc = run_oracle_study(args, d)
         elif args.study:
             rc = run_study(args, d)
         else:
