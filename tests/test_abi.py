@@ -110,3 +110,7 @@ def test_projection_entry_points_validate_on_the_host():
     assert S.splitkv_proj_in_bwd(make_problem(d=96), 128, *([dummy] * 11)) == u
     assert S._lib.splitkv_proj_status(None, 0, None) == inval
     assert S.splitkv_kernel_name(S.SPLITKV_K_PROJ) == "projection"
+
+
+def test_selftest_validates_on_the_host():
+    assert S._lib.splitkv_selftest_wait_timeout(None, None) == S.SPLITKV_EINVAL
