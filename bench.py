@@ -7,10 +7,15 @@ Metric: useful (masked) fwd+bwd TFLOP/s, FLOP = Hq * d * 14 * sum_j B*(a_j+B)
 self-block included), also as % of the dense bf16 tensor peak, plus the
 planned LPT imbalance against naive contiguous assignment.
 
-Default workload: config 2 (one sample, L = 65536 keys, prompt 8192,
-256 anchors x B = 16 = 4096 draft queries, Hq 32 / Hkv 8, d 128, chunk
-2048, bf16, seeded N(0,1) inputs). K + V are 256 MiB > L2, so every step
-streams them from HBM.
+Default workload: the largest single-GPU configuration, config 4 at
+L = 262144 (one sample, prompt 32768, 512 anchors x B = 16 = 8192 draft
+queries, Hq 32 / Hkv 8, d 128, chunk 2048, bf16, seeded N(0,1) inputs,
+68.7 useful TFLOP per step). K + V are 1 GiB > L2, so every step streams them
+from HBM. The same line carries a record per configuration (configs 1, 2,
+the three config-3 draws and every config-4 length): useful TFLOP/s and %
+of the burst bf16 peak, per-kernel times and TFLOP/s, HBM GB/s of the merge
+and dQ-reduce kernels, skip rate, and LPT against contiguous imbalance,
+planned and measured.
 
 N > 1 GPUs (torchrun): every rank runs its own independent batch (weak
 scaling, no data-path collective); gloo is used only for the barrier and the
@@ -169,9 +174,9 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def profile_traffic(kernel: str, source_sha: str):
+def profile_traffic(kernel: str, source_sha: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the current kernel source and on this workload (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_ncu.md")
     try:
         text = open(path).read()
@@ -179,7 +184,8 @@ def profile_traffic(kernel: str, source_sha: str):
         return None
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_b or m_sha.group(1) != source_sha:
+    m_w = re.search(r"traffic_workload:\s*(\S+)", text)
+    if not m_sha or not m_b or not m_w or m_sha.group(1) != source_sha or m_w.group(1) != workload:
         return None
     return float(m_b.group(1))
 
@@ -365,10 +371,13 @@ def run_ours(args, d: Dist):
     pst, ktimes = S.splitkv_profile_read()
     busy = busy_imbalance(kv, S)
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
 
     # ---- per-kernel roofline from the live CUDA-event brackets ----
     cp = context_pairs(w)
+    row_bytes = row_kernel_bytes(w)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAK["hbm_gbs"]))
     kernels = {}
     for name, (launches, tot) in ktimes.items():
         if launches == 0:
@@ -381,14 +390,19 @@ def run_ours(args, d: Dist):
         if name in KERNEL_FLOP_PER_PAIR_DIM:
             f = KERNEL_FLOP_PER_PAIR_DIM[name] * w.d * w.Hq * cp
             entry["tflops"] = f / (per_launch * 1e-3) / 1e12
+        if name in row_bytes:
+            entry["hbm_gbs"] = row_bytes[name] / (per_launch * 1e-3) / 1e9
+            entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
+            entry["bytes"] = row_bytes[name]
         kernels[name] = entry
     attn = {k: v for k, v in kernels.items() if k in KERNEL_FLOP_PER_PAIR_DIM}
     dom = max(attn, key=lambda k: attn[k]["ms_total"])
     sha = kernel_source_sha()
-    traffic = profile_traffic(dom, sha)
+    traffic = profile_traffic(dom, sha, w.name)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": attn[dom]["tflops"], "peak": peak,
                 "unit": "TFLOP/s", "frac": attn[dom]["tflops"] / peak, "traffic": traffic,
-                "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "frac_of_sustained": attn[dom]["tflops"] / peak_sus,
                 "flop_per_launch": KERNEL_FLOP_PER_PAIR_DIM[dom] * w.d * w.Hq * cp}
     launches_total = sum(v["launches"] for v in kernels.values())
     fwd_ms = sum(kernels.get(k, {}).get("ms_total", 0.0) for k in ("fwd_attention", "merge")) / args.steps
@@ -502,6 +516,18 @@ def run_ours(args, d: Dist):
                          f"({t:.1f} s), float64 numpy fwd+bwd"}
         errors = oracle_errors(w, blocks, ref, outs)
 
+    kv_mib = int(2 * w.total_ctx * w.Hkv * w.d * 2 / 2**20)
+    per_config = None
+    if d.rank == 0 and d.world == 1 and not args.no_configs:
+        del kv, gpu, outs
+        torch.cuda.empty_cache()
+        per_config = {}
+        for cfg, sweep in CONFIG_RECORDS:
+            wc = w if (cfg, sweep) == (args.config, args.sweep) else W.config(cfg, sweep)
+            key = f"{wc.name}_draw{sweep}" if cfg == 3 else wc.name
+            per_config[key] = measure_config(wc, dev, S, torch, args.config_steps, peak)
+            torch.cuda.empty_cache()
+
     if d.rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": d.world,
@@ -510,10 +536,11 @@ def run_ours(args, d: Dist):
             "data": "synthetic",
             "config": {"workload": workload_desc(w), "global_batch": d.world * w.n_q,
                        "seq_len": int(w.max_ctx), "parallelism": f"replicas x{d.world}",
-                       "l2": "inputs larger than L2 (K+V 256 MiB per step)"
-                             if args.config == 2 else "see workload",
+                       "l2": f"inputs larger than L2 (K+V {kv_mib} MiB per step)",
                        "step": "plan + forward + backward"},
             "pct_of_peak": 100.0 * value / d.world / peak,
+            "peak": {"bf16_tflops": peak, "source": f"bf16_tflops (burst) of {peak_src}",
+                     "pct_of_sustained": 100.0 * value / d.world / peak_sus},
             "plan": "contiguous" if args.contiguous else "lpt",
             "lpt_imbalance": {"fwd": st.fwd_lpt_imbalance, "bwd": st.bwd_lpt_imbalance},
             "busy_imbalance": busy,
@@ -530,9 +557,99 @@ def run_ours(args, d: Dist):
             "e2e_serial": e2e_serial,
             "cpu_baseline": cpu,
             "oracle_errors": errors,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# Per-configuration records (in the bench line)
+# ---------------------------------------------------------------------------
+CONFIG_RECORDS = [(1, 0), (2, 0), (3, 0), (3, 1), (3, 2), (4, 0), (4, 1), (4, 2), (4, 3), (4, 4)]
+
+
+def row_kernel_bytes(w) -> dict:
+    """Algorithmic HBM bytes of one merge and one dQ-reduce launch.
+
+    A (query, head) row of draft block j has nact_j = ceil(a_j / C) chunk
+    partials. The merge reads each partial row once ((d + 1) fp32: O and
+    lse), the row's Q (bf16) and, once per (block, kv head), the block's B
+    draft keys and values, and writes O (bf16) and LSE (fp32). The dQ reduce
+    reads each partial dQ row (d fp32) and the row's draft term (d fp32) and
+    writes dQ (bf16)."""
+    nact = -(-w.anchors.astype(np.int64) // w.chunk)
+    part_rows = int(nact.sum()) * w.B * w.Hq
+    rows = w.n_q * w.Hq
+    merge = (part_rows * (4 * w.d + 4) + rows * (2 * w.d + 2 * w.d + 4) +
+             w.total_anchors * w.Hkv * 2 * w.B * w.d * 2)
+    reduce = part_rows * 4 * w.d + rows * (4 * w.d + 2 * w.d)
+    return {"merge": merge, "dq_reduce": reduce}
+
+
+def measure_config(w, dev, S, torch, steps, peak):
+    """One configuration: plan + forward + backward steps with the LPT plan
+    and with the contiguous plan, CUDA events around `steps` steps (3 untimed
+    first), the library's per-launch event brackets for the kernel split,
+    and the per-CTA busy stamps of the last launch of each attention kernel."""
+    cp = context_pairs(w)
+    rb = row_kernel_bytes(w)
+    hbm_peak = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAK["hbm_gbs"]))
+    rec = {"workload": workload_desc(w), "useful_tflop_per_step": w.useful_flop(14) / 1e12,
+           "steps": steps}
+    for mode, flags in (("lpt", 0), ("contiguous", S.SPLITKV_FLAG_CONTIGUOUS)):
+        kv, keep, fwd, bwd = _setup(w, dev, flags, S, torch)
+
+        def step():
+            kv.plan()
+            fwd()
+            bwd()
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        S.splitkv_profile_enable(True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        S.splitkv_profile_enable(False)
+        if kv.device_status() != S.SPLITKV_OK:
+            raise RuntimeError(f"{w.name} {mode}: " +
+                               S.splitkv_status_string(kv.device_status()))
+        ms = a.elapsed_time(b) / steps
+        _, kt = S.splitkv_profile_read()
+        st = kv.stats()
+        busy = {k: v["imbalance"] for k, v in busy_imbalance(kv, S).items()}
+        tf = w.useful_flop(14) / (ms * 1e-3) / 1e12
+        r = {"ms_per_step": ms, "tflops": tf, "pct_of_peak": 100.0 * tf / peak,
+             "busy_imbalance": busy}
+        if mode == "lpt":
+            kern = {}
+            for name, (launches, tot) in kt.items():
+                if launches == 0:
+                    continue
+                e = {"ms_per_step": tot / steps}
+                if name in KERNEL_FLOP_PER_PAIR_DIM:
+                    f = KERNEL_FLOP_PER_PAIR_DIM[name] * w.d * w.Hq * cp
+                    e["tflops"] = f / (tot / steps * 1e-3) / 1e12
+                    e["frac_of_peak"] = e["tflops"] / peak
+                if name in rb:
+                    e["hbm_gbs"] = rb[name] / (tot / steps * 1e-3) / 1e9
+                    e["hbm_frac"] = e["hbm_gbs"] / hbm_peak
+                    e["bytes"] = rb[name]
+                kern[name] = e
+            r["kernels"] = kern
+            r["skip_rate"] = 1.0 - st.fwd_tiles / max(1, st.dense_tiles)
+            r["planned_imbalance"] = {
+                "lpt": {"fwd": st.fwd_lpt_imbalance, "bwd": st.bwd_lpt_imbalance},
+                "contiguous": {"fwd": st.fwd_contig_imbalance, "bwd": st.bwd_contig_imbalance}}
+        rec[mode] = r
+        del kv, keep
+        torch.cuda.empty_cache()
+    rec["speedup_lpt_over_contiguous"] = rec["contiguous"]["ms_per_step"] / rec["lpt"]["ms_per_step"]
+    return rec
 
 
 # ---------------------------------------------------------------------------
@@ -811,8 +928,12 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--sweep", type=int, default=0)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--sweep", type=int, default=4)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration records")
+    ap.add_argument("--config-steps", type=int, default=10,
+                    help="timed steps of each per-configuration record")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-target-s", type=float, default=15.0)

@@ -265,6 +265,50 @@ int run_proj(const ProjSpec* parts, int n, cudaStream_t s) {
   return cuda_status(timed(SPLITKV_K_PROJ, 1, s, [&] { return launch_proj(parts, n, s); }));
 }
 
+// The per-worker queues the attention kernels walk (LPT or contiguous,
+// whichever the plan holds), worker by worker in queue order, each entry
+// mapped back to its per-kv-head item id and cost.
+int export_queues(const Ctx& c, const PlanHeader& h, bool fwd, int64_t* ids, int64_t* costs,
+                  int32_t* worker, int32_t* pos, int64_t capacity, int64_t* count) {
+  const int m = c.P.workers, S = c.P.S, Hkv = c.P.Hkv;
+  const int ncand = fwd ? h.n_fwd_cand : h.n_bwd_cand;
+  std::vector<int32_t> qoff(m + 1), cand_off(S + 1), nsl(S + 1), slab_off(S + 1);
+  std::vector<int64_t> cost(ncand > 0 ? ncand : 1);
+  cudaError_t e = cudaMemcpy(qoff.data(), fwd ? c.pp.f_qoff : c.pp.b_qoff, 4 * (m + 1),
+                             cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(cand_off.data(), fwd ? c.pp.s_cand_off : c.pp.s_bcand_off, 4 * (S + 1),
+                         cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(nsl.data(), c.pp.s_nsl, 4 * (S + 1), cudaMemcpyDeviceToHost);
+  e = e ? e : cudaMemcpy(slab_off.data(), c.pp.s_slab_off, 4 * (S + 1), cudaMemcpyDeviceToHost);
+  if (ncand > 0)
+    e = e ? e : cudaMemcpy(cost.data(), fwd ? c.pp.f_cost : c.pp.b_cost, 8 * (size_t)ncand,
+                           cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return SPLITKV_ECUDA;
+  const int64_t n = qoff[m];
+  *count = n;
+  std::vector<QEntry> q(n > 0 ? n : 1);
+  if (n > 0 && cudaMemcpy(q.data(), fwd ? c.pp.f_queue : c.pp.b_queue, sizeof(QEntry) * n,
+                          cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPLITKV_ECUDA;
+  int64_t k = 0;
+  for (int w = 0; w < m; ++w) {
+    for (int32_t at = qoff[w]; at < qoff[w + 1]; ++at, ++k) {
+      if (k >= capacity) return SPLITKV_OK;
+      const QEntry& x = q[at];
+      if (x.s < 0 || x.s >= S) return SPLITKV_EINVAL;
+      const int64_t cand =
+          fwd ? (int64_t)cand_off[x.s] + (int64_t)x.c * nsl[x.s] + (x.slab - slab_off[x.s])
+              : (int64_t)cand_off[x.s] + x.c;
+      if (cand < 0 || cand >= ncand) return SPLITKV_EINVAL;
+      ids[k] = cand * Hkv + x.g;
+      costs[k] = cost[cand];
+      worker[k] = w;
+      pos[k] = at - qoff[w];
+    }
+  }
+  return SPLITKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -490,13 +534,14 @@ int splitkv_plan_export(const splitkv_problem* prob, const void* plan_ws, int ki
   Ctx c;
   int st = setup(prob, plan_ws, &c);
   if (st) return st;
-  if ((kind != 0 && kind != 1) || !count || capacity < 0) return SPLITKV_EINVAL;
+  if (kind < 0 || kind > 3 || !count || capacity < 0) return SPLITKV_EINVAL;
   if (capacity > 0 && (!ids || !costs || !worker || !pos)) return SPLITKV_EINVAL;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPLITKV_ECUDA;
   PlanHeader h;
   if (cudaMemcpy(&h, c.pp.hdr, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
     return SPLITKV_ECUDA;
   if (h.magic != kPlanMagic || h.status != SPLITKV_OK) return SPLITKV_EINVAL;
+  if (kind >= 2) return export_queues(c, h, kind == 2, ids, costs, worker, pos, capacity, count);
   const int n = kind == 0 ? h.n_fwd_items : h.n_bwd_items;
   const int Hkv = prob->Hkv;
   *count = (int64_t)n * Hkv;

@@ -18,11 +18,8 @@
 // into k slices whose fp32 results are added with vector atomics into a
 // zeroed output; every other output is written once.
 //
-// Where the device can co-schedule them, CTAs run in pairs (2-CTA clusters)
-// on vertically adjacent tiles of the same unit: each CTA loads its own A
-// rows and half of the shared B tile, multicast into both CTAs' shared
-// memory, so the bytes every SM pulls from L2 per k block drop from 48 KB to
-// 32 KB; both CTAs' MMAs release a stage before either producer refills it.
+// Every CTA loads its own A and B tiles into its own shared memory, from
+// the tensors its own call was given.
 //
 // Warp roles (256 threads, one CTA per SM): warp 0 loads A and B tiles with
 // TMA into a 4-stage ring, warp 1 issues the MMAs (one elected lane) into one
@@ -69,58 +66,24 @@ struct GUnit {
   int p, m0, n0, kb_lo, kb_hi;
 };
 
-// Unit u of a group run by clusters of C CTAs: the cluster's C CTAs take the
-// vertically adjacent tiles mg * C + rank of one (part, slice, n) unit.
-template <int C>
-__device__ __forceinline__ GUnit decode_unit(const ProjGroup& G, int u, int rank) {
+// Unit u of a group: part p, k slice s, output tile (mt, nt), n fastest so
+// that CTAs running side by side share the A rows.
+__device__ __forceinline__ GUnit decode_unit(const ProjGroup& G, int u) {
   int p = 0;
   while (p + 1 < G.nparts && u >= G.part[p + 1].unit0) ++p;
   const ProjPart& P = G.part[p];
   int r = u - P.unit0;
-  const int mg_count = (P.mt + C - 1) / C;
-  const int per_slice = mg_count * P.nt;
+  const int per_slice = P.mt * P.nt;
   const int s = r / per_slice;
   r -= s * per_slice;
-  const int mg = r / P.nt;  // n fastest: clusters running side by side share the A rows
+  const int mt = r / P.nt;
   GUnit U;
   U.p = p;
-  U.m0 = (mg * C + rank) * kGM;
-  U.n0 = (r - mg * P.nt) * kGN;
+  U.m0 = mt * kGM;
+  U.n0 = (r - mt * P.nt) * kGN;
   U.kb_lo = s * P.kb_per_split;
   U.kb_hi = min(P.nkb, U.kb_lo + P.kb_per_split);
   return U;
-}
-
-// Tiled 2-D load delivered to the same shared-memory offset (data and
-// complete_tx on the same barrier offset) of every CTA in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
-// Arrives on `bar` (same offset) in every CTA of `mask` once this thread's
-// issued tcgen05 ops are done.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-__device__ __forceinline__ int cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return (int)r;
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -137,10 +100,8 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, volatile i
   return __all_sync(0xffffffffu, mine);
 }
 
-template <int C>
 __global__ void __launch_bounds__(kGThreads, 1)
     proj_gemm_kernel(const __grid_constant__ GemmMaps maps, const ProjGroup G) {
-  static_assert(C == 1 || C == 2, "CTAs per cluster");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + kGBars);
@@ -152,14 +113,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(mma_drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = C == 1 ? 0 : cluster_rank();
-  const int cluster = blockIdx.x / C, nclusters = gridDim.x / C;
-  constexpr uint16_t kPair = (1u << C) - 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kGStages; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, C);  // every CTA's MMAs must release the stage
+      mbar_init(empty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
@@ -175,7 +133,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (C > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -183,8 +140,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // ---------------- TMA producer (whole warp waits, one lane issues) ----------------
     uint32_t it = 0;
     bool ok = true;
-    for (int u = cluster; u < G.units && ok; u += nclusters) {
-      const GUnit U = decode_unit<C>(G, u, rank);
+    for (int u = blockIdx.x; u < G.units && ok; u += gridDim.x) {
+      const GUnit U = decode_unit(G, u);
       const ProjPart& P = G.part[U.p];
       int sg = 0;
       for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
@@ -205,22 +162,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
           } else {
             tma_load_2d(sa, ma, full + st, S.a_k + k, P.a_off + U.m0);
           }
-          if constexpr (C == 1) {
-            if (P.b_mn) {
-              for (int i = 0; i < kGN / 64; ++i)
-                tma_load_2d(sb + i * kGChunk, mb, full + st, P.b_off + U.n0 + 64 * i, S.b_k + k);
-            } else {
-              tma_load_2d(sb, mb, full + st, S.b_k + k, P.b_off + U.n0);
-            }
-          } else {  // this CTA's half of B (columns rank * 128 ...), into both CTAs
-            if (P.b_mn) {
-              for (int i = 2 * rank; i < 2 * rank + 2; ++i)
-                tma_load_2d_mc(sb + i * kGChunk, mb, full + st, P.b_off + U.n0 + 64 * i,
-                               S.b_k + k, kPair);
-            } else {
-              tma_load_2d_mc(sb + rank * (kGB / 2), mb, full + st, S.b_k + k,
-                             P.b_off + U.n0 + rank * (kGN / 2), kPair);
-            }
+          if (P.b_mn) {
+            for (int i = 0; i < kGN / 64; ++i)
+              tma_load_2d(sb + i * kGChunk, mb, full + st, P.b_off + U.n0 + 64 * i, S.b_k + k);
+          } else {
+            tma_load_2d(sb, mb, full + st, S.b_k + k, P.b_off + U.n0);
           }
         }
         __syncwarp();
@@ -234,8 +180,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // ---------------- MMA issuer ----------------
     uint32_t it = 0, nu = 0;
     bool ok = true;
-    for (int u = cluster; u < G.units && ok; u += nclusters, ++nu) {
-      const GUnit U = decode_unit<C>(G, u, rank);
+    for (int u = blockIdx.x; u < G.units && ok; u += gridDim.x, ++nu) {
+      const GUnit U = decode_unit(G, u);
       const ProjPart& P = G.part[U.p];
       const uint32_t ab = nu & 1, au = nu >> 1;
       if (au > 0 && !(ok = gwait(acc_empty + ab, (au - 1) & 1, abort_flag))) break;
@@ -259,9 +205,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mma_ss(d_tmem, ad + (ao >> 4), bd + (bo >> 4), idesc,
                    (kb > U.kb_lo || kk > 0) ? 1u : 0u);
           }
-          // frees the stage (in every CTA whose producer writes it) once
-          // these MMAs have read it
-          if constexpr (C == 1) mma_commit(empty + st); else mma_commit_mc(empty + st, kPair);
+          mma_commit(empty + st);  // frees the stage once these MMAs have read it
         }
         __syncwarp();
       }
@@ -277,8 +221,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int q = warp & 3;
     uint32_t nu = 0;
     bool ok = true;
-    for (int u = cluster; u < G.units && ok; u += nclusters, ++nu) {
-      const GUnit U = decode_unit<C>(G, u, rank);
+    for (int u = blockIdx.x; u < G.units && ok; u += gridDim.x, ++nu) {
+      const GUnit U = decode_unit(G, u);
       const ProjPart& P = G.part[U.p];
       const uint32_t ab = nu & 1, au = nu >> 1;
       if (!(ok = gwait(acc_full + ab, au & 1, abort_flag))) break;
@@ -332,9 +276,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while its peer may still multicast into it or arrive on
-  // its barriers
-  if constexpr (C > 1) cluster_sync_all();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_proj_status, 0, (int)SPLITKV_ETIMEOUT);
@@ -377,41 +318,6 @@ int sm_count() {
   return n;
 }
 
-cudaLaunchConfig_t launch_cfg(int grid, int C, cudaStream_t st, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kGThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGSmem;
-  cfg.stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-// Co-resident 2-CTA clusters of the projection kernel on this device (0:
-// run single CTAs).
-int pair_clusters(int sms) {
-  static int cached_dev = -1, cached = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev == cached_dev) return cached;
-  int n = 0;
-  if (cudaFuncSetAttribute(proj_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGSmem) == cudaSuccess) {
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_cfg(2 * (sms / 2), 2, nullptr, attr);
-    if (cudaOccupancyMaxActiveClusters(&n, proj_gemm_kernel<2>, &cfg) != cudaSuccess) n = 0;
-  }
-  cudaGetLastError();  // a refused query leaves no sticky error behind
-  cached_dev = dev;
-  cached = n;
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st) {
@@ -435,8 +341,6 @@ cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st) {
     }
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
-  const int npairs = pair_clusters(sms);
-  const int C = npairs > 0 ? 2 : 1;
   GemmMaps maps;
   memset(&maps, 0, sizeof(maps));
   ProjGroup G;
@@ -469,7 +373,7 @@ cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st) {
                              s.a_mn ? 64u : (uint32_t)kGM);
       if (e != cudaSuccess) return e;
       e = map_2d(&maps.b[oi][j], s.b[j].ptr, s.b[j].cols, s.b[j].rows,
-                 s.b_mn ? 64u : (uint32_t)(kGN / C));  // a pair loads half of B each
+                 s.b_mn ? 64u : (uint32_t)kGN);
       if (e != cudaSuccess) return e;
     }
     P.nkb = kb;
@@ -480,24 +384,18 @@ cudaError_t launch_proj(const ProjSpec* parts, int nparts, cudaStream_t st) {
     P.ndst = s.ndst;
     for (int j = 0; j < s.ndst; ++j) P.dst[j] = s.dst[j];
     P.unit0 = (int)units;
-    units += (int64_t)((P.mt + C - 1) / C) * P.nt * P.ksplit;  // units of one cluster
+    units += (int64_t)P.mt * P.nt * P.ksplit;
   }
   G.nparts = nparts;
   if (units == 0) return cudaSuccess;
   if (units >= (1LL << 31)) return cudaErrorInvalidValue;
   G.units = (int)units;
-  if (C == 1) {
-    const int grid = (int)std::min<int64_t>(units, sms);
-    cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
-    if (e != cudaSuccess) return e;
-    proj_gemm_kernel<1><<<grid, kGThreads, kGSmem, st>>>(maps, G);
-    return cudaGetLastError();
-  }
-  const int grid = 2 * (int)std::min<int64_t>(units, npairs);
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_cfg(grid, 2, st, attr);
-  return cudaLaunchKernelEx(&cfg, proj_gemm_kernel<2>, maps, G);
+  const int grid = (int)std::min<int64_t>(units, sms);
+  cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kGSmem);
+  if (e != cudaSuccess) return e;
+  proj_gemm_kernel<<<grid, kGThreads, kGSmem, st>>>(maps, G);
+  return cudaGetLastError();
 }
 
 cudaError_t proj_status(int* status, bool clear) {

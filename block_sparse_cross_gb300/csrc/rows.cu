@@ -418,8 +418,7 @@ __global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp,
   float* dss = ps + R * B;   // [R][B]
   const int j = blockIdx.x, g = blockIdx.y;
   const int x = threadIdx.x;
-  // No status check here: bwd_prep_kernel, which runs first on the stream,
-  // skips its work on a latched error and the outputs are then undefined.
+  if (read_status(pp.hdr) != 0) return;  // every thread reads the same word
   for (int idx = x; idx < R * B; idx += blockDim.x) {
     const int r = idx / B, t = idx % B;
     const int n = j * B + r / P.group, h = g * P.group + r % P.group;

@@ -239,18 +239,24 @@ int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv
                        splitkv_stream stream);
 
 /*
- * splitkv_plan_export — SYNCHRONISES `stream` and copies the LPT result to
- *   host arrays, for verification against an independent implementation.
- *   kind: 0 = forward items, 1 = backward items. For every item of positive
- *   cost, in LPT order (cost desc, id asc), writes
+ * splitkv_plan_export — SYNCHRONISES `stream` and copies the plan to host
+ *   arrays, for verification against an independent implementation.
+ *   kind 0 = forward items, 1 = backward items: the LPT result. For every
+ *     item of positive cost, in LPT order (cost desc, id asc).
+ *   kind 2 = forward queues, 3 = backward queues: the queues the attention
+ *     kernels actually walk (the LPT queues, or the contiguous ranges of a
+ *     plan built with SPLITKV_FLAG_CONTIGUOUS), worker 0's queue first, each
+ *     queue in the order its CTA runs it.
+ *   Each entry i receives
  *     ids[i]    per-kv-head item id (forward: ((sample, chunk, slab) index) *
  *               Hkv + kv head; backward: ((sample, key tile) index) * Hkv + kv head)
  *     costs[i]  its cost
  *     worker[i] the persistent CTA it is assigned to
  *     pos[i]    its position in that CTA's queue
- *   capacity: length of each host array; *count receives the item count
+ *   capacity: length of each host array; *count receives the entry count
  *   (nothing is written past capacity).
- * Errors: EINVAL, ECUDA.
+ * Errors: EINVAL (also for a plan whose device status is not SPLITKV_OK),
+ * ECUDA.
  */
 int splitkv_plan_export(const splitkv_problem* prob, const void* plan_ws, int kind,
                         int64_t* ids, int64_t* costs, int32_t* worker, int32_t* pos,

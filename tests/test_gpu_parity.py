@@ -128,3 +128,58 @@ def test_tensor_core_matches_cuda_core_partials():
     cc = Case(w, flags=CC).plan().forward().numpy()
     assert rel_l2(tc["O"], cc["O"]) < 5e-3
     assert np.abs(tc["LSE"] - cc["LSE"]).max() < 1e-3
+
+
+CONTIG = S.SPLITKV_FLAG_CONTIGUOUS
+
+
+@pytest.mark.parametrize("which", ["cfg0", "fuzz0", "fuzz4", "fuzz6", "cfg1"])
+def test_contiguous_plan_full(which):
+    """The same kernels walking the naive contiguous queues give the same
+    results as the LPT queues: every item is run exactly once either way."""
+    if which == "cfg0":
+        w = W.config(0)
+    elif which == "cfg1":
+        w = W.config(1)
+    else:
+        spec = int(which[4:])
+        L, P, A, B, Hq, Hkv, d, chunk = FUZZ[spec]
+        w = W.custom(500 + spec, L, P, A, B=B, Hq=Hq, Hkv=Hkv, d=d, chunk=chunk)
+    case = Case(w, flags=CONTIG).plan().forward().backward()
+    compare_full(case, f"{which} contiguous")
+
+
+@pytest.mark.parametrize("idx,sweep,nh,na", [(3, 0, 4, 32), (3, 1, 4, 32), (3, 2, 4, 32),
+                                             (4, 0, 2, 16), (4, 2, 2, 16)])
+def test_contiguous_plan_large_configs_subset(idx, sweep, nh, na):
+    w = W.config(idx, sweep)
+    heads, blocks = W.subset(w, nh, na, seed=w.seed + 7)
+    case = Case(w, flags=CONTIG).plan().forward().backward()
+    compare_subset(case, heads, blocks, f"{w.name} contiguous subset")
+
+
+def test_config3_full():
+    """The packed variable-length batch (8 samples, 4096 queries, 109k keys)
+    against the float64 oracle on every row, head and gradient."""
+    case = Case(W.config(3)).plan().forward().backward()
+    compare_full(case, "cfg3 full")
+
+
+def test_unseen_keys_get_zero_gradients():
+    """Keys past a sample's last anchor (and every key of a sample without
+    anchors) are seen by no block: their dK, dV must be written as exact
+    zeros, not left as they were (the outputs start poisoned)."""
+    B, Hq, Hkv, d = 16, 8, 2, 128
+    w0 = W.custom(91, [2000, 640, 1500], [0, 0, 0], [2, 0, 3], B=B, Hq=Hq, Hkv=Hkv, d=d,
+                  chunk=256)
+    anchors = np.array([100, 300, 20, 700, 900], np.int32)  # sample 0 covers keys < 384 only
+    w = W.Workload("unseen", w0.cu_ctx, w0.cu_anchor, anchors, B, Hq, Hkv, d, 256, w0.seed)
+    case = Case(w).plan().forward().backward()
+    compare_full(case, "unseen keys")
+    out = case.numpy()
+    for k in ("dKc", "dVc"):
+        g = out[k]
+        assert np.all(g[384:2000] == 0.0), k          # sample 0 past its last anchor's tile
+        assert np.all(g[2000:2640] == 0.0), k         # sample 1 has no anchors
+        assert np.all(g[2640 + 1024:] == 0.0), k      # sample 2 past its last anchor's tile
+        assert np.abs(g[:300]).max() > 0, k

@@ -88,16 +88,77 @@ def test_plan_bit_exact_fuzz(seed):
     check_plan(w, workers)
 
 
-def test_contiguous_mode_queues_and_loads():
+def test_contiguous_mode_loads():
     w = W.config(3)
     kv = planned(w, 152, flags=S.SPLITKV_FLAG_CONTIGUOUS)
     st = kv.stats()
-    items = OP.fwd_items(w)
-    assert abs(st.fwd_contig_imbalance - OP.imbalance(OP.contiguous([i[-1] for i in items], 152))) < 1e-12
-    assert st.fwd_contig_imbalance > st.fwd_lpt_imbalance
+    for kind, items in (("fwd", OP.fwd_items(w)), ("bwd", OP.bwd_items(w))):
+        contig = OP.imbalance(OP.contiguous([i[-1] for i in items], 152))
+        assert abs(getattr(st, f"{kind}_contig_imbalance") - contig) < 1e-12
+        assert getattr(st, f"{kind}_contig_imbalance") > getattr(st, f"{kind}_lpt_imbalance")
 
 
 def test_skip_accounting():
     w = W.config(2)
     st = planned(w, 152).stats()
     assert 0 < st.fwd_tiles < st.dense_tiles
+
+
+def expected_queues(w, workers, contiguous):
+    """Per-worker queues of (per-head item id, cost) from the CPU oracle:
+    LPT queues in assignment order, or the contiguous id ranges."""
+    out = []
+    for items in (OP.fwd_items(w), OP.bwd_items(w)):
+        ids = [it[0] for it in items]
+        costs = [it[-1] for it in items]
+        if contiguous:
+            n = len(items)
+            queues = [list(range(wk * n // workers, (wk + 1) * n // workers))
+                      for wk in range(workers)]
+        else:
+            _, queues, _ = OP.lpt(ids, costs, workers)
+        q = [(ids[i], costs[i], wk, p) for wk, qq in enumerate(queues) for p, i in enumerate(qq)]
+        out.append(np.array(q, np.int64).reshape(-1, 4))
+    return out
+
+
+def check_queues(w, workers, flags=0):
+    kv = planned(w, workers, flags)
+    assert kv.stats().device_status == S.SPLITKV_OK
+    exp = expected_queues(w, workers, bool(flags & S.SPLITKV_FLAG_CONTIGUOUS))
+    for kind, e in zip((2, 3), exp):
+        s, gi, gc, gw, gp = S.splitkv_plan_export(kv.prob, kv.plan_ws, kind, len(e) + 5)
+        assert s == S.SPLITKV_OK
+        got = np.stack([gi, gc, gw.astype(np.int64), gp.astype(np.int64)], axis=1)
+        assert got.shape == e.shape, (kind, got.shape, e.shape)
+        assert np.array_equal(got, e), kind
+
+
+@pytest.mark.parametrize("contig", [False, True])
+@pytest.mark.parametrize("idx,sweep,workers", [
+    (0, 0, 152), (1, 0, 152), (3, 0, 152), (3, 1, 152), (3, 2, 152), (4, 0, 152), (4, 4, 152),
+    (0, 0, 5),
+])
+def test_executed_queues_bit_exact(idx, sweep, workers, contig):
+    """The queues the kernels walk, LPT or contiguous, match the CPU rule
+    entry by entry (item, cost, worker, position)."""
+    check_queues(W.config(idx, sweep), workers,
+                 S.SPLITKV_FLAG_CONTIGUOUS if contig else 0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_executed_contiguous_queues_fuzz(seed):
+    rng = np.random.default_rng(100 + seed)
+    S_ = int(rng.integers(1, 6))
+    B = int(rng.choice([1, 4, 8, 16]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    group = int(rng.choice([g for g in (1, 2, 4, 8) if 128 % (B * g) == 0]))
+    lengths = rng.integers(1, 3000, size=S_).tolist()
+    prompts = [int(rng.integers(0, max(1, L // 2))) for L in lengths]
+    counts = [int(rng.integers(0, max(1, min(40, L - B - P + 1)))) if L - B - P + 1 > 0 else 0
+              for L, P in zip(lengths, prompts)]
+    w = W.custom(100 + seed, lengths, prompts, counts, B=B, Hq=Hkv * group, Hkv=Hkv, d=64,
+                 chunk=int(rng.choice([128, 256, 512])))
+    workers = Hkv * int(rng.integers(1, 40))
+    check_queues(w, workers, S.SPLITKV_FLAG_CONTIGUOUS)
+    check_queues(w, workers, 0)
