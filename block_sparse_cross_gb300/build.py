@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsplitkv.so")
-SOURCES = ["api.cu", "plan.cu", "attn_simt.cu", "attn_tc.cu", "rows.cu", "noalloc.cu", "proj.cu", "selftest.cu"]
+SOURCES = ["api.cu", "plan.cu", "attn_simt.cu", "attn_tc.cu", "rows.cu", "draft.cu", "noalloc.cu", "proj.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -38,6 +38,17 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
                              const void* Q, const void* Kd, const void* Vd, const void* O,
                              const float* LSE, const void* dO, void* dKd, void* dVd,
                              int64_t nsl_cap, cudaStream_t st);
+// draft.cu — the draft-block products of the merge and of the backward
+// prologue as mma.sync tiles (bf16, B in {8, 16, 32}, 16 <= B * group <= 128);
+// launch_merge / launch_bwd_draft use them when draft_mma_supported(P).
+bool draft_mma_supported(const ProbDev& P);
+cudaError_t launch_merge_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                               const void* Q, const void* Kd, const void* Vd, void* O, float* LSE,
+                               cudaStream_t st);
+cudaError_t launch_bwd_draft_mma(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
+                                 const void* Q, const void* Kd, const void* Vd, const void* O,
+                                 const float* LSE, const void* dO, void* dKd, void* dVd,
+                                 cudaStream_t st);
 // Kernel launches launch_bwd_draft makes for this problem.
 int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap);
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,

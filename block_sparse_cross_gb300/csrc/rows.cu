@@ -692,6 +692,7 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
     constexpr int D = decltype(dtag)::value;
     const int64_t warps = P.NQ * P.Hq;
     if (warps == 0) return cudaSuccess;
+    if (draft_mma_supported(P)) return launch_merge_draft(P, pp, wk, Q, Kd, Vd, O, LSE, st);
     if (P.B <= kDraftBM) {
       const size_t smem = sizeof(float) * 2 * kDraftBM * D;
       merge_block_kernel<T, D><<<dim3((unsigned)P.NA, (unsigned)P.Hkv), 256, smem, st>>>(
@@ -706,7 +707,7 @@ cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& w
 
 int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap) {
   if (P.NQ * P.Hq == 0) return 0;
-  const bool fused = P.B <= kDraftBM && P.B * P.group <= kDraftRM;
+  const bool fused = draft_mma_supported(P) || (P.B <= kDraftBM && P.B * P.group <= kDraftRM);
   return (fused ? 1 : 2) + (nsl_cap > 0 ? 1 : 0);
 }
 
@@ -721,7 +722,10 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
     if (warps == 0) return cudaSuccess;
     cudaError_t err;
     dim3 grid((unsigned)P.NA, (unsigned)P.Hkv);
-    if (P.B <= kDraftBM && P.B * P.group <= kDraftRM) {
+    if (draft_mma_supported(P)) {
+      err = launch_bwd_draft_mma(P, pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, st);
+      if (err != cudaSuccess) return err;
+    } else if (P.B <= kDraftBM && P.B * P.group <= kDraftRM) {
       // one CTA per (draft block, kv head) does the whole draft-block backward
       const size_t smem = sizeof(float) * (2 * kDraftBM * D + 2 * kDraftRM * kDraftBM);
       auto k = bwd_draft_block_kernel<T, D>;
