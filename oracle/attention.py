@@ -28,6 +28,8 @@ variants are offered, selected by the workload's flags):
 
     inclusive       the context keys are 0 <= k <= a_j (a_j + 1 keys)
     causal block    query i of block j (row j*B + i) sees draft keys t <= i only
+    context offsets block j's context starts at its own offset o_j:
+                    o_j <= k < a_j (o_j <= k <= a_j when also inclusive)
 
 Every input holds exactly the values the device sees (the compute-dtype
 rounding happens before); slices are upcast to float64 before any
@@ -53,8 +55,16 @@ def _blocks(w) -> Iterable[Tuple[int, int, int]]:
 
 
 def _ctx_len(w, a: int) -> int:
-    """Number of context keys block with anchor a sees."""
+    """End (exclusive) of the context keys the block with anchor a sees."""
     return a + 1 if getattr(w, "mask_inclusive", False) else a
+
+
+def _ctx_range(w, j: int, a: int) -> Tuple[int, int]:
+    """[lo, hi) of the sample-local context keys block j sees."""
+    lo_arr = getattr(w, "ctx_lo", None)
+    lo = 0 if lo_arr is None else int(lo_arr[j])
+    hi = _ctx_len(w, a)
+    return lo, max(lo, hi)
 
 
 def _mask_draft(w, S: np.ndarray, n_ctx: int) -> np.ndarray:
@@ -92,11 +102,12 @@ def forward(w, Q, Kc, Vc, Kd, Vd, blocks=None, heads=None):
         if sel is not None and j not in sel:
             continue
         c0 = int(w.cu_ctx[s])
-        na = _ctx_len(w, a)
+        lo, hi = _ctx_range(w, j, a)
+        na = hi - lo
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + na, g], Kd[rows, g]], axis=0).astype(np.float64)
-            vals = np.concatenate([Vc[c0:c0 + na, g], Vd[rows, g]], axis=0).astype(np.float64)
+            keys = np.concatenate([Kc[c0 + lo:c0 + hi, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0 + lo:c0 + hi, g], Vd[rows, g]], axis=0).astype(np.float64)
             for h in hlist:
                 S = _mask_draft(w, scale * (Q[rows, h].astype(np.float64) @ keys.T), na)
                 lse = _logsumexp_rows(S)
@@ -124,11 +135,12 @@ def backward(w, Q, Kc, Vc, Kd, Vd, dO, blocks=None, heads=None):
         if sel is not None and j not in sel:
             continue
         c0 = int(w.cu_ctx[s])
-        na = _ctx_len(w, a)
+        lo, hi = _ctx_range(w, j, a)
+        na = hi - lo
         rows = slice(j * B, (j + 1) * B)
         for g, hlist in hs.items():
-            keys = np.concatenate([Kc[c0:c0 + na, g], Kd[rows, g]], axis=0).astype(np.float64)
-            vals = np.concatenate([Vc[c0:c0 + na, g], Vd[rows, g]], axis=0).astype(np.float64)
+            keys = np.concatenate([Kc[c0 + lo:c0 + hi, g], Kd[rows, g]], axis=0).astype(np.float64)
+            vals = np.concatenate([Vc[c0 + lo:c0 + hi, g], Vd[rows, g]], axis=0).astype(np.float64)
             dK = np.zeros_like(keys)
             dV = np.zeros_like(vals)
             for h in hlist:
@@ -144,8 +156,8 @@ def backward(w, Q, Kc, Vc, Kd, Vd, dO, blocks=None, heads=None):
                 dS = P * (dP - D[:, None])
                 dQ[rows, h] = scale * (dS @ keys)
                 dK += scale * (dS.T @ q)
-            dKc[c0:c0 + na, g] += dK[:na]
-            dVc[c0:c0 + na, g] += dV[:na]
+            dKc[c0 + lo:c0 + hi, g] += dK[:na]
+            dVc[c0 + lo:c0 + hi, g] += dV[:na]
             dKd[rows, g] += dK[na:]
             dVd[rows, g] += dV[na:]
     return {"dQ": dQ, "dKc": dKc, "dVc": dVc, "dKd": dKd, "dVd": dVd}
@@ -172,7 +184,8 @@ def partial_forward(w, Q, Kc, Vc, Kd, Vd, lo: int, hi: int, draft: bool):
             if draft:
                 keys, vals = Kd[rows, g], Vd[rows, g]
             else:
-                k0, k1 = max(lo, 0), min(hi, _ctx_len(w, a))
+                r_lo, r_hi = _ctx_range(w, j, a)
+                k0, k1 = max(lo, r_lo), min(hi, r_hi)
                 if k1 <= k0:
                     continue
                 keys, vals = Kc[c0 + k0:c0 + k1, g], Vc[c0 + k0:c0 + k1, g]

@@ -13,7 +13,10 @@ realized masked work of chunk [cs, cs + cl) of a sample is the number of
 
 (block j sees context keys [0, a_j), so it sees min(cl, a_j - cs) keys of
 the chunk, for each of its B query rows). With the inclusive mask variant
-(context [0, a_j]) the same formula runs on a_j + 1.
+(context [0, a_j]) the same formula runs on a_j + 1. With per-block context
+offsets o_j (block j sees [o_j, a_j)) each block contributes the overlap of
+its range with the chunk, max(0, min(cs + cl, a_j) - max(cs, o_j)) * B; with
+every o_j = 0 that is the formula above.
 
 Work items. The forward splits each chunk further by kv head g and by
 "slab" sigma: ``bps = 128 // (B * group)`` consecutive draft blocks of one
@@ -42,9 +45,18 @@ TILE_ROWS = 128   # (query, head) rows per forward work item
 KEY_TILE = 128    # keys per backward work item
 
 
-def chunk_cost(anchors: Sequence[int], cs: int, cl: int, B: int) -> int:
-    """Realized masked pairs of key range [cs, cs+cl) for the given anchors."""
-    return int(sum(min(cl, int(a) - cs) * B for a in anchors if int(a) > cs))
+def chunk_cost(anchors: Sequence[int], cs: int, cl: int, B: int,
+               starts: Sequence[int] = None) -> int:
+    """Realized masked pairs of key range [cs, cs+cl) for the given anchors
+    (ends of the visible context). With ``starts`` (per-block context
+    offsets) block j sees [starts[j], anchors[j]) instead of [0, anchors[j]),
+    and contributes the overlap of that range with the chunk."""
+    if starts is None:
+        return int(sum(min(cl, int(a) - cs) * B for a in anchors if int(a) > cs))
+    total = 0
+    for a, o in zip(anchors, starts):
+        total += max(0, min(cs + cl, int(a)) - max(cs, int(o))) * B
+    return int(total)
 
 
 def blocks_per_slab(w) -> int:
@@ -61,6 +73,15 @@ def _sample_anchors(w, s: int) -> np.ndarray:
     return anc + 1 if getattr(w, "mask_inclusive", False) else anc
 
 
+def _sample_starts(w, s: int):
+    """Start of the visible context of each block of sample s (None when the
+    mask has no per-block context offsets)."""
+    lo = getattr(w, "ctx_lo", None)
+    if lo is None:
+        return None
+    return np.asarray(lo[int(w.cu_anchor[s]):int(w.cu_anchor[s + 1])], np.int64)
+
+
 def fwd_items(w) -> List[Tuple[int, int, int, int, int, int]]:
     """(id, s, c, sigma, g, cost) for every forward item of positive cost."""
     bps = blocks_per_slab(w)
@@ -69,13 +90,15 @@ def fwd_items(w) -> List[Tuple[int, int, int, int, int, int]]:
     for s in range(w.num_samples):
         L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
         anc = _sample_anchors(w, s)
+        st = _sample_starts(w, s)
         nch = -(-L // w.chunk)
         nsl = -(-len(anc) // bps)
         for c in range(nch):
             cs = c * w.chunk
             cl = min(w.chunk, L - cs)
             for sg in range(nsl):
-                cost = chunk_cost(anc[sg * bps:(sg + 1) * bps], cs, cl, w.B)
+                cost = chunk_cost(anc[sg * bps:(sg + 1) * bps], cs, cl, w.B,
+                                  None if st is None else st[sg * bps:(sg + 1) * bps])
                 for g in range(w.Hkv):
                     if cost > 0:
                         out.append((nid, s, c, sg, g, cost))
@@ -90,9 +113,10 @@ def bwd_items(w) -> List[Tuple[int, int, int, int, int]]:
     for s in range(w.num_samples):
         L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
         anc = _sample_anchors(w, s)
+        st = _sample_starts(w, s)
         for kt in range(-(-L // KEY_TILE)):
             ks = kt * KEY_TILE
-            cost = chunk_cost(anc, ks, min(KEY_TILE, L - ks), w.B)
+            cost = chunk_cost(anc, ks, min(KEY_TILE, L - ks), w.B, st)
             for g in range(w.Hkv):
                 if cost > 0:
                     out.append((nid, s, kt, g, cost))

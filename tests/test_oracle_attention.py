@@ -8,8 +8,11 @@
   single-query textbook attention via scipy
 * invariants: exactness of any KV split merged by log-sum-exp (the property
   the Split-KV pages claim), strict prefix mask, GQA head map
-* the mask variants (inclusive context, causal draft block) through the same
-  brute-force, SDPA, finite-difference and split pins, plus their boundary keys
+* the mask variants (inclusive context, causal draft block, per-block context
+  offsets) through the same brute-force, SDPA, finite-difference and split
+  pins, plus their boundary keys and the special cases that reduce to the
+  plain mask (every offset 0) or to textbook attention over the draft keys
+  alone (every offset at the end of the context)
 """
 import json
 import math
@@ -47,13 +50,15 @@ def brute_force_forward(w, Q, Kc, Vc, Kd, Vd):
         j = n // w.B
         s = block_sample[j]
         a = int(w.anchors[j])
+        o = 0 if w.ctx_lo is None else int(w.ctx_lo[j])
         c0, c1 = int(w.cu_ctx[s]), int(w.cu_ctx[s + 1])
         for h in range(Hq):
             g = h // group
             scores, vals = [], []
             for t in range(T):                       # every context row
                 k = t - c0
-                visible = c0 <= t < c1 and (k <= a if w.mask_inclusive else k < a)
+                visible = (c0 <= t < c1 and (k <= a if w.mask_inclusive else k < a)
+                           and k >= o)
                 if visible:
                     scores.append(w.scale * sum(Q[n, h, x] * Kc[t, g, x] for x in range(d)))
                     vals.append(Vc[t, g])
@@ -81,7 +86,8 @@ def sdpa_reference(w, t):
         j = n // w.B
         s = block_sample[j]
         c0 = int(w.cu_ctx[s])
-        mask[n, c0:c0 + int(w.anchors[j]) + (1 if w.mask_inclusive else 0)] = True
+        o = 0 if w.ctx_lo is None else int(w.ctx_lo[j])
+        mask[n, c0 + o:c0 + int(w.anchors[j]) + (1 if w.mask_inclusive else 0)] = True
         for u in range(w.B):
             if not w.mask_causal_block or u <= n % w.B:
                 mask[n, T + j * w.B + u] = True
@@ -361,3 +367,121 @@ def test_causal_block_first_query_sees_one_draft_key():
     o2, _ = OA.forward(w, t2["Q"], t2["Kc"], t2["Vc"], t2["Kd"], t2["Vd"])
     assert np.array_equal(base[0], o2[0])       # query 0: unchanged
     assert np.abs(o2[3] - base[3]).max() > 1.0  # query 3 sees them
+
+
+# ---- per-block context offsets ---------------------------------------------
+OFFSET_MASKS = [(False, False), (True, False), (False, True), (True, True)]
+
+
+def offset_workload(seed, inclusive=False, causal=False, B=2, Hq=4, Hkv=2, d=5):
+    w = tiny_workload(seed=seed, B=B, Hq=Hq, Hkv=Hkv, d=d).with_mask(inclusive, causal)
+    return w.with_ctx_offsets(W.context_offsets(w, seed + 1000))
+
+
+@pytest.mark.parametrize("inclusive,causal", OFFSET_MASKS)
+def test_context_offsets_match_brute_force_loops(inclusive, causal):
+    w = offset_workload(41, inclusive, causal)
+    assert (w.ctx_lo > 0).any()
+    t = _f64(W.tensors(w))
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    Ob, LSEb = brute_force_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    np.testing.assert_allclose(O, Ob, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(LSE, LSEb, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("inclusive,causal", OFFSET_MASKS)
+def test_context_offsets_match_torch_sdpa(inclusive, causal):
+    w = offset_workload(43, inclusive, causal, B=3)
+    t = _f64(W.tensors(w))
+    ref = sdpa_reference(w, t)
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    g = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], t["dO"])
+    np.testing.assert_allclose(O, ref["O"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, ref["LSE"], rtol=0, atol=1e-12)
+    for k in ("dQ", "dKc", "dVc", "dKd", "dVd"):
+        np.testing.assert_allclose(g[k], ref[k], rtol=0, atol=1e-12, err_msg=k)
+
+
+def test_context_offsets_backward_matches_central_differences():
+    w0 = W.custom(47, lengths=[80], prompts=[30], counts=[3], B=4, Hq=2, Hkv=1, d=8, chunk=32)
+    lo = np.array([int(a) // 3 for a in w0.anchors], np.int32)
+    w = w0.with_ctx_offsets(lo)
+    t = _f64(W.tensors(w))
+    g = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], t["dO"])
+    rng = np.random.default_rng(5)
+    h = 1e-6
+
+    def loss(tt):
+        O, _ = OA.forward(w, tt["Q"], tt["Kc"], tt["Vc"], tt["Kd"], tt["Vd"])
+        return float((O * tt["dO"]).sum())
+
+    for name, gname in (("Q", "dQ"), ("Kc", "dKc"), ("Vc", "dVc"), ("Kd", "dKd"), ("Vd", "dVd")):
+        arr = t[name]
+        flat_idx = rng.choice(arr.size, size=10, replace=False)
+        if name in ("Kc", "Vc"):  # the offset rows (first visible) and the ones just before
+            flat_idx[:3] = [int(o) * w.d * w.Hkv for o in lo]
+            flat_idx[3:6] = [max(int(o) - 1, 0) * w.d * w.Hkv for o in lo]
+        for fi in flat_idx:
+            idx = np.unravel_index(fi, arr.shape)
+            tp = dict(t); tm = dict(t)
+            tp[name] = arr.copy(); tp[name][idx] += h
+            tm[name] = arr.copy(); tm[name][idx] -= h
+            fd = (loss(tp) - loss(tm)) / (2 * h)
+            assert abs(fd - g[gname][idx]) <= 1e-6 * max(1.0, abs(g[gname][idx])), (name, idx)
+
+
+@pytest.mark.parametrize("inclusive,causal", OFFSET_MASKS)
+def test_context_offsets_any_kv_split_merges_to_unsplit_result(inclusive, causal):
+    w0 = W.custom(150, lengths=[300, 170], prompts=[60, 20], counts=[5, 3], B=4, Hq=4, Hkv=2,
+                  d=8, chunk=64).with_mask(inclusive, causal)
+    w = w0.with_ctx_offsets(W.context_offsets(w0, 151))
+    t = _f64(W.tensors(w))
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    edges = [0, 37, 64, 128, 200, 300]
+    parts = [OA.partial_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], lo, hi, False)
+             for lo, hi in zip(edges[:-1], edges[1:])]
+    parts.append(OA.partial_forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], 0, 0, True))
+    Om, LSEm = OA.merge(parts)
+    np.testing.assert_allclose(Om, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSEm, LSE, rtol=0, atol=1e-12)
+
+
+def test_context_offset_key_is_the_first_visible_one():
+    w0 = W.custom(9, lengths=[50], prompts=[10], counts=[1], B=2, Hq=1, Hkv=1, d=4, chunk=16)
+    o = int(w0.anchors[0]) // 2
+    w = w0.with_ctx_offsets(np.array([o], np.int32))
+    t = _f64(W.tensors(w))
+    base, _ = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    t2 = {k: v.copy() for k, v in t.items()}
+    t2["Vc"][o - 1] = 1e6                       # last key before the offset: invisible
+    o2, _ = OA.forward(w, t2["Q"], t2["Kc"], t2["Vc"], t2["Kd"], t2["Vd"])
+    assert np.array_equal(base, o2)
+    t3 = {k: v.copy() for k, v in t.items()}
+    t3["Vc"][o] = 1e6                           # the offset key itself: visible
+    o3, _ = OA.forward(w, t3["Q"], t3["Kc"], t3["Vc"], t3["Kd"], t3["Vd"])
+    assert np.abs(o3 - base).max() > 1.0
+
+
+def test_zero_offsets_reduce_to_the_plain_mask():
+    w = tiny_workload(seed=53)
+    wz = w.with_ctx_offsets(np.zeros_like(w.anchors))
+    t = _f64(W.tensors(w))
+    a = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    b = OA.forward(wz, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_offset_at_the_context_end_leaves_textbook_attention_over_the_draft_keys():
+    w0 = W.custom(57, lengths=[60], prompts=[10], counts=[2], B=4, Hq=2, Hkv=1, d=6, chunk=16)
+    w = w0.with_ctx_offsets(w0.anchors.copy())   # o_j = a_j: no context key at all
+    t = _f64(W.tensors(w))
+    O, LSE = OA.forward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"])
+    for j in range(2):
+        rows = slice(4 * j, 4 * j + 4)
+        for h in range(2):
+            s = t["Q"][rows, h] @ t["Kd"][rows, 0].T * w.scale
+            np.testing.assert_allclose(O[rows, h], sps.softmax(s, axis=1) @ t["Vd"][rows, 0],
+                                       rtol=0, atol=1e-13)
+            np.testing.assert_allclose(LSE[h, rows], sps.logsumexp(s, axis=1), rtol=0, atol=1e-13)
+    g = OA.backward(w, t["Q"], t["Kc"], t["Vc"], t["Kd"], t["Vd"], t["dO"])
+    assert np.abs(g["dKc"]).max() == 0.0 and np.abs(g["dVc"]).max() == 0.0

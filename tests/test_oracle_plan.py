@@ -22,11 +22,13 @@ def brute_mask_count(w, s, k0, k1):
     """Count (row, key) pairs of sample s's mask with key in [k0, k1)."""
     B = w.B
     anc = w.anchors[w.cu_anchor[s]:w.cu_anchor[s + 1]]
+    los = (np.zeros(len(anc), np.int64) if w.ctx_lo is None
+           else w.ctx_lo[w.cu_anchor[s]:w.cu_anchor[s + 1]])
     L = int(w.cu_ctx[s + 1] - w.cu_ctx[s])
     mask = np.zeros((len(anc) * B, L), bool)
-    for j, a in enumerate(anc):
+    for j, (a, o) in enumerate(zip(anc, los)):
         for k in range(L):  # the set rule, key by key
-            if k < a or (w.mask_inclusive and k == a):
+            if (k < a or (w.mask_inclusive and k == a)) and k >= o:
                 mask[j * B:(j + 1) * B, k] = True
     return int(mask[:, k0:k1].sum())
 
@@ -156,3 +158,29 @@ def test_inclusive_items_equal_mask_count(seed):
         for kt, ks in enumerate(range(0, L, OP.KEY_TILE)):
             got = sum(it[-1] for it in bwd if it[1] == s and it[2] == kt)
             assert got == brute_mask_count(w, s, ks, min(L, ks + OP.KEY_TILE)) * w.Hkv
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("inclusive", [False, True])
+def test_chunk_cost_with_context_offsets_equals_mask_count(seed, inclusive):
+    rng = np.random.default_rng(50 + seed)
+    S = 3
+    lengths = rng.integers(40, 400, size=S).tolist()
+    prompts = [int(rng.integers(0, L // 2)) for L in lengths]
+    B = int(rng.choice([1, 2, 4, 8]))
+    counts = [int(rng.integers(0, max(1, min(12, L - B - P + 1)))) for L, P in zip(lengths, prompts)]
+    w0 = W.custom(50 + seed, lengths, prompts, counts, B=B, Hq=2, Hkv=1, d=4,
+                  chunk=int(rng.choice([16, 33, 64]))).with_mask(inclusive, False)
+    w = w0.with_ctx_offsets(W.context_offsets(w0, 60 + seed))
+    for s in range(S):
+        sl = slice(int(w.cu_anchor[s]), int(w.cu_anchor[s + 1]))
+        ends = w.anchors[sl].astype(np.int64) + (1 if inclusive else 0)
+        L = lengths[s]
+        for cs in range(0, L, w.chunk):
+            cl = min(w.chunk, L - cs)
+            got = OP.chunk_cost(ends, cs, cl, B, w.ctx_lo[sl])
+            assert got == brute_mask_count(w, s, cs, cs + cl)
+    # the items partition the masked pairs
+    total = sum(brute_mask_count(w, s, 0, lengths[s]) for s in range(S))
+    assert sum(it[-1] for it in OP.fwd_items(w)) == total * w.Hkv
+    assert sum(it[-1] for it in OP.bwd_items(w)) == total * w.Hkv

@@ -50,6 +50,10 @@ class Workload:
     # block (query i of a block sees draft keys t <= i)
     mask_inclusive: bool = False
     mask_causal_block: bool = False
+    # per-block context offsets: block j sees context keys from ctx_lo[j] on
+    # (sample-local, 0 <= ctx_lo[j] <= the end of its visible context);
+    # None = every block's context starts at key 0
+    ctx_lo: Optional[np.ndarray] = None
 
     @property
     def num_samples(self) -> int:
@@ -86,13 +90,31 @@ class Workload:
         return dataclasses.replace(self, name=self.name + tag, mask_inclusive=inclusive,
                                    mask_causal_block=causal_block)
 
+    def with_ctx_offsets(self, ctx_lo: np.ndarray, tag: str = "_off") -> "Workload":
+        """The same draw with per-block context offsets ``ctx_lo``."""
+        lo = np.asarray(ctx_lo, np.int32)
+        if lo.shape != self.anchors.shape:
+            raise ValueError("one offset per draft block")
+        return dataclasses.replace(self, name=self.name + tag, ctx_lo=lo)
+
+    def context_ends(self) -> np.ndarray:
+        """End (exclusive) of every block's visible context: a_j, or a_j + 1
+        when inclusive."""
+        return self.anchors.astype(np.int64) + (1 if self.mask_inclusive else 0)
+
+    def context_starts(self) -> np.ndarray:
+        """Start of every block's visible context (0 without offsets)."""
+        if self.ctx_lo is None:
+            return np.zeros(self.anchors.shape, np.int64)
+        return self.ctx_lo.astype(np.int64)
+
     def masked_pairs(self) -> int:
         """(query, key) pairs per query head: sum over blocks of B*(a_j + B)
-        (B*(a_j + 1) context pairs when inclusive, B*(B+1)/2 draft pairs when
-        causal within the block)."""
-        a = self.anchors.astype(np.int64) + (1 if self.mask_inclusive else 0)
+        (B*(a_j + 1) context pairs when inclusive, B*(a_j - o_j) with context
+        offsets, B*(B+1)/2 draft pairs when causal within the block)."""
+        ctx = np.maximum(self.context_ends() - self.context_starts(), 0)
         draft = self.B * (self.B + 1) // 2 if self.mask_causal_block else self.B * self.B
-        return int((self.B * a + draft).sum())
+        return int((self.B * ctx + draft).sum())
 
     def useful_flop(self, per_pair_per_dim: int = 14) -> int:
         """Useful FLOP of fwd+bwd: Hq * d * c * pairs (c=14: 4 fwd + 10 bwd)."""
@@ -285,6 +307,20 @@ def layer_tensors(w: Workload, hidden: Optional[int] = None, seed_offset: int = 
                np.float32(math.sqrt(w.Hq * w.d))),
         "dY": rng.standard_normal((nq, H), dtype=dtype),
     }
+
+
+def context_offsets(w: Workload, seed: int, window: Optional[int] = None) -> np.ndarray:
+    """Seeded per-block context offsets for the context-offset mask variant.
+
+    With ``window`` each block keeps the last ``window`` keys of its visible
+    context (o_j = max(0, end_j - window)); otherwise o_j is uniform on
+    [0, end_j] (the empty context end_j included), end_j = a_j (+1 when
+    inclusive)."""
+    ends = w.anchors.astype(np.int64) + (1 if w.mask_inclusive else 0)
+    if window is not None:
+        return np.maximum(ends - int(window), 0).astype(np.int32)
+    rng = _rng(seed)
+    return np.floor(rng.random(ends.shape) * (ends + 1)).astype(np.int32)
 
 
 def subset(w: Workload, n_heads: int, n_anchors: int, seed: int) -> tuple:
