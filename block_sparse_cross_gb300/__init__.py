@@ -44,6 +44,7 @@ SPLITKV_FLAG_CUDA_CORE = 1
 SPLITKV_FLAG_CONTIGUOUS = 2
 SPLITKV_FLAG_MASK_INCLUSIVE = 4
 SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
+SPLITKV_FLAG_MASK_CONTEXT_OFFSET = 16
 SPLITKV_NUM_KERNELS = 9
 SPLITKV_NOALLOC_SCRATCH_BYTES = 64 << 20
 (SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,
@@ -68,6 +69,7 @@ class splitkv_problem(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("num_workers", ctypes.c_int32),
         ("flags", ctypes.c_int32),
+        ("ctx_lo", ctypes.c_void_p),
     ]
 
 
@@ -309,8 +311,9 @@ def splitkv_selftest_wait_timeout(stream=None):
 class SplitKV:
     """One problem (metadata resident on the device) plus its workspaces.
 
-    cu_ctx / cu_anchor / anchors: int32 CUDA tensors; the host scalars are
-    taken from the caller (no device read). Allocates the two workspaces with
+    cu_ctx / cu_anchor / anchors (and ctx_lo, the per-block context offsets,
+    which select SPLITKV_FLAG_MASK_CONTEXT_OFFSET): int32 CUDA tensors; the
+    host scalars are taken from the caller (no device read). Allocates the two workspaces with
     torch once; ``plan()``, ``forward()`` and ``backward()`` then only enqueue
     kernels on the current torch stream.
     """
@@ -318,14 +321,17 @@ class SplitKV:
     def __init__(self, cu_ctx, cu_anchor, anchors, total_ctx: int, total_anchors: int,
                  max_ctx: int, B: int, Hq: int, Hkv: int, d: int, chunk: int,
                  scale: float, dtype: int = SPLITKV_BF16, num_workers: int = 0,
-                 flags: int = 0):
+                 flags: int = 0, ctx_lo=None):
         import torch
-        self._keep = (cu_ctx, cu_anchor, anchors)
+        self._keep = (cu_ctx, cu_anchor, anchors, ctx_lo)
+        if ctx_lo is not None:
+            flags |= SPLITKV_FLAG_MASK_CONTEXT_OFFSET
         self.prob = splitkv_problem(
             num_samples=int(cu_ctx.numel() - 1), cu_ctx=_ptr(cu_ctx), cu_anchor=_ptr(cu_anchor),
             anchors=_ptr(anchors) if anchors.numel() else None, total_ctx=int(total_ctx),
             total_anchors=int(total_anchors), max_ctx=int(max_ctx), B=B, Hq=Hq, Hkv=Hkv, d=d,
-            chunk=chunk, scale=float(scale), dtype=dtype, num_workers=num_workers, flags=flags)
+            chunk=chunk, scale=float(scale), dtype=dtype, num_workers=num_workers, flags=flags,
+            ctx_lo=_ptr(ctx_lo) if ctx_lo is not None and ctx_lo.numel() else None)
         st, self.plan_bytes, self.work_bytes = splitkv_workspace_size(self.prob)
         _check("splitkv_workspace_size", st)
         dev = cu_ctx.device

@@ -16,12 +16,15 @@ using namespace skv;
 namespace {
 
 constexpr int kKnownFlags = SPLITKV_FLAG_CUDA_CORE | SPLITKV_FLAG_CONTIGUOUS |
-                            SPLITKV_FLAG_MASK_INCLUSIVE | SPLITKV_FLAG_MASK_CAUSAL_BLOCK;
+                            SPLITKV_FLAG_MASK_INCLUSIVE | SPLITKV_FLAG_MASK_CAUSAL_BLOCK |
+                            SPLITKV_FLAG_MASK_CONTEXT_OFFSET;
 
 int check_problem(const splitkv_problem* p) {
   if (!p) return SPLITKV_EINVAL;
   if (p->num_samples < 1 || !p->cu_ctx || !p->cu_anchor) return SPLITKV_EINVAL;
   if (p->total_anchors > 0 && !p->anchors) return SPLITKV_EINVAL;
+  if ((p->flags & SPLITKV_FLAG_MASK_CONTEXT_OFFSET) && p->total_anchors > 0 && !p->ctx_lo)
+    return SPLITKV_EINVAL;
   if (p->total_ctx < 0 || p->total_anchors < 0 || p->max_ctx < 0) return SPLITKV_EINVAL;
   if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->chunk < 1 || p->num_workers < 0)
     return SPLITKV_EINVAL;
@@ -92,7 +95,7 @@ uint64_t problem_hash(const splitkv_problem* p, int m) {
   mix(p->B); mix(p->Hq); mix(p->Hkv); mix(p->d); mix(p->chunk); mix(p->dtype);
   mix(m); mix(sbits);
   mix(p->flags & (SPLITKV_FLAG_CONTIGUOUS | SPLITKV_FLAG_MASK_INCLUSIVE |
-                  SPLITKV_FLAG_MASK_CAUSAL_BLOCK));
+                  SPLITKV_FLAG_MASK_CAUSAL_BLOCK | SPLITKV_FLAG_MASK_CONTEXT_OFFSET));
   return h;
 }
 
@@ -120,6 +123,8 @@ ProbDev make_dev(const splitkv_problem* p, int m) {
   P.cu_anchor = p->cu_anchor;
   P.anchors = p->anchors;      // replaced by the plan's a_j + 1 table when inclusive
   P.anchors_in = p->anchors;
+  P.ctx_lo = nullptr;          // the plan's table (set up in setup())
+  P.ctx_lo_in = (p->flags & SPLITKV_FLAG_MASK_CONTEXT_OFFSET) ? p->ctx_lo : nullptr;
   return P;
 }
 
@@ -154,6 +159,7 @@ int setup(const splitkv_problem* p, const void* plan_ws, Ctx* c) {
   // every kernel after the planner's validation reads the end of each
   // block's visible context from P.anchors
   if (p->flags & SPLITKV_FLAG_MASK_INCLUSIVE) c->P.anchors = c->pp.anchor_end;
+  c->P.ctx_lo = c->pp.anchor_lo;  // the start of every block's context (0 without offsets)
   return SPLITKV_OK;
 }
 
@@ -438,7 +444,8 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
   if (prob->total_ctx > 0) {
-    e = timed(SPLITKV_K_ZERO, 1, s, [&] { return launch_zero_uncovered(c.P, c.pp, dKc, dVc, s); });
+    e = timed(SPLITKV_K_ZERO, 1, s,
+              [&] { return launch_zero_uncovered(c.P, c.pp, c.caps.NCB, dKc, dVc, s); });
     if (e != cudaSuccess) return SPLITKV_ECUDA;
   }
   if (!any_q) return SPLITKV_OK;

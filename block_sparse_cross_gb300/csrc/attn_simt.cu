@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
       }
       __syncthreads();
       const int nt = min(kSimtKeys, min(ke, ri.anchor) - kb);
-      for (int t = 0; t < nt; ++t) {
+      for (int t = max(0, ri.lo - kb); t < nt; ++t) {  // keys [lo, end) of the row
         float sdot = 0.f;
 #pragma unroll
         for (int x = 0; x < D; ++x) sdot = fmaf(qT[x * kRows + r], ks[t * D + x], sdot);
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
       }
       __syncthreads();
       const int nt = min(kSimtKeys, min(ke, ri.anchor) - kb);
-      for (int t = 0; t < nt; ++t) {
+      for (int t = max(0, ri.lo - kb); t < nt; ++t) {  // keys [lo, end) of the row
         float sdot = 0.f, dp = 0.f;
 #pragma unroll
         for (int x = 0; x < D; ++x) {
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
   float* lse_s = dos + kRowBatch * RS; // [kRowBatch]
   float* d_s = lse_s + kRowBatch;      // [kRowBatch]
   int* anc_s = (int*)(d_s + kRowBatch);// [kRowBatch]
+  int* lo_s = anc_s + kRowBatch;       // [kRowBatch]
   if (!plan_ok_cta(P, pp.hdr)) return;
   if (threadIdx.x == 0) stamp_busy(P, pp, 2, 0);
   const int w = blockIdx.x;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
             lse_s[rr] = ri.n >= 0 ? LSE[(size_t)ri.h * P.NQ + ri.n] : 0.f;
             d_s[rr] = ri.n >= 0 ? wk.dvec[(size_t)ri.h * P.NQ + ri.n] : 0.f;
             anc_s[rr] = ri.anchor;
+            lo_s[rr] = ri.lo;
           }
         }
         __syncthreads();
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
           }
           ps += __shfl_xor_sync(0xffffffffu, ps, 1);
           pd += __shfl_xor_sync(0xffffffffu, pd, 1);
-          const float p = key < anc_s[rr] ? expf(ps * P.scale - lse_s[rr]) : 0.f;
+          const float p =
+              (key < anc_s[rr] && key >= lo_s[rr]) ? expf(ps * P.scale - lse_s[rr]) : 0.f;
           const float ds = p * (pd - d_s[rr]);
 #pragma unroll
           for (int x = 0; x < HD; ++x) {
@@ -354,7 +357,7 @@ cudaError_t launch_bwd_dkdv_simt(const ProbDev& P, const PlanPtrs& pp, const Wor
     constexpr int HD = D / 2;
     auto k = bwd_dkdv_simt_kernel<T, D>;
     const size_t smem =
-        sizeof(float) * (2 * D * kRows + 2 * kRowBatch * 2 * (HD + 1) + 3 * kRowBatch);
+        sizeof(float) * (2 * D * kRows + 2 * kRowBatch * 2 * (HD + 1) + 4 * kRowBatch);
     cudaError_t err = set_smem(k, smem);
     if (err != cudaSuccess) return err;
     k<<<P.workers, 256, smem, st>>>(P, pp, wk, (const T*)Q, (const T*)Kc, (const T*)Vc,

@@ -82,12 +82,13 @@ __device__ __forceinline__ RowInfo row_info_early(const ProbDev& P, const FwdRec
   const int per_blk = P.B * P.group;
   const int b = r / per_blk;
   if (b >= I.nblk) {
-    ri.n = -1; ri.h = 0; ri.anchor = 0;
+    ri.n = -1; ri.h = 0; ri.anchor = 0; ri.lo = 0;
     return ri;
   }
   ri.n = (I.first + b) * P.B + (r / P.group) % P.B;
   ri.h = I.g * P.group + r % P.group;
   ri.anchor = ld_int_early(P.anchors + I.first + b);
+  ri.lo = ld_int_early(P.ctx_lo + I.first + b);
   return ri;
 }
 
@@ -415,17 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = ns & 1;
         if (!(ok = warp_wait(s_full + sb, (ns >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        // padding rows (beyond the slab's blocks) compute on whatever Q rows the
-        // tile box holds; their partials are never read
-        const int lim = (ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile)) -
-                        64 * hf;
+        // the row sees keys [llo, lim) of this half (padding rows, beyond the
+        // slab's blocks, compute on whatever Q rows the tile box holds; their
+        // partials are never read)
+        const int kt0 = I.cs + t * kKeyTile;
+        const int lim = (ri.n < 0 ? kKeyTile : min(max(ri.anchor - kt0, 0), kKeyTile)) - 64 * hf;
+        const int llo = (ri.n < 0 ? 0 : min(max(ri.lo - kt0, 0), kKeyTile)) - 64 * hf;
         const uint32_t sa = tS + lane_base + sb * 128 + 64 * hf;
         uint32_t x[64];  // raw scores of this half row (masked entries -> -inf)
         tmem_ld_row<64>(sa, x);
-        if (!__all_sync(0xffffffffu, lim >= 64)) {
+        if (!__all_sync(0xffffffffu, lim >= 64 && llo <= 0)) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (i >= lim) x[i] = __float_as_uint(-INFINITY);
+            if (i >= lim || i < llo) x[i] = __float_as_uint(-INFINITY);
         }
         // row max of this half: eight chains of three-input maxima
         float mx[8];
@@ -875,8 +878,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         if (!(ok = warp_wait(s_full, gt & 1, abort_flag))) break;
         tc_fence_after();
-        const int lim =
-            (ri.n < 0 ? kKeyTile : min(max(ri.anchor - (I.cs + t * kKeyTile), 0), kKeyTile)) - 64 * hf;
+        const int kt0 = I.cs + t * kKeyTile;
+        const int lim = (ri.n < 0 ? kKeyTile : min(max(ri.anchor - kt0, 0), kKeyTile)) - 64 * hf;
+        const int llo = (ri.n < 0 ? 0 : min(max(ri.lo - kt0, 0), kKeyTile)) - 64 * hf;
         // S, then dP, then dS of this tile: region gt % 2, this half's columns
         const uint32_t sa = tmem + 128 * (gt & 1) + lane_base + 64 * hf;
         const uint32_t pa = sa;
@@ -889,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();  // S is in registers: dP may overwrite it
           __syncwarp();
           if (lane == 0) mbar_arrive(s_read);
-          if (__all_sync(0xffffffffu, lim >= 64)) {
+          if (__all_sync(0xffffffffu, lim >= 64 && llo <= 0)) {
             const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2x2 = f2_pack(nl2, nl2);
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
@@ -902,8 +906,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-              const float p0 = (i < lim) ? ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)) : 0.f;
-              const float p1 = (i + 1 < lim) ? ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2)) : 0.f;
+              const float p0 =
+                  (i < lim && i >= llo) ? ex2(fmaf(__uint_as_float(sv[i]), sl2, nl2)) : 0.f;
+              const float p1 = (i + 1 < lim && i + 1 >= llo)
+                                   ? ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, nl2))
+                                   : 0.f;
               pk[i / 2] = pack_bf16(p0, p1);
             }
           }
@@ -1203,6 +1210,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     const int r = wq * 32 + lane;  // key of the tile owned by this thread
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
+    // with per-block context offsets every element is checked against its
+    // row's [lo, end); otherwise a key below the slab's first anchor is seen
+    // by every row
+    const bool offsets = (P.flags & SPLITKV_FLAG_MASK_CONTEXT_OFFSET) != 0;
     uint32_t nst = 0, nit = 0;
     bool ok = true;
     KvItem In = q0 < q1 ? ld_brec(pp.b_rec + q0) : KvItem{};
@@ -1221,7 +1232,8 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
         const float* nl2 = (const float*)(sb + Lay::info_off) + 64 * hf;  // -LSE*log2(e)
         const float* dvv = nl2 + kRows;
-        const int* anc = (const int*)(dvv + kRows);
+        const int* anc = (const int*)(dvv + kRows);   // end of each row's visible context
+        const int* alo = anc + kRows;                 // start of each row's visible context
         const int* anc0 = anc - 64 * hf;  // the slab's first row: its smallest anchor
         // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs.
         // Rows are ordered by block and anchors rise with the block, so a key
@@ -1231,7 +1243,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         {
           uint32_t sv[64];
           tmem_ld_row<64>(tS + lane_base + 64 * hf, sv);
-          if (__all_sync(0xffffffffu, key < anc0[0])) {
+          if (!offsets && __all_sync(0xffffffffu, key < anc0[0])) {
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t* nl2x2 = (const uint64_t*)nl2;  // (row c, row c + 1) pairs
 #pragma unroll
@@ -1245,9 +1257,12 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
           } else {
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
-              const float p0 = key < anc[c] ? ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c])) : 0.f;
-              const float p1 =
-                  key < anc[c + 1] ? ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1])) : 0.f;
+              const float p0 = (key < anc[c] && key >= alo[c])
+                                   ? ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c]))
+                                   : 0.f;
+              const float p1 = (key < anc[c + 1] && key >= alo[c + 1])
+                                   ? ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nl2[c + 1]))
+                                   : 0.f;
               pk[c / 2] = pack_bf16(p0, p1);
             }
           }

@@ -100,7 +100,8 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* ws, T* total) {
 struct RowInfo {
   int n;        // global query index, or -1 if the row is padding
   int h;        // query head
-  int anchor;   // anchor of the row's block (0 for padding rows)
+  int anchor;   // end of the row's visible context (0 for padding rows)
+  int lo;       // start of the row's visible context (0 for padding rows)
 };
 
 __device__ __forceinline__ RowInfo row_info(const ProbDev& P, int first_block, int nblk, int g,
@@ -109,7 +110,7 @@ __device__ __forceinline__ RowInfo row_info(const ProbDev& P, int first_block, i
   const int per_blk = P.B * P.group;
   const int b = r / per_blk;
   if (b >= nblk) {
-    ri.n = -1; ri.h = 0; ri.anchor = 0;
+    ri.n = -1; ri.h = 0; ri.anchor = 0; ri.lo = 0;
     return ri;
   }
   const int qi = (r / P.group) % P.B;
@@ -117,6 +118,7 @@ __device__ __forceinline__ RowInfo row_info(const ProbDev& P, int first_block, i
   ri.n = (first_block + b) * P.B + qi;
   ri.h = g * P.group + hg;
   ri.anchor = P.anchors[first_block + b];
+  ri.lo = P.ctx_lo[first_block + b];
   return ri;
 }
 

@@ -297,14 +297,16 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
   const int lj = j - P.cu_anchor[s];
   const int slab = pp.s_slab_off[s] + lj / P.bps;
   const int rbase = (lj % P.bps) * R;
+  // the block sees chunks [c_lo, nact) (none when its context [lo, end) is empty)
   const int nact = (P.anchors[j] + P.chunk - 1) / P.chunk;
+  const int c_lo = P.ctx_lo[j] >= P.anchors[j] ? nact : P.ctx_lo[j] / P.chunk;
   const size_t slot0 = (size_t)pp.sl_slot[slab];
   const size_t cstride = (size_t)P.Hkv * kRows;  // between chunks of a row
   const size_t ostride = cstride * D;
   const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + rbase;
   const float* pbase = wk.part_o + ((slot0 * P.Hkv + g) * kRows + rbase) * D + lane * EPL;
   const int x0 = lane * EPL;
-  auto load_lse = [&](int r, int cb) -> float {
+  auto load_lse = [&](int r, int cb) -> float {  // chunk cb + lane (absolute index)
     return cb + lane < nact ? plse[(size_t)(cb + lane) * cstride + r] * kLog2eD : -INFINITY;
   };
   auto load_rows = [&](int r, int c0, float (&v)[U][EPL]) {
@@ -323,9 +325,9 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
   };
   float nl = -INFINITY, nv[U][EPL];
   int r = warp;
-  if (r < R && nact > 0) {
-    nl = load_lse(r, 0);
-    load_rows(r, 0, nv);
+  if (r < R && nact > c_lo) {
+    nl = load_lse(r, c_lo);
+    load_rows(r, c_lo, nv);
   }
   for (; r < R; r += nw) {
     float lc = nl, v[U][EPL];
@@ -333,9 +335,9 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int i = 0; i < EPL; ++i) v[u][i] = nv[u][i];
-    if (r + nw < R && nact > 0) {  // the next row's first loads land while this row merges
-      nl = load_lse(r + nw, 0);
-      load_rows(r + nw, 0, nv);
+    if (r + nw < R && nact > c_lo) {  // the next row's first loads land while this row merges
+      nl = load_lse(r + nw, c_lo);
+      load_rows(r + nw, c_lo, nv);
     }
     float accr[EPL];
     {
@@ -349,9 +351,9 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
       }
     }
     float Mr = lsed[r], Sr = 1.f;  // the draft partial: weight 1 at its own lse
-    for (int cb = 0; cb < nact; cb += 32) {
+    for (int cb = c_lo; cb < nact; cb += 32) {
       const int nc = min(32, nact - cb);
-      if (cb > 0) {
+      if (cb > c_lo) {
         lc = load_lse(r, cb);
         load_rows(r, cb, v);
       }

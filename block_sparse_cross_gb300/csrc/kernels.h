@@ -53,8 +53,9 @@ cudaError_t launch_bwd_draft_mma(const ProbDev& P, const PlanPtrs& pp, const Wor
 int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap);
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
                              cudaStream_t st);
-cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,
-                                  cudaStream_t st);
+// ncb_cap: the host bound on backward candidates (sample, key tile)
+cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, int64_t ncb_cap,
+                                  void* dKc, void* dVc, cudaStream_t st);
 
 // proj.cu — grouped tcgen05 GEMM of the drafter layer's projections.
 constexpr int kProjMaxParts = 3, kProjMaxSegs = 3, kProjMaxDst = 3;

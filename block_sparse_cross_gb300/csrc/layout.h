@@ -117,6 +117,9 @@ struct PlanPtrs {
   int64_t* b_load_contig;
   // [NA] a_j + 1 (end of the visible context) when the mask is inclusive
   int32_t* anchor_end;
+  // [NA] start of every block's visible context: the caller's offset o_j
+  // with SPLITKV_FLAG_MASK_CONTEXT_OFFSET, else 0
+  int32_t* anchor_lo;
   // [3][workers][2] %globaltimer (ns) at the start and the end of every
   // worker's CTA in the latest forward, dQ and dK/dV attention launch
   uint64_t* busy_ns;
@@ -171,6 +174,7 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   q.b_load_lpt = (int64_t*)take(8 * c.M);
   q.b_load_contig = (int64_t*)take(8 * c.M);
   q.anchor_end = (int32_t*)take(4 * (c.NA + 1));
+  q.anchor_lo = (int32_t*)take(4 * (c.NA + 1));
   q.busy_ns = (uint64_t*)take(16 * 3 * c.M);
   if (p) *p = q;
   return align_up(off, 256);
@@ -187,10 +191,11 @@ struct WorkPtrs {
   float* dvec;
   float* draft_p;    // [N_q][Hq][B] softmax weight of each draft key
   float* draft_ds;   // [N_q][Hq][B] dS of each draft key
-  float* rowinfo;    // [slab][Hkv][3][128]: -LSE*log2(e) (-inf on padding rows), D, anchor bits
+  float* rowinfo;    // [slab][Hkv][4][128]: -LSE*log2(e) (-inf on padding rows), D, and the
+                     // row's visible context [lo, end) as int bits
 };
 
-constexpr int kRowInfoFloats = 3 * kRows;  // one (slab, kv head) record: 1536 bytes
+constexpr int kRowInfoFloats = 4 * kRows;  // one (slab, kv head) record: 2048 bytes
 
 inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int64_t B,
                           int64_t slabs_x_hkv, char* base, WorkPtrs* p) {
@@ -225,6 +230,8 @@ struct ProbDev {
   const int32_t* cu_anchor;
   const int32_t* anchors;     // end of each block's visible context (a_j, or a_j + 1)
   const int32_t* anchors_in;  // the caller's anchors (validated by the planner)
+  const int32_t* ctx_lo;      // start of each block's visible context (the plan's table)
+  const int32_t* ctx_lo_in;   // the caller's offsets (SPLITKV_FLAG_MASK_CONTEXT_OFFSET)
 };
 
 }  // namespace skv

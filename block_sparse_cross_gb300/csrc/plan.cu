@@ -27,34 +27,46 @@ namespace skv {
 
 namespace {
 
+// Cost of forward item (sample s, chunk c, slab sigma): the masked pairs of
+// the slab's blocks in the chunk, sum over blocks of the overlap of their
+// visible context [lo_j, end_j) with the chunk, times B. *ks_out / *ke_out:
+// the first and the end of the keys any block of the slab sees in the chunk
+// (the kernels compute the 128-key tiles covering [*ks_out, *ke_out)).
 __device__ __forceinline__ int64_t fwd_item_cost(const ProbDev& P, int s, int c, int sigma,
-                                                 int* ke_out) {
+                                                 int* ks_out, int* ke_out) {
   const int c0 = P.cu_ctx[s];
   const int L = P.cu_ctx[s + 1] - c0;
   const int a0 = P.cu_anchor[s];
   const int A = P.cu_anchor[s + 1] - a0;
   const int cs = c * P.chunk;
-  const int cl = min(P.chunk, L - cs);
+  const int ce = cs + min(P.chunk, L - cs);
   const int first = a0 + sigma * P.bps;
   const int nblk = min(P.bps, A - sigma * P.bps);
   int64_t cost = 0;
-  int amax = 0;
+  int ks = ce, ke = cs;
   for (int b = 0; b < nblk; ++b) {
-    const int a = P.anchors[first + b];
-    amax = max(amax, a);
-    if (a > cs) cost += (int64_t)min(cl, a - cs) * P.B;
+    const int lo = max(cs, P.ctx_lo[first + b]);
+    const int hi = min(ce, P.anchors[first + b]);
+    if (hi > lo) {
+      cost += (int64_t)(hi - lo) * P.B;
+      ks = min(ks, lo);
+      ke = max(ke, hi);
+    }
   }
-  *ke_out = min(cs + cl, amax);
+  *ks_out = ks;
+  *ke_out = ke;
   return cost;
 }
 
+// Cost of backward item (sample s, 128-key tile kt): the masked pairs of all
+// of the sample's blocks in the tile.
 __device__ __forceinline__ int64_t bwd_item_cost(const ProbDev& P, int s, int kt) {
   const int c0 = P.cu_ctx[s];
   const int L = P.cu_ctx[s + 1] - c0;
   const int a0 = P.cu_anchor[s];
   const int a1 = P.cu_anchor[s + 1];
   const int ks = kt * kKeyTile;
-  const int tl = min(kKeyTile, L - ks);
+  const int ke = ks + min(kKeyTile, L - ks);
   // first anchor > ks (anchors are non-decreasing within the sample)
   int lo = a0, hi = a1;
   while (lo < hi) {
@@ -62,7 +74,10 @@ __device__ __forceinline__ int64_t bwd_item_cost(const ProbDev& P, int s, int kt
     if (P.anchors[mid] > ks) hi = mid; else lo = mid + 1;
   }
   int64_t cost = 0;
-  for (int j = lo; j < a1; ++j) cost += (int64_t)min(tl, P.anchors[j] - ks) * P.B;
+  for (int j = lo; j < a1; ++j) {
+    const int v = min(ke, P.anchors[j]) - max(ks, P.ctx_lo[j]);
+    if (v > 0) cost += (int64_t)v * P.B;
+  }
   return cost;
 }
 
@@ -131,7 +146,12 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
     if (i + 1 < P.NA && i + 1 < P.cu_anchor[s + 1] && P.anchors_in[i + 1] < a)
       latch(H, SPLITKV_EMETA);
     // inclusive context [0, a_j]: every later step works with its end a_j + 1
-    if (P.flags & SPLITKV_FLAG_MASK_INCLUSIVE) pp.anchor_end[i] = a + 1;
+    const int end = (P.flags & SPLITKV_FLAG_MASK_INCLUSIVE) ? a + 1 : a;
+    if (P.flags & SPLITKV_FLAG_MASK_INCLUSIVE) pp.anchor_end[i] = end;
+    // the start of the block's visible context: its offset, or 0
+    const int lo = P.ctx_lo_in ? P.ctx_lo_in[i] : 0;
+    if (lo < 0 || lo > end) latch(H, SPLITKV_EMETA);
+    pp.anchor_lo[i] = lo;
   }
   __syncthreads();
   if (read_status(H) != 0) return;
@@ -185,10 +205,13 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
     const int local = id - pp.s_cand_off[s];
     const int nsl = pp.s_nsl[s];
     const int c = local / nsl, sigma = local % nsl;
-    int ke;
-    const int64_t cost = fwd_item_cost(P, s, c, sigma, &ke);
+    int ks, ke;
+    const int64_t cost = fwd_item_cost(P, s, c, sigma, &ks, &ke);
     pp.f_cost[id] = cost;
-    if (cost > 0) my_tiles += (unsigned long long)((ke - c * P.chunk + kKeyTile - 1) / kKeyTile);
+    if (cost > 0) {  // tiles from the one holding the first seen key to the last seen key
+      const int t0 = (ks - c * P.chunk) / kKeyTile;
+      my_tiles += (unsigned long long)((ke - c * P.chunk - t0 * kKeyTile + kKeyTile - 1) / kKeyTile);
+    }
   }
   for (int o = 16; o > 0; o >>= 1) my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
   if ((tid & 31) == 0 && my_tiles) atomicAdd(&tiles_acc, my_tiles);
@@ -385,16 +408,18 @@ __device__ __forceinline__ QEntry decode_fwd(const ProbDev& P, const PlanPtrs& p
   return e;
 }
 
-// The decoded form of forward entry e (see FwdRec): the chunk's tiles end at
-// the slab's last visible key (its largest anchor end) or the chunk end.
+// The decoded form of forward entry e (see FwdRec): the 128-key tiles of
+// the chunk from the one holding the first key any block of the slab sees to
+// the last such key; cs / row0 name the first computed tile.
 __device__ __forceinline__ FwdRec fwd_rec(const ProbDev& P, const PlanPtrs& pp, const QEntry& e) {
   FwdRec R;
   R.first = pp.sl_first[e.slab];
   R.nblk = pp.sl_nblk[e.slab];
-  const int c0 = P.cu_ctx[e.s], L = P.cu_ctx[e.s + 1] - c0;
-  const int amax = P.anchors[R.first + R.nblk - 1];
-  R.cs = e.c * P.chunk;
-  const int ke = min(min(R.cs + P.chunk, L), amax);
+  const int c0 = P.cu_ctx[e.s];
+  int ks, ke;
+  fwd_item_cost(P, e.s, e.c, e.slab - pp.s_slab_off[e.s], &ks, &ke);
+  const int t0 = (ks - e.c * P.chunk) / kKeyTile;
+  R.cs = e.c * P.chunk + t0 * kKeyTile;
   R.ntiles = (ke - R.cs + kKeyTile - 1) / kKeyTile;
   R.row0 = c0 + R.cs;
   R.n0 = R.first * P.B;

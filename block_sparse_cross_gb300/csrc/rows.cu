@@ -30,7 +30,8 @@ struct RowGeom {
   int slab;     // global slab index
   int r;        // row inside the slab's 128-row item
   int anchor;
-  int nact;     // chunks whose keys the row sees: ceil(anchor / C)
+  int c_lo;     // chunks whose keys the row sees: [c_lo, nact), empty when its
+  int nact;     // visible context [lo, anchor) is (nact = ceil(anchor / C))
 };
 
 __device__ __forceinline__ RowGeom row_geom(const ProbDev& P, const PlanPtrs& pp, int n, int h) {
@@ -43,6 +44,8 @@ __device__ __forceinline__ RowGeom row_geom(const ProbDev& P, const PlanPtrs& pp
   G.r = (b * P.B + qi) * P.group + (h % P.group);
   G.anchor = P.anchors[j];
   G.nact = (G.anchor + P.chunk - 1) / P.chunk;
+  const int lo = P.ctx_lo[j];
+  G.c_lo = lo >= G.anchor ? G.nact : lo / P.chunk;
   return G;
 }
 
@@ -224,7 +227,7 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
   float Mr = -INFINITY, Sr = 0.f;
-  for (int cb = 0; cb < G.nact; cb += 32) {
+  for (int cb = G.c_lo; cb < G.nact; cb += 32) {
     const int nc = min(32, G.nact - cb);
     const float lc = lane < nc ? plse[(cb + lane) * cstride] : -INFINITY;
     float v[U][EPL];
@@ -619,6 +622,7 @@ __global__ void __launch_bounds__(128) slab_rowinfo_kernel(ProbDev P, PlanPtrs p
     rec[kRows + r] = 0.f;
   }
   ((int*)rec)[2 * kRows + r] = ri.anchor;
+  ((int*)rec)[3 * kRows + r] = ri.lo;
 }
 
 template <typename T, int D>
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
 #pragma unroll 4
-  for (int c = 0; c < G.nact; ++c) {
+  for (int c = G.c_lo; c < G.nact; ++c) {
     const float* po = wk.part_o + (((slot0 + c) * P.Hkv + g) * kRows + G.r) * D + x0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[i] += po[i];
@@ -649,25 +653,27 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
   st_vec<T, EPL>(dQ + ((size_t)n * P.Hq + h) * D + x0, acc);
 }
 
-// Rows of sample s at local index >= 128 * ceil(a_last / 128) are in no
-// backward item (no block sees them); their key/value gradients are zero.
+// Key tiles that no block sees (backward candidates of cost 0: past a
+// sample's last visible key, every tile of a sample without anchors, and
+// with per-block context offsets any tile outside every block's range) are
+// in no backward item; their key/value gradients are zero. CTA x takes
+// candidates x, x + gridDim.x, ...; the rows of a tile are written with
+// 16-byte stores.
 template <typename T>
 __global__ void zero_uncovered_kernel(ProbDev P, PlanPtrs pp, T* __restrict__ dKc,
                                       T* __restrict__ dVc) {
-  // CTA (x, y) takes samples y, y + gridDim.y, ...: the rows of sample s
-  // from the end of its last visible key's tile to the sample's end, in
-  // 16-byte stores, strided over the x CTAs
   if (read_status(pp.hdr) != 0) return;
+  const int ncand = pp.hdr->n_bwd_cand;
   const size_t row16 = (size_t)P.Hkv * P.d * sizeof(T) / 16;  // d in {64, 128}: whole 16 B units
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (int s = blockIdx.y; s < P.S; s += gridDim.y) {
+  for (int cand = blockIdx.x; cand < ncand; cand += gridDim.x) {
+    if (pp.b_cost[cand] != 0) continue;
+    const int s = seg_of(pp.s_bcand_off, P.S, cand);
+    const int kt = cand - pp.s_bcand_off[s];
     const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
-    const int a0 = P.cu_anchor[s], a1 = P.cu_anchor[s + 1];
-    const int alast = a1 > a0 ? P.anchors[a1 - 1] : 0;
-    const int covered = min(L, (alast + kKeyTile - 1) / kKeyTile * kKeyTile);
-    const size_t lo = (size_t)(c0 + covered) * row16, hi = (size_t)(c0 + L) * row16;
-    for (size_t i = lo + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi;
-         i += (size_t)gridDim.x * blockDim.x) {
+    const int k0 = kt * kKeyTile, k1 = min(L, k0 + kKeyTile);
+    const size_t lo = (size_t)(c0 + k0) * row16, hi = (size_t)(c0 + k1) * row16;
+    for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
       ((uint4*)dKc)[i] = z;
       ((uint4*)dVc)[i] = z;
     }
@@ -763,11 +769,10 @@ cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
   });
 }
 
-cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, void* dKc, void* dVc,
-                                  cudaStream_t st) {
-  if (P.T == 0) return cudaSuccess;
-  const int ys = P.S < 2048 ? P.S : 2048;
-  const dim3 grid((unsigned)(2048 / ys < 64 ? 2048 / ys : 64), (unsigned)ys);
+cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, int64_t ncb_cap,
+                                  void* dKc, void* dVc, cudaStream_t st) {
+  if (P.T == 0 || ncb_cap == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)(ncb_cap < 4096 ? ncb_cap : 4096);
   if (P.dtype == SPLITKV_FP32)
     zero_uncovered_kernel<float><<<grid, 256, 0, st>>>(P, pp, (float*)dKc, (float*)dVc);
   else

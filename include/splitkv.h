@@ -91,9 +91,15 @@ enum {
    * MASK_INCLUSIVE: block j sees context keys [0, a_j] instead of [0, a_j)
    *   (chunk costs, tile skipping and masks all use a_j + 1);
    * MASK_CAUSAL_BLOCK: query i of a block sees its draft keys t <= i only,
-   *   instead of all B. The flags may be combined. */
+   *   instead of all B;
+   * MASK_CONTEXT_OFFSET: block j's context starts at its own offset
+   *   o_j = ctx_lo[j] (sample-local): it sees context keys [o_j, a_j)
+   *   ([o_j, a_j] with MASK_INCLUSIVE) instead of [0, a_j). Chunk costs, tile
+   *   skipping, masks, the merge and the zeroing of unseen keys all use the
+   *   range. The flags may be combined. */
   SPLITKV_FLAG_MASK_INCLUSIVE = 4,
-  SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
+  SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8,
+  SPLITKV_FLAG_MASK_CONTEXT_OFFSET = 16
 };
 
 /*
@@ -121,6 +127,12 @@ enum {
  *                count rounded down to a multiple of Hkv. Must be a multiple
  *                of Hkv and at most 256 * Hkv (and at most 4096).
  *  flags         SPLITKV_FLAG_* bits.
+ *  ctx_lo        int32 [total_anchors] device, read only with
+ *                SPLITKV_FLAG_MASK_CONTEXT_OFFSET (may be NULL otherwise):
+ *                start of each block's visible context, sample-local,
+ *                0 <= ctx_lo[j] <= the end of its context (a_j, or a_j + 1
+ *                when inclusive; equal to it = no context key). Validated on
+ *                the device (SPLITKV_EMETA).
  *
  * Supported set: 128 % (B * group) == 0 (a work item is 128 (query, head)
  * rows = 128 / (B*group) whole draft blocks), d in {64, 128}, dtype bf16 or
@@ -143,6 +155,7 @@ typedef struct splitkv_problem {
   int32_t dtype;
   int32_t num_workers;
   int32_t flags;
+  const int32_t* ctx_lo;
 } splitkv_problem;
 
 /* Plan statistics (host struct filled by splitkv_plan_stats). Costs are in

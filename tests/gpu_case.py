@@ -66,10 +66,12 @@ class Case:
         self.cu_ctx = torch.from_numpy(w.cu_ctx.astype(np.int32)).cuda()
         self.cu_anchor = torch.from_numpy(w.cu_anchor.astype(np.int32)).cuda()
         self.anchors = torch.from_numpy(w.anchors.astype(np.int32)).cuda()
+        self.ctx_lo = (None if w.ctx_lo is None
+                       else torch.from_numpy(w.ctx_lo.astype(np.int32)).cuda())
         self.kv = S.SplitKV(self.cu_ctx, self.cu_anchor, self.anchors, w.total_ctx,
                             w.total_anchors, w.max_ctx, w.B, w.Hq, w.Hkv, w.d, w.chunk, w.scale,
                             S.SPLITKV_BF16 if dtype == "bf16" else S.SPLITKV_FP32,
-                            num_workers=num_workers, flags=flags)
+                            num_workers=num_workers, flags=flags, ctx_lo=self.ctx_lo)
         # both workspaces replaced by poisoned, guarded buffers of the same size
         self.g_plan = Guarded((self.kv.plan_bytes,), torch.uint8)
         self.g_work = Guarded((self.kv.work_bytes,), torch.uint8)

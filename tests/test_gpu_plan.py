@@ -15,8 +15,10 @@ def planned(w, workers, flags=0):
     cu_ctx = torch.from_numpy(w.cu_ctx.astype(np.int32)).cuda()
     cu_anchor = torch.from_numpy(w.cu_anchor.astype(np.int32)).cuda()
     anchors = torch.from_numpy(w.anchors.astype(np.int32)).cuda()
+    ctx_lo = None if w.ctx_lo is None else torch.from_numpy(w.ctx_lo.astype(np.int32)).cuda()
     kv = S.SplitKV(cu_ctx, cu_anchor, anchors, w.total_ctx, w.total_anchors, w.max_ctx, w.B,
-                   w.Hq, w.Hkv, w.d, w.chunk, w.scale, num_workers=workers, flags=flags)
+                   w.Hq, w.Hkv, w.d, w.chunk, w.scale, num_workers=workers, flags=flags,
+                   ctx_lo=ctx_lo)
     kv.plan()
     return kv
 
