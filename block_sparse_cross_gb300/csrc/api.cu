@@ -470,7 +470,8 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
     if (e != cudaSuccess) return SPLITKV_ECUDA;
   }
   return cuda_status(
-      timed(SPLITKV_K_DQ_REDUCE, 1, s, [&] { return launch_dq_reduce(c.P, c.pp, wk, dQ, s); }));
+      timed(SPLITKV_K_DQ_REDUCE, 1, s,
+            [&] { return launch_dq_reduce(c.P, c.pp, wk, dQ, c.caps.NSL, s); }));
 }
 
 int splitkv_device_status(const splitkv_problem* prob, const void* plan_ws, int* status,

@@ -91,12 +91,11 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
       }
     }
     const size_t slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
-    float* po = wk.part_o + (slot * kRows + r) * D;
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int x = 0; x < D; x += 4)
-      *(float4*)(po + x) = make_float4(acc[x] * inv, acc[x + 1] * inv, acc[x + 2] * inv,
-                                       acc[x + 3] * inv);
+      *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
+          make_float4(acc[x] * inv, acc[x + 1] * inv, acc[x + 2] * inv, acc[x + 3] * inv);
     wk.part_lse[slot * kRows + r] = l > 0.f ? m + logf(l) : -INFINITY;
   }
   __syncthreads();
@@ -175,10 +174,10 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
       }
     }
     const size_t slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
-    float* po = wk.part_o + (slot * kRows + r) * D;
 #pragma unroll
     for (int x = 0; x < D; x += 4)
-      *(float4*)(po + x) = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+      *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
+          make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
   }
   __syncthreads();
   if (threadIdx.x == 0) stamp_busy(P, pp, 1, 1);

@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = lm[r] * w0 + lm[128 + r] * w1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float f0 = w0 * inv, f1 = w1 * inv;
-      float* po = wk.part_o + ((size_t)I.slot * kRows + r) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {  // 32 columns of each half at a time (register budget)
         uint32_t v0[32], v1[32];
@@ -379,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             o[k] = fmaf(__uint_as_float(v0[i + k]), f0, __uint_as_float(v1[i + k]) * f1);
-          st_global_v8(po + 32 * c + i, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+          st_global_v8(wk.part_o + part_off(I.slot, r, 32 * c + i, D), o[0], o[1], o[2], o[3],
+                       o[4], o[5], o[6], o[7]);
         }
       }
       wk.part_lse[(size_t)I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
@@ -793,7 +793,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto write_dq = [&](const FwdItem& I, uint32_t it) -> bool {
       if (!warp_wait(dq_done, it & 1, abort_flag)) return false;
       tc_fence_after();
-      float* po = wk.part_o + ((size_t)I.slot * kRows + r) * D;
 #pragma unroll 1
       for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
         uint32_t v[64];
@@ -805,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < 64; i += 8)
-          st_global_v8(po + 64 * h + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+          st_global_v8(wk.part_o + part_off(I.slot, r, 64 * h + i, D), __uint_as_float(v[i]),
+                       __uint_as_float(v[i + 1]),
                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]),
                        __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
                        __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));

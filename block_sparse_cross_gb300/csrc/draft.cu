@@ -59,6 +59,14 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Eight consecutive floats (32-byte aligned) in one 256-bit load.
+__device__ __forceinline__ void ld_global_v8(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -185,14 +193,13 @@ __device__ __forceinline__ void tile_times_rows(float (&acc)[D / 8][4], const ui
 // partial data in flight while the previous row is combined): the exact
 // log-sum-exp merge, starting from the draft partial, chunks ascending.
 template <int D, int NT>
-__global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+__global__ void __launch_bounds__(512) merge_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                           const __nv_bfloat16* __restrict__ Q,
                                                           const __nv_bfloat16* __restrict__ Kd,
                                                           const __nv_bfloat16* __restrict__ Vd,
                                                           __nv_bfloat16* __restrict__ O,
                                                           float* __restrict__ LSE) {
-  constexpr int EPL = D / 32;  // head dims per lane in phase 2
-  constexpr int U = 8;         // partial rows per load batch
+  constexpr int kGroups = D / 32;  // 8-dim groups per thread in phase 2 (4 threads per row)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   if (read_status(pp.hdr) != 0) return;
   const int G = P.group, R = P.B * G;
@@ -209,7 +216,6 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
   float* lsed = (float*)(smem_raw + v_off + sizeof(__nv_bfloat16) * geo.B16 * geo.ld_row);  // [R]
   const int j = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = blockDim.x >> 5;
   const int gr = lane >> 2, tq = lane & 3;
   stage_rows<D>(Qs, geo.ld_row, Q, j * P.B, g * G, G, P.Hq, R);
   stage_keys<D>(Ks, geo.ld_row, Kd, j * P.B, g, P.Hkv, P.B, geo.B16);
@@ -221,11 +227,12 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
   // normalised result goes to Od, which aliases the staged tiles, so each
   // half is written only after every warp has read them.
   const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
-  const int w = warp;  // R / 16 warps: one tile each
+  const int w = warp;  // warps 0 .. R/16 - 1 take one 16-row tile each
+  const bool tile_warp = w < R / 16;
   const int r_lo = 16 * w + gr, r_hi = r_lo + 8;
   uint32_t a[NT / 2][4];  // P as the A operand, 16 draft keys per k step
-  float il_lo, il_hi;
-  {
+  float il_lo = 0.f, il_hi = 0.f;
+  if (tile_warp) {
     float sc[NT][4];
     tile_scores<D, NT>(sc, Qs, Ks, geo.ld_row, w, lane);
     const int qi_lo = r_lo / G, qi_hi = r_hi / G;
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
     }
   }
   __syncthreads();  // every warp has its scores: Od may overwrite Qs / Ks
-  {
+  if (tile_warp) {
     constexpr int H = D / 2;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
@@ -283,16 +290,20 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
         for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
       tile_times_rows<H, NT / 2>(acc, a, Vs + hh * H, geo.ld_row, lane);
 #pragma unroll
-      for (int n = 0; n < H / 8; ++n) {
-        const int col = hh * H + 8 * n + 2 * tq;
-        *(float2*)(Od + r_lo * D + col) = make_float2(acc[n][0] * il_lo, acc[n][1] * il_lo);
-        *(float2*)(Od + r_hi * D + col) = make_float2(acc[n][2] * il_hi, acc[n][3] * il_hi);
+      for (int n = 0; n < H / 8; ++n) {  // Od is [D/8][R][8], like a partial slot
+        const int k = hh * (H / 8) + n;
+        *(float2*)(Od + (k * R + r_lo) * 8 + 2 * tq) =
+            make_float2(acc[n][0] * il_lo, acc[n][1] * il_lo);
+        *(float2*)(Od + (k * R + r_hi) * 8 + 2 * tq) =
+            make_float2(acc[n][2] * il_hi, acc[n][3] * il_hi);
       }
     }
   }
   __syncthreads();
 
-  // ---- phase 2: merge, one warp per row ----
+  // ---- phase 2: merge, four threads per row (thread t: row t % R, 8-dim
+  // groups t / R + 4i), so that a warp reads 32 consecutive rows of a group,
+  // 1 KB contiguous, per load ----
   const int s = seg_of(P.cu_anchor, P.S, j);
   const int lj = j - P.cu_anchor[s];
   const int slab = pp.s_slab_off[s] + lj / P.bps;
@@ -303,92 +314,50 @@ __global__ void __launch_bounds__(256) merge_draft_kernel(ProbDev P, PlanPtrs pp
   const size_t slot0 = (size_t)pp.sl_slot[slab];
   const size_t cstride = (size_t)P.Hkv * kRows;  // between chunks of a row
   const size_t ostride = cstride * D;
-  const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + rbase;
-  const float* pbase = wk.part_o + ((slot0 * P.Hkv + g) * kRows + rbase) * D + lane * EPL;
-  const int x0 = lane * EPL;
-  auto load_lse = [&](int r, int cb) -> float {  // chunk cb + lane (absolute index)
-    return cb + lane < nact ? plse[(size_t)(cb + lane) * cstride + r] * kLog2eD : -INFINITY;
-  };
-  auto load_rows = [&](int r, int c0, float (&v)[U][EPL]) {
+  const int r = threadIdx.x % R, q = threadIdx.x / R;
+  const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + rbase + r;
+  const float* prow = wk.part_o + part_off(slot0 * P.Hkv + g, rbase + r, 8 * q, D);
+  // pass A: the row's largest lse (log2 units), the draft partial's included
+  const float ld = lsed[r];
+  float M = ld;
+#pragma unroll 4
+  for (int c = c_lo; c < nact; ++c) M = fmaxf(M, plse[(size_t)c * cstride] * kLog2eD);
+  // pass B: O = (2^(ld - M) O_d + sum_c 2^(lse_c - M) O_c) / T, chunks ascending
+  float acc[kGroups][8];
+  float T = exp2f(ld - M);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = min(c0 + u, nact - 1);  // rows past nact are clamped, weight 0
-      const float* p = pbase + (size_t)c * ostride + (size_t)r * D;
-      if constexpr (EPL == 4) {
-        const float4 t = *(const float4*)p;
-        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-      } else {
-        const float2 t = *(const float2*)p;
-        v[u][0] = t.x; v[u][1] = t.y;
-      }
-    }
-  };
-  float nl = -INFINITY, nv[U][EPL];
-  int r = warp;
-  if (r < R && nact > c_lo) {
-    nl = load_lse(r, c_lo);
-    load_rows(r, c_lo, nv);
+  for (int i = 0; i < kGroups; ++i) {
+    const float* od = Od + ((q + 4 * i) * R + r) * 8;
+    const float4 a = *(const float4*)od, b = *(const float4*)(od + 4);
+    acc[i][0] = a.x * T; acc[i][1] = a.y * T; acc[i][2] = a.z * T; acc[i][3] = a.w * T;
+    acc[i][4] = b.x * T; acc[i][5] = b.y * T; acc[i][6] = b.z * T; acc[i][7] = b.w * T;
   }
-  for (; r < R; r += nw) {
-    float lc = nl, v[U][EPL];
+#pragma unroll 2
+  for (int c = c_lo; c < nact; ++c) {
+    const float w = exp2f(plse[(size_t)c * cstride] * kLog2eD - M);
+    T += w;
+    const float* pc = prow + (size_t)c * ostride;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int i = 0; i < kGroups; ++i) {
+      float v[8];
+      ld_global_v8(pc + (size_t)(4 * i) * kRows * 8, v);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) v[u][i] = nv[u][i];
-    if (r + nw < R && nact > c_lo) {  // the next row's first loads land while this row merges
-      nl = load_lse(r + nw, c_lo);
-      load_rows(r + nw, c_lo, nv);
+      for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(w, v[e], acc[i][e]);
     }
-    float accr[EPL];
-    {
-      const float4* od = (const float4*)(Od + r * D + x0);
-      if constexpr (EPL == 4) {
-        const float4 t = *od;
-        accr[0] = t.x; accr[1] = t.y; accr[2] = t.z; accr[3] = t.w;
-      } else {
-        const float2 t = *(const float2*)od;
-        accr[0] = t.x; accr[1] = t.y;
-      }
-    }
-    float Mr = lsed[r], Sr = 1.f;  // the draft partial: weight 1 at its own lse
-    for (int cb = c_lo; cb < nact; cb += 32) {
-      const int nc = min(32, nact - cb);
-      if (cb > c_lo) {
-        lc = load_lse(r, cb);
-        load_rows(r, cb, v);
-      }
-      const float Mn = fmaxf(Mr, warp_max(lc));
-      const float f = exp2f(Mr - Mn);
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) accr[i] *= f;
-      const float e = exp2f(lc - Mn);  // this lane's chunk weight (0 past nact)
-      Sr = Sr * f + warp_sum(e);
-      Mr = Mn;
-      for (int c0 = 0; c0 < nc; c0 += U) {
-        if (c0 > 0) load_rows(r, cb + c0, v);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const float wgt = __shfl_sync(0xffffffffu, e, min(c0 + u, 31));
-          if (c0 + u < nc) {
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) accr[i] = fmaf(wgt, v[u][i], accr[i]);
-          }
-        }
-      }
-    }
-    const float inv = 1.f / Sr;
-    const int n = j * P.B + r / G, h = g * G + r % G;
-    __nv_bfloat16* o = O + ((size_t)n * P.Hq + h) * D + x0;
-    if constexpr (EPL == 4) {
-      uint2 pk;
-      pk.x = pack2(accr[0] * inv, accr[1] * inv);
-      pk.y = pack2(accr[2] * inv, accr[3] * inv);
-      *(uint2*)o = pk;
-    } else {
-      *(uint32_t*)o = pack2(accr[0] * inv, accr[1] * inv);
-    }
-    if (lane == 0) LSE[(size_t)h * P.NQ + n] = (Mr + log2f(Sr)) * kLn2D;
   }
+  const float inv = 1.f / T;
+  const int n = j * P.B + r / G, h = g * G + r % G;
+  __nv_bfloat16* o = O + ((size_t)n * P.Hq + h) * D + 8 * q;
+#pragma unroll
+  for (int i = 0; i < kGroups; ++i) {
+    uint4 pk;
+    pk.x = pack2(acc[i][0] * inv, acc[i][1] * inv);
+    pk.y = pack2(acc[i][2] * inv, acc[i][3] * inv);
+    pk.z = pack2(acc[i][4] * inv, acc[i][5] * inv);
+    pk.w = pack2(acc[i][6] * inv, acc[i][7] * inv);
+    *(uint4*)(o + 32 * i) = pk;
+  }
+  if (q == 0) LSE[(size_t)h * P.NQ + n] = (M + log2f(T)) * kLn2D;
 }
 
 // ===========================================================================
@@ -583,7 +552,7 @@ cudaError_t launch_merge_draft(const ProbDev& P, const PlanPtrs& pp, const WorkP
     auto k = merge_draft_kernel<D, NT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<dim3((unsigned)P.NA, (unsigned)P.Hkv), 32 * (R / 16), smem, st>>>(
+    k<<<dim3((unsigned)P.NA, (unsigned)P.Hkv), 4 * R, smem, st>>>(
         P, pp, wk, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)Kd, (const __nv_bfloat16*)Vd,
         (__nv_bfloat16*)O, LSE);
     return cudaGetLastError();

@@ -51,8 +51,9 @@ cudaError_t launch_bwd_draft_mma(const ProbDev& P, const PlanPtrs& pp, const Wor
                                  cudaStream_t st);
 // Kernel launches launch_bwd_draft makes for this problem.
 int bwd_draft_launches(const ProbDev& P, int64_t nsl_cap);
+// nsl_cap: the host bound on slabs (the grid covers every slab and kv head)
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
-                             cudaStream_t st);
+                             int64_t nsl_cap, cudaStream_t st);
 // ncb_cap: the host bound on backward candidates (sample, key tile)
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, int64_t ncb_cap,
                                   void* dKc, void* dVc, cudaStream_t st);

@@ -180,8 +180,8 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
   return align_up(off, 256);
 }
 
-// Work workspace: partial O (or dQ) [slots][128][d] fp32, partial lse
-// [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32, the
+// Work workspace: partial O (or dQ) [slots][d/8][128][8] fp32 (part_off),
+// partial lse [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32, the
 // backward row term D [Hq][N_q] fp32, the draft-key P / dS [N_q][Hq][B] and
 // the per-(slab, kv head) row table the dK/dV kernel streams with each slab.
 struct WorkPtrs {
@@ -196,6 +196,14 @@ struct WorkPtrs {
 };
 
 constexpr int kRowInfoFloats = 4 * kRows;  // one (slab, kv head) record: 2048 bytes
+
+// Offset (in floats) of element (row r, dim x) of partial slot `slot` in
+// part_o. A slot's 128 rows x D fp32 are stored as [D/8][128][8]: the eight
+// consecutive dims of a row that a 32-byte store writes form one sector, and
+// the 32 rows of a warp writing the same 8-dim group fill 1 KB contiguously.
+__host__ __device__ inline size_t part_off(size_t slot, int r, int x, int D) {
+  return slot * (size_t)kRows * D + ((size_t)(x >> 3) * kRows + r) * 8 + (x & 7);
+}
 
 inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int64_t B,
                           int64_t slabs_x_hkv, char* base, WorkPtrs* p) {

@@ -60,6 +60,22 @@ __device__ __forceinline__ void st_vec(T* p, const float* v) {
   for (int i = 0; i < EPL; ++i) st_f(p + i, v[i]);
 }
 
+// Eight consecutive outputs in one store (16 bytes of bf16, or 2 x 16 bytes
+// of fp32); p aligned accordingly.
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 u;
+  __nv_bfloat162 t;
+  t = __floats2bfloat162_rn(v[0], v[1]); u.x = *(uint32_t*)&t;
+  t = __floats2bfloat162_rn(v[2], v[3]); u.y = *(uint32_t*)&t;
+  t = __floats2bfloat162_rn(v[4], v[5]); u.z = *(uint32_t*)&t;
+  t = __floats2bfloat162_rn(v[6], v[7]); u.w = *(uint32_t*)&t;
+  *(uint4*)p = u;
+}
+__device__ __forceinline__ void st8(float* p, const float (&v)[8]) {
+  *(float4*)p = make_float4(v[0], v[1], v[2], v[3]);
+  *(float4*)(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -206,8 +222,8 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
   const size_t slot0 = (size_t)pp.sl_slot[G.slab];
   const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + G.r;  // chunk c at c * Hkv * 128
   const size_t cstride = (size_t)P.Hkv * kRows;
-  const float* pbase = wk.part_o + (slot0 * P.Hkv + g) * kRows * D + (size_t)G.r * D + x0;
-  const size_t ostride = cstride * D;
+  const float* pbase = wk.part_o + part_off(slot0 * P.Hkv + g, G.r, x0, D);
+  const size_t ostride = cstride * D;  // between chunks of the row
   constexpr int U = 8;
   auto load_rows = [&](int cb, int c0, int nc, float (&v)[U][EPL]) {
 #pragma unroll
@@ -625,32 +641,53 @@ __global__ void __launch_bounds__(128) slab_rowinfo_kernel(ProbDev P, PlanPtrs p
   ((int*)rec)[3 * kRows + r] = ri.lo;
 }
 
+// dQ = scale * (sum of the row's chunk partials in ascending chunk order +
+// its draft term), one CTA per (slab, kv head, half of the slab's 128-row
+// tile): four threads per row (thread t: row 64 z + t % 64, 8-dim groups
+// t / 64 + 4i), so that a warp reads 32 consecutive rows of one group, 1 KB
+// contiguous, from each partial slot.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                         T* __restrict__ dQ) {
-  constexpr int EPL = D / 32;
+  constexpr int kGroups = D / 32;
   if (read_status(pp.hdr) != 0) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (wid >= P.NQ * P.Hq) return;
-  const int n = (int)(wid / P.Hq), h = (int)(wid % P.Hq);
-  const int g = h / P.group;
-  const RowGeom G = row_geom(P, pp, n, h);
-  const int x0 = lane * EPL;
-  const size_t slot0 = (size_t)pp.sl_slot[G.slab];
-  float acc[EPL];
+  const int sg = blockIdx.x, g = blockIdx.y;
+  if (sg >= pp.hdr->n_slabs) return;
+  const int r = 64 * blockIdx.z + threadIdx.x % 64, q = threadIdx.x / 64;
+  const RowInfo ri = row_info(P, pp.sl_first[sg], pp.sl_nblk[sg], g, r);
+  if (ri.n < 0) return;  // padding row of the slab's tile
+  const int nact = (ri.anchor + P.chunk - 1) / P.chunk;
+  const int c_lo = ri.lo >= ri.anchor ? nact : ri.lo / P.chunk;
+  const size_t slot0 = (size_t)pp.sl_slot[sg];
+  const float* prow = wk.part_o + part_off(slot0 * P.Hkv + g, r, 8 * q, D);
+  const size_t ostride = (size_t)P.Hkv * kRows * D;  // between chunks of the row
+  float acc[kGroups][8];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int c = G.c_lo; c < G.nact; ++c) {
-    const float* po = wk.part_o + (((slot0 + c) * P.Hkv + g) * kRows + G.r) * D + x0;
+  for (int i = 0; i < kGroups; ++i)
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) acc[i] += po[i];
+    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+#pragma unroll 2
+  for (int c = c_lo; c < nact; ++c) {
+    const float* pc = prow + (size_t)c * ostride;
+#pragma unroll
+    for (int i = 0; i < kGroups; ++i) {
+      const float4 a = *(const float4*)(pc + (size_t)(4 * i) * kRows * 8);
+      const float4 b = *(const float4*)(pc + (size_t)(4 * i) * kRows * 8 + 4);
+      acc[i][0] += a.x; acc[i][1] += a.y; acc[i][2] += a.z; acc[i][3] += a.w;
+      acc[i][4] += b.x; acc[i][5] += b.y; acc[i][6] += b.z; acc[i][7] += b.w;
+    }
   }
-  const float* dd = wk.dq_draft + ((size_t)n * P.Hq + h) * D + x0;
+  const size_t row = ((size_t)ri.n * P.Hq + ri.h) * D + 8 * q;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) acc[i] = (acc[i] + dd[i]) * P.scale;
-  st_vec<T, EPL>(dQ + ((size_t)n * P.Hq + h) * D + x0, acc);
+  for (int i = 0; i < kGroups; ++i) {
+    const float* dd = wk.dq_draft + row + 32 * i;
+    const float4 a = *(const float4*)dd, b = *(const float4*)(dd + 4);
+    float v[8] = {(acc[i][0] + a.x) * P.scale, (acc[i][1] + a.y) * P.scale,
+                  (acc[i][2] + a.z) * P.scale, (acc[i][3] + a.w) * P.scale,
+                  (acc[i][4] + b.x) * P.scale, (acc[i][5] + b.y) * P.scale,
+                  (acc[i][6] + b.z) * P.scale, (acc[i][7] + b.w) * P.scale};
+    st8(dQ + row + 32 * i, v);
+  }
 }
 
 // Key tiles that no block sees (backward candidates of cost 0: past a
@@ -758,13 +795,13 @@ cudaError_t launch_bwd_draft(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
 }
 
 cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk, void* dQ,
-                             cudaStream_t st) {
+                             int64_t nsl_cap, cudaStream_t st) {
   return dispatch(P, [&](auto tag, auto dtag) -> cudaError_t {
     using T = decltype(tag);
     constexpr int D = decltype(dtag)::value;
-    const int64_t warps = P.NQ * P.Hq;
-    if (warps == 0) return cudaSuccess;
-    dq_reduce_kernel<T, D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(P, pp, wk, (T*)dQ);
+    if (P.NQ * P.Hq == 0 || nsl_cap == 0) return cudaSuccess;
+    dq_reduce_kernel<T, D><<<dim3((unsigned)nsl_cap, (unsigned)P.Hkv, 2), 256, 0, st>>>(
+        P, pp, wk, (T*)dQ);
     return cudaGetLastError();
   });
 }
