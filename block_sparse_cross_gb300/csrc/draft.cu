@@ -193,7 +193,7 @@ __device__ __forceinline__ void tile_times_rows(float (&acc)[D / 8][4], const ui
 // partial data in flight while the previous row is combined): the exact
 // log-sum-exp merge, starting from the draft partial, chunks ascending.
 template <int D, int NT>
-__global__ void __launch_bounds__(512) merge_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
+__global__ void __launch_bounds__(512, 2) merge_draft_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                           const __nv_bfloat16* __restrict__ Q,
                                                           const __nv_bfloat16* __restrict__ Kd,
                                                           const __nv_bfloat16* __restrict__ Vd,

@@ -294,8 +294,21 @@ namespace {
 
 // Greedy LPT over the worker groups for one direction, run by one warp.
 // Lane l owns groups l, l+32, ... (at most kMaxGroupsPerLane each).
+//
+// Runs of equal cost (most items are whole chunks of full slabs, so most
+// share one cost) are dealt in one step. Write group g's load as
+// base + q_g c + rho_g (base = the least load, 0 <= rho_g < c): its i-th
+// next item would be picked at load base + (q_g + i) c + rho_g, so LPT's
+// picks for k items of cost c go level by level (level j: every group with
+// q_g <= j still taking items), and inside a level by (rho_g, g) — the
+// least-loaded-first, lowest-id-on-ties order, the same in every level. The
+// run's last level J and each group's count follow from counting, and the
+// item of run rank t goes to the slot of rank t in that order: exactly the
+// one-at-a-time greedy result, without its serial chain.
+constexpr int kLptBatch = 48;  // shorter runs go one item at a time
+
 __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32_t* pos,
-                         int64_t* gload, int32_t* gcount) {
+                         int64_t* gload, int32_t* gcount, int32_t* scratch) {
   const int lane = threadIdx.x & 31;
   // Fast path: one group per lane and 32-bit keys. While items are dealt
   // most expensive first to the least-loaded group, max load - min load
@@ -303,36 +316,104 @@ __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32
   // fits 32 bits when that cost is < 2^26, and a single warp min-reduction
   // finds the least-loaded group with the lowest id.
   if (G <= 32 && (n == 0 || scost[0] < (1LL << 26))) {
-    // rel = this lane's load minus the running minimum (< 2^26), so every
-    // step is 32-bit and branch-free: the group that takes item t is the
-    // warp-uniform minimum m & 31; lane t keeps item t's (group, position)
-    // and stores them once per 32 items.
+    // rel = this lane's load minus the running minimum base (< 2^26)
     uint32_t rel = 0;
     int64_t base = 0;
     int32_t cnt = 0;
-    for (int r0 = 0; r0 < n; r0 += 32) {
-      const int32_t mine = (r0 + lane < n) ? (int32_t)scost[r0 + lane] : 0;
-      const int lim = min(32, n - r0);
-      int32_t my_grp = 0, my_pos = 0;
-      for (int t = 0; t < lim; ++t) {
-        const uint32_t c = (uint32_t)__shfl_sync(0xffffffffu, mine, t);
-        const uint32_t key = lane < G ? (rel << 5) | (uint32_t)lane : 0xffffffffu;
-        const uint32_t m = __reduce_min_sync(0xffffffffu, key);
-        const int gsel = (int)(m & 31u);
-        const bool take = gsel == lane;
-        const int32_t p = __shfl_sync(0xffffffffu, cnt, gsel);
-        if (lane == t) {
-          my_grp = gsel;
-          my_pos = p;
+    int32_t* s_q = scratch;        // [32] per group: q_g, take_g, (rho, g) rank
+    int32_t* s_take = scratch + 32;
+    int32_t* s_ord = scratch + 64;
+    int r = 0;
+    while (r < n) {
+      const int64_t c64 = scost[r];  // the same address in every lane
+      int e = r + 1;                  // end of the run of items of cost c64
+      for (;;) {
+        const int i = e + lane;
+        const unsigned diff = __ballot_sync(0xffffffffu, i >= n || scost[i] != c64);
+        if (diff) {
+          e += __ffs(diff) - 1;
+          break;
         }
-        rel = rel - (m >> 5) + (take ? c : 0u);
-        cnt += take ? 1 : 0;
-        base += (int64_t)(m >> 5);
+        e += 32;
       }
-      if (lane < lim) {
-        grp[r0 + lane] = my_grp;
-        pos[r0 + lane] = my_pos;
+      const uint32_t c = (uint32_t)c64;
+      const int k = e - r;
+      if (k < kLptBatch) {
+        // one item at a time: the least-loaded group (lowest id on ties) takes it
+        for (int t = r; t < e; ++t) {
+          const uint32_t key = lane < G ? (rel << 5) | (uint32_t)lane : 0xffffffffu;
+          const uint32_t m = __reduce_min_sync(0xffffffffu, key);
+          const bool take = (int)(m & 31u) == lane;
+          if (take) {
+            grp[t] = lane;
+            pos[t] = cnt;
+          }
+          rel = rel - (m >> 5) + (take ? c : 0u);
+          cnt += take ? 1 : 0;
+          base += (int64_t)(m >> 5);
+        }
+      } else {
+        const bool act = lane < G;
+        const int q = act ? (int)(rel / c) : 0x3fffffff;   // level of this group's first pick
+        const uint32_t rho = rel % c;
+        // J = the smallest level with sum_g max(0, J - q_g + 1) >= k
+        int lo = 0, hi = k / G + 1 + (int)__reduce_max_sync(0xffffffffu, act ? (uint32_t)q : 0u);
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          const uint32_t have = __reduce_add_sync(0xffffffffu, act && q <= mid ? (uint32_t)(mid - q + 1) : 0u);
+          if ((int)have >= k) hi = mid; else lo = mid + 1;
+        }
+        const int J = lo;
+        const int below = (int)__reduce_add_sync(0xffffffffu, act && q < J ? (uint32_t)(J - q) : 0u);
+        // rank of this group in the in-level order (rho, g)
+        int ord = 0;
+        for (int o = 0; o < G; ++o) {
+          const uint32_t ro = __shfl_sync(0xffffffffu, rho, o);
+          ord += (ro < rho || (ro == rho && o < lane)) ? 1 : 0;
+        }
+        // in level J, the first (k - below) groups in that order that reach it
+        const bool inJ = act && q <= J;
+        const unsigned inJmask = __ballot_sync(0xffffffffu, inJ);
+        int before = 0;  // groups of level J ahead of this one in the order
+        for (int o = 0; o < G; ++o) {
+          const int oo = __shfl_sync(0xffffffffu, ord, o);
+          before += (((inJmask >> o) & 1u) && oo < ord) ? 1 : 0;
+        }
+        const int take = !act ? 0 : (q < J ? J - q : 0) + (inJ && before < k - below ? 1 : 0);
+        if (act) {
+          s_q[lane] = q;
+          s_take[lane] = take;
+          s_ord[lane] = ord;
+        }
+        __syncwarp();
+        // this group's picks: level j = q + i; rank = picks of earlier levels +
+        // picks of groups ahead of it in level j
+        for (int i = 0; i < take; ++i) {
+          const int j = q + i;
+          int rank = 0;
+          for (int o = 0; o < G; ++o) {
+            const int qo = s_q[o], to = s_take[o];
+            rank += min(max(j - qo, 0), to);
+            rank += (s_ord[o] < ord && qo <= j && j < qo + to) ? 1 : 0;
+          }
+          grp[r + rank] = lane;
+          pos[r + rank] = cnt + i;
+        }
+        __syncwarp();
+        // new loads (64-bit: a long run can add more than 2^32), renormalised
+        // to the least one; the spread stays below the largest cost (< 2^26)
+        const uint64_t nrel = act ? (uint64_t)rel + (uint64_t)take * c : ~0ull;
+        uint64_t mn = nrel;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t x = __shfl_xor_sync(0xffffffffu, mn, o);
+          mn = x < mn ? x : mn;
+        }
+        rel = act ? (uint32_t)(nrel - mn) : 0u;
+        base += (int64_t)mn;
+        cnt += take;
       }
+      r = e;
     }
     if (lane < G) {
       gload[lane] = base + (int64_t)rel;
@@ -467,6 +548,7 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   __shared__ int64_t ws[32];
   __shared__ int64_t gload[2][32 * kMaxGroupsPerLane];
   __shared__ int32_t gcount[2][32 * kMaxGroupsPerLane];
+  __shared__ int32_t lpt_scratch[2][96];
   const PlanHeader* H = pp.hdr;
   if (read_status(H) != 0) return;
   const int tid = threadIdx.x;
@@ -476,7 +558,7 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   if (warp < 2) {
     const int n = warp == 0 ? H->n_fwd_items : H->n_bwd_items;
     lpt_warp(n, G, warp == 0 ? pp.f_scost : pp.b_scost, warp == 0 ? pp.f_grp : pp.b_grp,
-             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp]);
+             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp], lpt_scratch[warp]);
   }
   __syncthreads();
   for (int kind = 0; kind < 2; ++kind) {

@@ -693,27 +693,39 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
 // Key tiles that no block sees (backward candidates of cost 0: past a
 // sample's last visible key, every tile of a sample without anchors, and
 // with per-block context offsets any tile outside every block's range) are
-// in no backward item; their key/value gradients are zero. CTA x takes
-// candidates x, x + gridDim.x, ...; the rows of a tile are written with
-// 16-byte stores.
+// in no backward item; their key/value gradients are zero. A CTA takes eight
+// candidates at a time (one cost read per warp) and zeroes each tile of cost
+// 0 among them with all its threads, in 16-byte stores.
 template <typename T>
-__global__ void zero_uncovered_kernel(ProbDev P, PlanPtrs pp, T* __restrict__ dKc,
-                                      T* __restrict__ dVc) {
+__global__ void __launch_bounds__(256) zero_uncovered_kernel(ProbDev P, PlanPtrs pp,
+                                                             T* __restrict__ dKc,
+                                                             T* __restrict__ dVc) {
+  __shared__ int unseen[8];
   if (read_status(pp.hdr) != 0) return;
   const int ncand = pp.hdr->n_bwd_cand;
+  const int warp = threadIdx.x >> 5;
   const size_t row16 = (size_t)P.Hkv * P.d * sizeof(T) / 16;  // d in {64, 128}: whole 16 B units
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (int cand = blockIdx.x; cand < ncand; cand += gridDim.x) {
-    if (pp.b_cost[cand] != 0) continue;
-    const int s = seg_of(pp.s_bcand_off, P.S, cand);
-    const int kt = cand - pp.s_bcand_off[s];
-    const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
-    const int k0 = kt * kKeyTile, k1 = min(L, k0 + kKeyTile);
-    const size_t lo = (size_t)(c0 + k0) * row16, hi = (size_t)(c0 + k1) * row16;
-    for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-      ((uint4*)dKc)[i] = z;
-      ((uint4*)dVc)[i] = z;
+  for (int base = blockIdx.x * 8; base < ncand; base += gridDim.x * 8) {
+    if ((threadIdx.x & 31) == 0) {
+      const int cand = base + warp;
+      unseen[warp] = cand < ncand && pp.b_cost[cand] == 0;
     }
+    __syncthreads();
+    for (int w = 0; w < 8; ++w) {
+      if (!unseen[w]) continue;  // CTA-uniform
+      const int cand = base + w;
+      const int s = seg_of(pp.s_bcand_off, P.S, cand);
+      const int kt = cand - pp.s_bcand_off[s];
+      const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
+      const int k0 = kt * kKeyTile, k1 = min(L, k0 + kKeyTile);
+      const size_t lo = (size_t)(c0 + k0) * row16, hi = (size_t)(c0 + k1) * row16;
+      for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        ((uint4*)dKc)[i] = z;
+        ((uint4*)dVc)[i] = z;
+      }
+    }
+    __syncthreads();  // the flags are rewritten by the next group
   }
 }
 
@@ -809,7 +821,8 @@ cudaError_t launch_dq_reduce(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
 cudaError_t launch_zero_uncovered(const ProbDev& P, const PlanPtrs& pp, int64_t ncb_cap,
                                   void* dKc, void* dVc, cudaStream_t st) {
   if (P.T == 0 || ncb_cap == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(ncb_cap < 4096 ? ncb_cap : 4096);
+  const int64_t g8 = (ncb_cap + 7) / 8;  // 8 warps per CTA, one candidate per warp at a time
+  const unsigned grid = (unsigned)(g8 < 1024 ? g8 : 1024);
   if (P.dtype == SPLITKV_FP32)
     zero_uncovered_kernel<float><<<grid, 256, 0, st>>>(P, pp, (float*)dKc, (float*)dVc);
   else
