@@ -103,8 +103,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mine);
 }
 
+// The first 1024-byte boundary at or after p, a pointer into the dynamic
+// shared array. It is reached by pointer arithmetic on p so that the compiler
+// still knows the result points to shared memory: an integer round trip
+// would turn every access through it into a generic load or store.
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // ===========================================================================
