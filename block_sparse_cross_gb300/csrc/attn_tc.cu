@@ -41,7 +41,12 @@ constexpr int kNS = 2;               // pipeline stages
 // per TMEM lane quadrant) and warp 15 (V loads).
 constexpr int kThreads = 512;    // forward and dQ
 constexpr int kVWarp = 15;
-constexpr int kThreadsKv = 352;  // dK / dV: warp 10 loads dO
+// dK / dV: warps 2..17 are the softmax (four per TMEM lane quadrant, one
+// 32-row quarter of the slab each; on config 4 at L = 262144 this ran 2 %
+// faster than two half-row warps per quadrant), warp 18 loads dO
+constexpr int kKvSoftmaxWarps = 16;
+constexpr int kKvDoWarp = 2 + kKvSoftmaxWarps;
+constexpr int kThreadsKv = 32 * (kKvDoWarp + 1);
 constexpr int kEpiWarp0 = 11;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
@@ -97,6 +102,10 @@ __device__ __forceinline__ RowInfo row_info_early(const ProbDev& P, const FwdRec
 // packed columns at 64h, inside its own half of the fp32 tile it read, so
 // the two halves never write where the other still reads.
 __device__ __forceinline__ uint32_t a_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
+// The same for the dK/dV kernel's P^T and dS^T: softmax quarter q (rows
+// 32q .. 32q + 31 of the slab) writes its 32 rows as 16 packed columns at the
+// start of its own 32 fp32 columns.
+__device__ __forceinline__ uint32_t kv_acol(int kk) { return (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1)); }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const bool mine = mbar_wait(bar, parity, abort);
@@ -1027,10 +1036,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, kSoftmaxWarps);
-    mbar_init(ds_ready, kSoftmaxWarps);
+    mbar_init(p_ready, kKvSoftmaxWarps);
+    mbar_init(ds_ready, kKvSoftmaxWarps);
     mbar_init(acc_done, 1);
-    mbar_init(acc_free, kSoftmaxWarps);
+    mbar_init(acc_free, kKvSoftmaxWarps);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -1093,7 +1102,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
           mbar_wait_drain(st_full + j % kNS, (j / kNS) & 1, kDrainNs);
       }
     }
-  } else if (warp == kSoftmaxWarps + 2) {
+  } else if (warp == kKvDoWarp) {
     // ---------------- dO producer: its own warp, so that it runs in parallel
     // with the Q producer instead of taking turns with it ----------------
     {  // the whole warp runs the loop and waits; one elected lane issues the copies
@@ -1179,7 +1188,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
-            mma_ts(tdV, tS + a_col(kk), dom0 + (mnmajor_off(kk) >> 4), kIdKV,
+            mma_ts(tdV, tS + kv_acol(kk), dom0 + (mnmajor_off(kk) >> 4), kIdKV,
                    (first && kk == 0) ? 0u : 1u);
         }
         __syncwarp();
@@ -1195,7 +1204,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
-            mma_ts(tdK, tP + a_col(kk), qm0 + (mnmajor_off(kk) >> 4), kIdKV,
+            mma_ts(tdK, tP + kv_acol(kk), qm0 + (mnmajor_off(kk) >> 4), kIdKV,
                    (first && kk == 0) ? 0u : 1u);
           mma_commit(st_empty + s);
           if (last) mma_commit(acc_done);
@@ -1207,10 +1216,12 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     __syncwarp();
     mbar_wait_drain(mma_drain, 0, kDrainNs);
   } else {
-    // softmax + epilogue (warps 2..9): key lane quadrant warp % 4, row half hf
-    constexpr int OH = D / 2;
+    // softmax + epilogue (warps 2..17): key lane quadrant warp % 4, row
+    // quarter qr (32 rows of the slab; a quarter of dK and dV's columns in
+    // the epilogue)
+    constexpr int OQ = D / 4;
     const int wq = warp & 3;
-    const int hf = (warp - 2) >> 2;
+    const int qr = (warp - 2) >> 2;
     const int r = wq * 32 + lane;  // key of the tile owned by this thread
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = P.scale_log2;
@@ -1234,24 +1245,24 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         if (!(ok = warp_wait(s_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         const uint8_t* sb = smem + Lay::stage0 + s * Lay::stage_bytes;
-        const float* nl2 = (const float*)(sb + Lay::info_off) + 64 * hf;  // -LSE*log2(e)
+        const float* nl2 = (const float*)(sb + Lay::info_off) + 32 * qr;  // -LSE*log2(e)
         const float* dvv = nl2 + kRows;
         const int* anc = (const int*)(dvv + kRows);   // end of each row's visible context
         const int* alo = anc + kRows;                 // start of each row's visible context
-        const int* anc0 = anc - 64 * hf;  // the slab's first row: its smallest anchor
+        const int* anc0 = anc - 32 * qr;  // the slab's first row: its smallest anchor
         // phase 1: P^T = exp(S^T * scale - LSE) on visible (key, row) pairs.
         // Rows are ordered by block and anchors rise with the block, so a key
         // below the slab's first anchor is seen by every row (padding rows give
         // 0 through their -inf): no per-element mask on such warps.
-        uint32_t pk[32];
+        uint32_t pk[16];
         {
-          uint32_t sv[64];
-          tmem_ld_row<64>(tS + lane_base + 64 * hf, sv);
+          uint32_t sv[32];
+          tmem_ld_row<32>(tS + lane_base + 32 * qr, sv);
           if (!offsets && __all_sync(0xffffffffu, key < anc0[0])) {
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t* nl2x2 = (const uint64_t*)nl2;  // (row c, row c + 1) pairs
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
               float y0, y1;
               f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
                                nl2x2[c / 2]),
@@ -1260,7 +1271,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
               const float p0 = (key < anc[c] && key >= alo[c])
                                    ? ex2(fmaf(__uint_as_float(sv[c]), sl2, nl2[c]))
                                    : 0.f;
@@ -1271,7 +1282,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
             }
           }
         }
-        tmem_st32(tS + lane_base + 64 * hf, pk);  // packed P^T of this half: columns a_col()
+        tmem_st16(tS + lane_base + 32 * qr, pk);  // packed P^T of this quarter: kv_acol()
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1280,11 +1291,11 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         if (!(ok = warp_wait(dp_full, nst & 1, abort_flag))) break;
         tc_fence_after();
         {
-          uint32_t dv[64];
-          tmem_ld_row<64>(tP + lane_base + 64 * hf, dv);
+          uint32_t dv[32];
+          tmem_ld_row<32>(tP + lane_base + 32 * qr, dv);
           const uint64_t* dvv2 = (const uint64_t*)dvv;  // (row c, row c + 1) pairs
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
+          for (int c = 0; c < 32; c += 2) {
             const uint32_t pp2 = pk[c / 2];
             const uint64_t d2 =
                 f2_mul(f2_pack(__uint_as_float(pp2 << 16), __uint_as_float(pp2 & 0xffff0000u)),
@@ -1294,7 +1305,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
             pk[c / 2] = pack_bf16(d0, d1);
           }
         }
-        tmem_st32(tP + lane_base + 64 * hf, pk);  // packed dS^T of this half
+        tmem_st16(tP + lane_base + 32 * qr, pk);  // packed dS^T of this quarter
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1304,10 +1315,10 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
       if (!(ok = warp_wait(acc_done, nit & 1, abort_flag))) break;
       tc_fence_after();
       const bool valid = key < I.L;
-      const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D + OH * hf;
+      const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D + OQ * qr;
       for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled)
-        uint32_t a[OH];
-        tmem_ld_row<OH>((which == 0 ? tdV : tdK) + lane_base + OH * hf, a);
+        uint32_t a[OQ];
+        tmem_ld_row<OQ>((which == 0 ? tdV : tdK) + lane_base + OQ * qr, a);
         if (which == 1) {  // both accumulators read: the next item may overwrite them
           tc_fence_before();
           __syncwarp();
@@ -1317,7 +1328,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
         __nv_bfloat16* dst = (which == 0 ? dVc : dKc) + off;
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < OH; i += 8) {
+          for (int i = 0; i < OQ; i += 8) {
             uint4 pv;
             pv.x = pack_bf16(__uint_as_float(a[i]) * f, __uint_as_float(a[i + 1]) * f);
             pv.y = pack_bf16(__uint_as_float(a[i + 2]) * f, __uint_as_float(a[i + 3]) * f);
