@@ -396,7 +396,7 @@ int splitkv_plan(const splitkv_problem* prob, void* plan_ws, size_t plan_bytes,
   if (st) return st;
   if (plan_bytes < plan_bytes_for(prob)) return SPLITKV_EWORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
-  return cuda_status(timed(SPLITKV_K_PLAN, 3, s, [&] { return launch_plan(c.P, c.pp, c.caps, s); }));
+  return cuda_status(timed(SPLITKV_K_PLAN, 4, s, [&] { return launch_plan(c.P, c.pp, c.caps, s); }));
 }
 
 int splitkv_fwd(const splitkv_problem* prob, const void* plan_ws, const void* Q, const void* Kc,

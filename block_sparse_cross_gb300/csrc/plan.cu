@@ -303,12 +303,13 @@ namespace {
 // q_g <= j still taking items), and inside a level by (rho_g, g) — the
 // least-loaded-first, lowest-id-on-ties order, the same in every level. The
 // run's last level J and each group's count follow from counting, and the
-// item of run rank t goes to the slot of rank t in that order: exactly the
-// one-at-a-time greedy result, without its serial chain.
+// item of run rank t goes to the slot of rank t in that order (one warp step
+// per level): exactly the one-at-a-time greedy result, without its serial
+// chain.
 constexpr int kLptBatch = 48;  // shorter runs go one item at a time
 
 __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32_t* pos,
-                         int64_t* gload, int32_t* gcount, int32_t* scratch) {
+                         int64_t* gload, int32_t* gcount) {
   const int lane = threadIdx.x & 31;
   // Fast path: one group per lane and 32-bit keys. While items are dealt
   // most expensive first to the least-loaded group, max load - min load
@@ -320,21 +321,35 @@ __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32
     uint32_t rel = 0;
     int64_t base = 0;
     int32_t cnt = 0;
-    int32_t* s_q = scratch;        // [32] per group: q_g, take_g, (rho, g) rank
-    int32_t* s_take = scratch + 32;
-    int32_t* s_ord = scratch + 64;
     int r = 0;
+    // costs [w0, w0 + 32), one per lane (-1 past the end: costs are
+    // positive), refilled by one coalesced load when r leaves the window, so
+    // that finding a run costs a shuffle and a ballot, not two dependent
+    // loads
+    int w0 = 0;
+    int64_t win = lane < n ? scost[lane] : -1;
     while (r < n) {
-      const int64_t c64 = scost[r];  // the same address in every lane
-      int e = r + 1;                  // end of the run of items of cost c64
-      for (;;) {
-        const int i = e + lane;
-        const unsigned diff = __ballot_sync(0xffffffffu, i >= n || scost[i] != c64);
-        if (diff) {
-          e += __ffs(diff) - 1;
-          break;
+      if (r >= w0 + 32) {
+        w0 = r;
+        win = w0 + lane < n ? scost[w0 + lane] : -1;
+      }
+      const int64_t c64 = __shfl_sync(0xffffffffu, win, r - w0);
+      int e;  // end of the run of items of cost c64
+      const unsigned diff =
+          __ballot_sync(0xffffffffu, lane > r - w0 && win != c64);
+      if (diff) {
+        e = w0 + __ffs(diff) - 1;
+      } else {  // the run reaches past the window: scan on in global memory
+        e = w0 + 32;
+        for (;;) {
+          const int i = e + lane;
+          const unsigned d2 = __ballot_sync(0xffffffffu, i >= n || scost[i] != c64);
+          if (d2) {
+            e += __ffs(d2) - 1;
+            break;
+          }
+          e += 32;
         }
-        e += 32;
       }
       const uint32_t c = (uint32_t)c64;
       const int k = e - r;
@@ -380,26 +395,22 @@ __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32
           before += (((inJmask >> o) & 1u) && oo < ord) ? 1 : 0;
         }
         const int take = !act ? 0 : (q < J ? J - q : 0) + (inJ && before < k - below ? 1 : 0);
-        if (act) {
-          s_q[lane] = q;
-          s_take[lane] = take;
-          s_ord[lane] = ord;
-        }
-        __syncwarp();
-        // this group's picks: level j = q + i; rank = picks of earlier levels +
-        // picks of groups ahead of it in level j
-        for (int i = 0; i < take; ++i) {
-          const int j = q + i;
-          int rank = 0;
-          for (int o = 0; o < G; ++o) {
-            const int qo = s_q[o], to = s_take[o];
-            rank += min(max(j - qo, 0), to);
-            rank += (s_ord[o] < ord && qo <= j && j < qo + to) ? 1 : 0;
+        // the picks, level by level: the groups active at level j (those
+        // with q_g <= j < q_g + take_g) take the next ranks of the run, in the
+        // in-level order; the set is a bit mask over order positions (G <= 32)
+        const int jmin =
+            (int)__reduce_min_sync(0xffffffffu, act && take > 0 ? (uint32_t)q : 0x7fffffffu);
+        int rk0 = r;
+        for (int j = jmin; j <= J; ++j) {
+          const bool on = act && take > 0 && q <= j && j < q + take;
+          const uint32_t mask = __reduce_or_sync(0xffffffffu, on ? (1u << ord) : 0u);
+          if (on) {
+            const int rk = rk0 + __popc(mask & ((1u << ord) - 1u));
+            grp[rk] = lane;
+            pos[rk] = cnt + (j - q);
           }
-          grp[r + rank] = lane;
-          pos[r + rank] = cnt + i;
+          rk0 += __popc(mask);
         }
-        __syncwarp();
         // new loads (64-bit: a long run can add more than 2^32), renormalised
         // to the least one; the spread stays below the largest cost (< 2^26)
         const uint64_t nrel = act ? (uint64_t)rel + (uint64_t)take * c : ~0ull;
@@ -548,7 +559,6 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   __shared__ int64_t ws[32];
   __shared__ int64_t gload[2][32 * kMaxGroupsPerLane];
   __shared__ int32_t gcount[2][32 * kMaxGroupsPerLane];
-  __shared__ int32_t lpt_scratch[2][96];
   const PlanHeader* H = pp.hdr;
   if (read_status(H) != 0) return;
   const int tid = threadIdx.x;
@@ -558,7 +568,7 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   if (warp < 2) {
     const int n = warp == 0 ? H->n_fwd_items : H->n_bwd_items;
     lpt_warp(n, G, warp == 0 ? pp.f_scost : pp.b_scost, warp == 0 ? pp.f_grp : pp.b_grp,
-             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp], lpt_scratch[warp]);
+             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp]);
   }
   __syncthreads();
   for (int kind = 0; kind < 2; ++kind) {
@@ -568,7 +578,6 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
     const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
     const int64_t* prefix = kind == 0 ? pp.f_prefix : pp.b_prefix;
     int32_t* qoff = kind == 0 ? pp.f_qoff : pp.b_qoff;
-    QEntry* queue = kind == 0 ? pp.f_queue : pp.b_queue;
     int64_t* load_lpt = kind == 0 ? pp.f_load_lpt : pp.b_load_lpt;
     int64_t* load_contig = kind == 0 ? pp.f_load_contig : pp.b_load_contig;
     // Per-head cost prefix F(x) over the per-head items in id order.
@@ -588,43 +597,63 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
           m, [&](int w) { return (int64_t)gcount[kind][w / Hkv]; },
           [&](int w, int64_t v) { qoff[w] = (int32_t)v; }, ws);
       if (tid == 0) qoff[m] = (int32_t)tot;
-      __syncthreads();
-      const int32_t* sorted = kind == 0 ? pp.f_sorted : pp.b_sorted;
-      const int32_t* grp = kind == 0 ? pp.f_grp : pp.b_grp;
-      const int32_t* pos = kind == 0 ? pp.f_pos : pp.b_pos;
-      for (int r = tid; r < n; r += blockDim.x) {
-        const int cand = item[sorted[r]];
-        const int Gr = grp[r], p = pos[r];
-        // the record of replica g differs from replica 0's only in g (and slot)
-        QEntry e = kind == 0 ? decode_fwd(P, pp, cand, 0) : decode_bwd(P, pp, cand, 0);
-        FwdRec fr;
-        BwdRec br;
-        if (kind == 0) fr = fwd_rec(P, pp, e); else br = bwd_rec(P, pp, e);
-        for (int g = 0; g < Hkv; ++g) {
-          const int at = qoff[Gr * Hkv + g] + p;
-          e.g = g;
-          queue[at] = e;
-          if (kind == 0) {
-            fr.g = g;
-            pp.f_rec[at] = fr;
-            ++fr.slot;
-          } else {
-            br.g = g;
-            pp.b_rec[at] = br;
-          }
-        }
-      }
     } else {
       for (int w = tid; w <= m; w += blockDim.x) qoff[w] = (int32_t)((int64_t)w * N / m);
-      for (int64_t x = tid; x < N; x += blockDim.x) {
-        const int cand = item[x / Hkv];
-        const int g = (int)(x % Hkv);
-        queue[x] = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
-        if (kind == 0) pp.f_rec[x] = fwd_rec(P, pp, queue[x]);
-        else pp.b_rec[x] = bwd_rec(P, pp, queue[x]);
-      }
     }
     __syncthreads();
+  }
+}
+
+// Queue entries and decoded records at the positions the assignment chose:
+// one thread per candidate (LPT: its Hkv replicas go to the same position of
+// the Hkv workers of its group) or per per-head item (contiguous), over a
+// grid, since every entry is independent. blockIdx.y is the direction.
+__global__ void __launch_bounds__(256) plan_queue_kernel(ProbDev P, PlanPtrs pp) {
+  const PlanHeader* H = pp.hdr;
+  if (read_status(H) != 0) return;
+  const int kind = blockIdx.y;
+  const int Hkv = P.Hkv;
+  const int n = kind == 0 ? H->n_fwd_items : H->n_bwd_items;
+  const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
+  QEntry* queue = kind == 0 ? pp.f_queue : pp.b_queue;
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if ((P.flags & SPLITKV_FLAG_CONTIGUOUS) == 0) {
+    const int32_t* qoff = kind == 0 ? pp.f_qoff : pp.b_qoff;
+    const int32_t* sorted = kind == 0 ? pp.f_sorted : pp.b_sorted;
+    const int32_t* grp = kind == 0 ? pp.f_grp : pp.b_grp;
+    const int32_t* pos = kind == 0 ? pp.f_pos : pp.b_pos;
+    for (int64_t r = first; r < n; r += stride) {
+      const int cand = item[sorted[r]];
+      const int Gr = grp[r], p = pos[r];
+      // the record of replica g differs from replica 0's only in g (and slot)
+      QEntry e = kind == 0 ? decode_fwd(P, pp, cand, 0) : decode_bwd(P, pp, cand, 0);
+      FwdRec fr;
+      BwdRec br;
+      if (kind == 0) fr = fwd_rec(P, pp, e); else br = bwd_rec(P, pp, e);
+      for (int g = 0; g < Hkv; ++g) {
+        const int at = qoff[Gr * Hkv + g] + p;
+        e.g = g;
+        queue[at] = e;
+        if (kind == 0) {
+          fr.g = g;
+          pp.f_rec[at] = fr;
+          ++fr.slot;
+        } else {
+          br.g = g;
+          pp.b_rec[at] = br;
+        }
+      }
+    }
+  } else {
+    const int64_t N = (int64_t)n * Hkv;  // per-head items, in id order
+    for (int64_t x = first; x < N; x += stride) {
+      const int cand = item[x / Hkv];
+      const int g = (int)(x % Hkv);
+      queue[x] = kind == 0 ? decode_fwd(P, pp, cand, g) : decode_bwd(P, pp, cand, g);
+      if (kind == 0) pp.f_rec[x] = fwd_rec(P, pp, queue[x]);
+      else pp.b_rec[x] = bwd_rec(P, pp, queue[x]);
+    }
   }
 }
 
@@ -643,6 +672,9 @@ cudaError_t launch_plan(const ProbDev& P, const PlanPtrs& pp, const PlanCaps& ca
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   plan_assign_kernel<<<1, 1024, 0, st>>>(P, pp);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  plan_queue_kernel<<<grid, 256, 0, st>>>(P, pp);
   return cudaGetLastError();
 }
 
