@@ -8,6 +8,11 @@ module raises at import time.
 
 The ``SplitKV`` helper bundles a problem, its two workspaces and the three
 passes for callers that hold their tensors in torch.
+
+With the environment variable ``SPLITKV_DEBUG=1`` set at import, the module
+loads the debug build (``libsplitkv_debug.so``, ``build.py --debug``), whose
+kernels check their indices and report failures through
+``splitkv_plan_stats`` (``debug_violations``); it is never the default.
 """
 from __future__ import annotations
 
@@ -17,12 +22,14 @@ import re
 from typing import Dict, Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libsplitkv.so")
+DEBUG_BUILD = os.environ.get("SPLITKV_DEBUG", "") == "1"
+LIB_PATH = os.path.join(HERE, "libsplitkv_debug.so" if DEBUG_BUILD else "libsplitkv.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "splitkv.h")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python block_sparse_cross_gb300/build.py` "
+        f"{LIB_PATH} is missing: build it with `python block_sparse_cross_gb300/build.py"
+        f"{' --debug' if DEBUG_BUILD else ''}` "
         "(no CPU fallback exists)")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -45,6 +52,7 @@ SPLITKV_FLAG_CONTIGUOUS = 2
 SPLITKV_FLAG_MASK_INCLUSIVE = 4
 SPLITKV_FLAG_MASK_CAUSAL_BLOCK = 8
 SPLITKV_FLAG_MASK_CONTEXT_OFFSET = 16
+SPLITKV_BUILD_DEBUG = 1
 SPLITKV_NUM_KERNELS = 9
 SPLITKV_NOALLOC_SCRATCH_BYTES = 64 << 20
 (SPLITKV_K_PLAN, SPLITKV_K_FWD_ATTN, SPLITKV_K_MERGE, SPLITKV_K_BWD_DRAFT, SPLITKV_K_BWD_DQ,
@@ -93,6 +101,10 @@ class splitkv_stats(ctypes.Structure):
         ("fwd_tiles", ctypes.c_int64),
         ("dense_tiles", ctypes.c_int64),
         ("work_bytes_used", ctypes.c_size_t),
+        ("debug_violations", ctypes.c_int64),
+        ("debug_site", ctypes.c_int32),
+        ("pad0", ctypes.c_int32),
+        ("debug_index", ctypes.c_int64),
     ]
 
     def as_dict(self) -> Dict[str, object]:
@@ -126,6 +138,7 @@ _SIGS = {
     "splitkv_proj_out_bwd": ([_P, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "splitkv_proj_status": ([ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp], ctypes.c_int),
     "splitkv_selftest_wait_timeout": ([ctypes.POINTER(ctypes.c_int), _vp], ctypes.c_int),
+    "splitkv_build_flags": ([], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -171,6 +184,11 @@ def _check(where: str, st: int) -> None:
 # ---- same-name wrappers ----------------------------------------------------
 def splitkv_status_string(status: int) -> str:
     return _lib.splitkv_status_string(int(status)).decode()
+
+
+def splitkv_build_flags() -> int:
+    """SPLITKV_BUILD_DEBUG when the loaded library checks its indices."""
+    return _lib.splitkv_build_flags()
 
 
 def splitkv_kernel_name(kernel_id: int) -> str:

@@ -501,6 +501,11 @@ int splitkv_plan_stats(const splitkv_problem* prob, const void* plan_ws, splitkv
   memset(out, 0, sizeof(*out));
   out->device_status = h.magic == kPlanMagic ? h.status : SPLITKV_EPLAN;
   out->workers = c.P.workers;
+  if (h.magic == kPlanMagic) {
+    out->debug_violations = h.dbg_count;
+    out->debug_site = (int32_t)((uint64_t)h.dbg_first >> 48);
+    out->debug_index = (int64_t)((uint64_t)h.dbg_first & 0xffffffffffffull);
+  }
   if (out->device_status != SPLITKV_OK) return SPLITKV_OK;
   const int m = c.P.workers;
   std::vector<int64_t> buf(m);
@@ -714,6 +719,14 @@ int splitkv_proj_status(int* status, int clear, splitkv_stream stream) {
 int splitkv_selftest_wait_timeout(int* status, splitkv_stream stream) {
   if (!status) return SPLITKV_EINVAL;
   return cuda_status(run_wait_probe(status, (cudaStream_t)stream));
+}
+
+int splitkv_build_flags(void) {
+#ifdef SKV_DEBUG
+  return SPLITKV_BUILD_DEBUG;
+#else
+  return 0;
+#endif
 }
 
 const char* splitkv_status_string(int status) {

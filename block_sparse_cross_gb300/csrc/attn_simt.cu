@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
   if (threadIdx.x == 0) stamp_busy(P, pp, 0, 0);
   const int w = blockIdx.x;
   const int r = threadIdx.x;
-  const int q0 = pp.f_qoff[w], q1 = pp.f_qoff[w + 1];
+  const int q0 = pp.f_qoff[w];
+  const int q1 = queue_end(pp.f_qoff, w, (int64_t)pp.hdr->n_fwd_items * P.Hkv, pp.hdr);
   for (int qi = q0; qi < q1; ++qi) {
     const QEntry e = pp.f_queue[qi];
     const int first = pp.sl_first[e.slab], nblk = pp.sl_nblk[e.slab];
@@ -92,11 +93,13 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(ProbDev P, PlanPtrs pp, W
     }
     const size_t slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (SKV_OK(slot < (size_t)pp.hdr->n_slot_base * P.Hkv, pp.hdr, kDbgFwdSlot, slot)) {
 #pragma unroll
-    for (int x = 0; x < D; x += 4)
-      *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
-          make_float4(acc[x] * inv, acc[x + 1] * inv, acc[x + 2] * inv, acc[x + 3] * inv);
-    wk.part_lse[slot * kRows + r] = l > 0.f ? m + logf(l) : -INFINITY;
+      for (int x = 0; x < D; x += 4)
+        *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
+            make_float4(acc[x] * inv, acc[x + 1] * inv, acc[x + 2] * inv, acc[x + 3] * inv);
+      wk.part_lse[slot * kRows + r] = l > 0.f ? m + logf(l) : -INFINITY;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) stamp_busy(P, pp, 0, 1);
@@ -118,7 +121,8 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
   if (threadIdx.x == 0) stamp_busy(P, pp, 1, 0);
   const int w = blockIdx.x;
   const int r = threadIdx.x;
-  const int q0 = pp.f_qoff[w], q1 = pp.f_qoff[w + 1];
+  const int q0 = pp.f_qoff[w];
+  const int q1 = queue_end(pp.f_qoff, w, (int64_t)pp.hdr->n_fwd_items * P.Hkv, pp.hdr);
   for (int qi = q0; qi < q1; ++qi) {
     const QEntry e = pp.f_queue[qi];
     const int first = pp.sl_first[e.slab], nblk = pp.sl_nblk[e.slab];
@@ -174,10 +178,12 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(ProbDev P, PlanPtrs pp
       }
     }
     const size_t slot = (size_t)(pp.sl_slot[e.slab] + e.c) * P.Hkv + e.g;
+    if (SKV_OK(slot < (size_t)pp.hdr->n_slot_base * P.Hkv, pp.hdr, kDbgDqSlot, slot)) {
 #pragma unroll
-    for (int x = 0; x < D; x += 4)
-      *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
-          make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+      for (int x = 0; x < D; x += 4)
+        *(float4*)(wk.part_o + part_off(slot, r, x, D)) =
+            make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) stamp_busy(P, pp, 1, 1);
@@ -212,7 +218,8 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
   const int w = blockIdx.x;
   const int tid = threadIdx.x;
   const int kl = tid >> 1, half = tid & 1;
-  const int q0 = pp.b_qoff[w], q1 = pp.b_qoff[w + 1];
+  const int q0 = pp.b_qoff[w];
+  const int q1 = queue_end(pp.b_qoff, w, (int64_t)pp.hdr->n_bwd_items * P.Hkv, pp.hdr);
   for (int qi = q0; qi < q1; ++qi) {
     const QEntry e = pp.b_queue[qi];
     const int s = e.s, g = e.g;
@@ -289,7 +296,8 @@ __global__ void __launch_bounds__(256) bwd_dkdv_simt_kernel(ProbDev P, PlanPtrs 
         }
       }
     }
-    if (key < L) {
+    if (key < L && SKV_OK((int64_t)c0 + key < P.T && g >= 0 && g < P.Hkv, pp.hdr, kDbgKvRow,
+                          (int64_t)c0 + key)) {
       const size_t off = ((size_t)(c0 + key) * P.Hkv + g) * D + half * HD;
 #pragma unroll
       for (int x = 0; x < HD; ++x) {

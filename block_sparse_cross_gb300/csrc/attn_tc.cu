@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tO = tmem + 256;  // two S buffers, then O_0 and O_1 (D columns each)
   float* lm = (float*)(smem + Lay::lm);
-  const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
+  const int q0 = pp.f_qoff[blockIdx.x];
+  const int q1 = queue_end(pp.f_qoff, blockIdx.x, (int64_t)pp.hdr->n_fwd_items * P.Hkv, pp.hdr);
 
   if (warp == 0) {
     // ---------------- TMA producer: Q and K (V comes from warp 15) ----------------
@@ -373,6 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = lm[r] * w0 + lm[128 + r] * w1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float f0 = w0 * inv, f1 = w1 * inv;
+      const bool sok = SKV_OK(I.slot >= 0 && (int64_t)I.slot < (int64_t)pp.hdr->n_slot_base * P.Hkv,
+                              pp.hdr, kDbgFwdSlot, I.slot);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {  // 32 columns of each half at a time (register budget)
         uint32_t v0[32], v1[32];
@@ -391,11 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             o[k] = fmaf(__uint_as_float(v0[i + k]), f0, __uint_as_float(v1[i + k]) * f1);
-          st_global_v8(wk.part_o + part_off(I.slot, r, 32 * c + i, D), o[0], o[1], o[2], o[3],
-                       o[4], o[5], o[6], o[7]);
+          if (sok)
+            st_global_v8(wk.part_o + part_off(I.slot, r, 32 * c + i, D), o[0], o[1], o[2], o[3],
+                         o[4], o[5], o[6], o[7]);
         }
       }
-      wk.part_lse[(size_t)I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+      if (sok)
+        wk.part_lse[(size_t)I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
     }
   } else {
     // ---------------- softmax (warps 2..9) ----------------
@@ -647,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tdQ = tmem + 256;           // D columns
   const uint32_t tQ = tdQ + D;               // D / 2 columns: Q, bf16 pairs
   const uint32_t tdO = tQ + D / 2;           // D / 2 columns: dO
-  const int q0 = pp.f_qoff[blockIdx.x], q1 = pp.f_qoff[blockIdx.x + 1];
+  const int q0 = pp.f_qoff[blockIdx.x];
+  const int q1 = queue_end(pp.f_qoff, blockIdx.x, (int64_t)pp.hdr->n_fwd_items * P.Hkv, pp.hdr);
 
   if (warp == 0) {
     // ---------------- TMA producer: Q, dO and K (V comes from warp 15) ----------------
@@ -806,6 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto write_dq = [&](const FwdItem& I, uint32_t it) -> bool {
       if (!warp_wait(dq_done, it & 1, abort_flag)) return false;
       tc_fence_after();
+      const bool sok = SKV_OK(I.slot >= 0 && (int64_t)I.slot < (int64_t)pp.hdr->n_slot_base * P.Hkv,
+                              pp.hdr, kDbgDqSlot, I.slot);
 #pragma unroll 1
       for (int h = 0; h < D / 64; ++h) {  // 64 columns at a time (register budget)
         uint32_t v[64];
@@ -817,7 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < 64; i += 8)
-          st_global_v8(wk.part_o + part_off(I.slot, r, 64 * h + i, D), __uint_as_float(v[i]),
+          if (sok)
+            st_global_v8(wk.part_o + part_off(I.slot, r, 64 * h + i, D), __uint_as_float(v[i]),
                        __uint_as_float(v[i + 1]),
                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]),
                        __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]),
@@ -1053,7 +1062,8 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-  const int q0 = pp.b_qoff[blockIdx.x], q1 = pp.b_qoff[blockIdx.x + 1];
+  const int q0 = pp.b_qoff[blockIdx.x];
+  const int q1 = queue_end(pp.b_qoff, blockIdx.x, (int64_t)pp.hdr->n_bwd_items * P.Hkv, pp.hdr);
 
   if (warp == 0) {
     // ---------------- producer: K/V per item, then Q and the slab's row table
@@ -1314,7 +1324,9 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
       if (!ok) break;
       if (!(ok = warp_wait(acc_done, nit & 1, abort_flag))) break;
       tc_fence_after();
-      const bool valid = key < I.L;
+      const bool valid =
+          key < I.L && SKV_OK((int64_t)I.c0 + key < P.T && I.g >= 0 && I.g < P.Hkv, pp.hdr,
+                              kDbgKvRow, (int64_t)I.c0 + key);
       const size_t off = ((size_t)(I.c0 + key) * P.Hkv + I.g) * D + OQ * qr;
       for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled)
         uint32_t a[OQ];

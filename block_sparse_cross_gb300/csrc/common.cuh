@@ -12,6 +12,44 @@ __device__ __forceinline__ void latch(PlanHeader* h, int code) {
   atomicCAS(&h->status, 0, code);
 }
 
+// Index checks of the debug build (compiled with -DSKV_DEBUG=1): a failed
+// check counts itself in the plan header, keeps the first failure's site and
+// index there, and the caller skips the access. In the release build a check
+// is the constant true: its condition is not even evaluated.
+enum DebugSite : int {
+  kDbgFwdSlot = 1,       // forward partial slot written (tensor-core or CUDA-core kernel)
+  kDbgDqSlot = 2,        // dQ partial slot written
+  kDbgKvRow = 3,         // dK/dV context row written
+  kDbgQueue = 4,         // a CTA's queue range [q0, q1) within the plan's items
+  kDbgMergeSlot = 5,     // partial slots a merge row reads
+  kDbgReduceSlot = 6,    // partial slots a dQ-reduce row reads
+  kDbgQueryRow = 7,      // O / LSE / dQ query row written
+  kDbgPlanScatter = 8,   // a planner scatter position (sorted order, LPT pick, queue entry)
+  kDbgDraftRow = 9,      // draft key/value gradient row written
+  kDbgZeroRow = 10,      // context row zeroed
+};
+#ifdef SKV_DEBUG
+static __device__ __noinline__ bool skv_dbg_fail(const PlanHeader* h, int site, int64_t idx) {
+  PlanHeader* w = const_cast<PlanHeader*>(h);
+  atomicAdd((unsigned long long*)&w->dbg_count, 1ull);
+  const unsigned long long code =
+      ((unsigned long long)site << 48) | ((unsigned long long)idx & 0xffffffffffffull);
+  atomicCAS((unsigned long long*)&w->dbg_first, 0ull, code);
+  return false;
+}
+#define SKV_OK(cond, h, site, idx) ((cond) || ::skv::skv_dbg_fail((h), (site), (int64_t)(idx)))
+#else
+#define SKV_OK(cond, h, site, idx) true
+#endif
+
+// The end of worker w's queue range [qoff[w], qoff[w + 1]): the range is
+// made empty when the debug build finds it outside the plan's n entries.
+__device__ __forceinline__ int queue_end(const int32_t* qoff, int w, int64_t n,
+                                         const PlanHeader* h) {
+  const int q0 = qoff[w], q1 = qoff[w + 1];
+  return SKV_OK(q0 >= 0 && q0 <= q1 && q1 <= n, h, kDbgQueue, w) ? q1 : q0;
+}
+
 __device__ __forceinline__ int read_status(const PlanHeader* h) {
   return *(volatile const int32_t*)&h->status;
 }

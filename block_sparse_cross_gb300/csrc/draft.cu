@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(512, 2) merge_draft_kernel(ProbDev P, PlanPtrs
   float* Od = (float*)smem_raw;                                    // [R][D]
   float* lsed = (float*)(smem_raw + v_off + sizeof(__nv_bfloat16) * geo.B16 * geo.ld_row);  // [R]
   const int j = blockIdx.x, g = blockIdx.y;
+  if (!SKV_OK(j < P.NA && g < P.Hkv, pp.hdr, kDbgDraftRow, j)) return;  // CTA-uniform
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tq = lane & 3;
   stage_rows<D>(Qs, geo.ld_row, Q, j * P.B, g * G, G, P.Hq, R);
@@ -309,9 +310,15 @@ __global__ void __launch_bounds__(512, 2) merge_draft_kernel(ProbDev P, PlanPtrs
   const int slab = pp.s_slab_off[s] + lj / P.bps;
   const int rbase = (lj % P.bps) * R;
   // the block sees chunks [c_lo, nact) (none when its context [lo, end) is empty)
-  const int nact = (P.anchors[j] + P.chunk - 1) / P.chunk;
-  const int c_lo = P.ctx_lo[j] >= P.anchors[j] ? nact : P.ctx_lo[j] / P.chunk;
-  const size_t slot0 = (size_t)pp.sl_slot[slab];
+  const int na = (P.anchors[j] + P.chunk - 1) / P.chunk;
+  const int c_lo = P.ctx_lo[j] >= P.anchors[j] ? na : P.ctx_lo[j] / P.chunk;
+  const bool slab_ok = SKV_OK(slab >= 0 && slab < pp.hdr->n_slabs, pp.hdr, kDbgMergeSlot, slab);
+  const size_t slot0 = slab_ok ? (size_t)pp.sl_slot[slab] : 0;
+  // the block's rows read partial slots slot0 + c, c in [c_lo, nact)
+  const int nact = slab_ok && SKV_OK(slot0 + (size_t)na <= (size_t)pp.hdr->n_slot_base, pp.hdr,
+                                     kDbgMergeSlot, slot0 + na)
+                       ? na
+                       : c_lo;
   const size_t cstride = (size_t)P.Hkv * kRows;  // between chunks of a row
   const size_t ostride = cstride * D;
   const int r = threadIdx.x % R, q = threadIdx.x / R;
@@ -383,6 +390,7 @@ __global__ void __launch_bounds__(256) bwd_draft_mma_kernel(
   __nv_bfloat16* dSs = Ps + R * geo.ld_key;             // [R][B16 + 8]  dS
   float* Dr = (float*)(dSs + R * geo.ld_key);           // [R]
   const int j = blockIdx.x, g = blockIdx.y;
+  if (!SKV_OK(j < P.NA && g < P.Hkv, pp.hdr, kDbgDraftRow, j)) return;  // CTA-uniform
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tq = lane & 3;
   const int nw = blockDim.x >> 5;

@@ -38,7 +38,12 @@ struct PlanHeader {
   int64_t fwd_tiles;       // per kv head
   int64_t dense_tiles;     // per kv head
   uint64_t problem_hash;
-  int64_t pad1[7];
+  // index checks of the debug build (SKV_DEBUG): failed checks since the
+  // plan, and the first one as (site << 48) | (index & (2^48 - 1)); zero in
+  // the release build
+  int64_t dbg_count;
+  int64_t dbg_first;
+  int64_t pad1[5];
 };
 static_assert(sizeof(PlanHeader) % 16 == 0, "header alignment");
 

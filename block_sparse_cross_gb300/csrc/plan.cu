@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
     H->n_slabs = H->n_fwd_cand = H->n_fwd_items = H->n_slot_base = 0;
     H->n_bwd_cand = H->n_bwd_items = 0;
     H->fwd_total_cost = H->bwd_total_cost = H->fwd_tiles = H->dense_tiles = 0;
+    H->dbg_count = H->dbg_first = 0;
     tiles_acc = 0;
     dense_acc = 0;
   }
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(256) plan_rank_kernel(PlanPtrs pp) {
       rank += (cj > ci) | ((cj == ci) & (j0 + t < i));
     }
   }
-  if (i < n) {
+  if (i < n && SKV_OK(rank < n, H, kDbgPlanScatter, rank)) {
     (kind == 0 ? pp.f_sorted : pp.b_sorted)[rank] = i;
     (kind == 0 ? pp.f_scost : pp.b_scost)[rank] = ci;
   }
@@ -309,7 +310,7 @@ namespace {
 constexpr int kLptBatch = 48;  // shorter runs go one item at a time
 
 __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32_t* pos,
-                         int64_t* gload, int32_t* gcount) {
+                         int64_t* gload, int32_t* gcount, const PlanHeader* H) {
   const int lane = threadIdx.x & 31;
   // Fast path: one group per lane and 32-bit keys. While items are dealt
   // most expensive first to the least-loaded group, max load - min load
@@ -406,8 +407,10 @@ __device__ void lpt_warp(int n, int G, const int64_t* scost, int32_t* grp, int32
           const uint32_t mask = __reduce_or_sync(0xffffffffu, on ? (1u << ord) : 0u);
           if (on) {
             const int rk = rk0 + __popc(mask & ((1u << ord) - 1u));
-            grp[rk] = lane;
-            pos[rk] = cnt + (j - q);
+            if (SKV_OK(rk >= r && rk < e, H, kDbgPlanScatter, rk)) {
+              grp[rk] = lane;
+              pos[rk] = cnt + (j - q);
+            }
           }
           rk0 += __popc(mask);
         }
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   if (warp < 2) {
     const int n = warp == 0 ? H->n_fwd_items : H->n_bwd_items;
     lpt_warp(n, G, warp == 0 ? pp.f_scost : pp.b_scost, warp == 0 ? pp.f_grp : pp.b_grp,
-             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp]);
+             warp == 0 ? pp.f_pos : pp.b_pos, gload[warp], gcount[warp], H);
   }
   __syncthreads();
   for (int kind = 0; kind < 2; ++kind) {
@@ -633,6 +636,7 @@ __global__ void __launch_bounds__(256) plan_queue_kernel(ProbDev P, PlanPtrs pp)
       if (kind == 0) fr = fwd_rec(P, pp, e); else br = bwd_rec(P, pp, e);
       for (int g = 0; g < Hkv; ++g) {
         const int at = qoff[Gr * Hkv + g] + p;
+        if (!SKV_OK(at >= 0 && at < (int64_t)n * Hkv, H, kDbgPlanScatter, at)) continue;
         e.g = g;
         queue[at] = e;
         if (kind == 0) {

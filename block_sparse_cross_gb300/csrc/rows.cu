@@ -219,7 +219,14 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
   // rescaled when the maximum grows. Lane c of each group of 32 chunks holds
   // chunk c's lse; the group's lse values and its first eight partial rows
   // are loaded together, eight rows in flight per step.
-  const size_t slot0 = (size_t)pp.sl_slot[G.slab];
+  // the row reads partial slots slot0 + c, c in [c_lo, nhi), of its slab
+  const bool slab_ok =
+      SKV_OK(G.slab >= 0 && G.slab < pp.hdr->n_slabs, pp.hdr, kDbgMergeSlot, G.slab);
+  const size_t slot0 = slab_ok ? (size_t)pp.sl_slot[G.slab] : 0;
+  const int nhi = slab_ok && SKV_OK(slot0 + (size_t)G.nact <= (size_t)pp.hdr->n_slot_base, pp.hdr,
+                                    kDbgMergeSlot, slot0 + G.nact)
+                      ? G.nact
+                      : G.c_lo;
   const float* plse = wk.part_lse + (slot0 * P.Hkv + g) * kRows + G.r;  // chunk c at c * Hkv * 128
   const size_t cstride = (size_t)P.Hkv * kRows;
   const float* pbase = wk.part_o + part_off(slot0 * P.Hkv + g, G.r, x0, D);
@@ -243,8 +250,8 @@ __device__ __forceinline__ void merge_row(const ProbDev& P, const PlanPtrs& pp, 
 #pragma unroll
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
   float Mr = -INFINITY, Sr = 0.f;
-  for (int cb = G.c_lo; cb < G.nact; cb += 32) {
-    const int nc = min(32, G.nact - cb);
+  for (int cb = G.c_lo; cb < nhi; cb += 32) {
+    const int nc = min(32, nhi - cb);
     const float lc = lane < nc ? plse[(cb + lane) * cstride] : -INFINITY;
     float v[U][EPL];
     load_rows(cb, 0, nc, v);
@@ -323,6 +330,7 @@ __global__ void __launch_bounds__(256) merge_block_kernel(ProbDev P, PlanPtrs pp
   if (read_status(pp.hdr) != 0) return;
   const int B = P.B, Gs = P.group, R = B * Gs;
   const int j = blockIdx.x, g = blockIdx.y;
+  if (!SKV_OK(j < P.NA && g < P.Hkv, pp.hdr, kDbgDraftRow, j)) return;  // CTA-uniform
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < B * D; i += blockDim.x) {
     const size_t o = ((size_t)(j * B + i / D) * P.Hkv + g) * D + i % D;
@@ -436,6 +444,7 @@ __global__ void __launch_bounds__(D) bwd_draft_kv_kernel(ProbDev P, PlanPtrs pp,
   float* ps = sm;            // [R][B]
   float* dss = ps + R * B;   // [R][B]
   const int j = blockIdx.x, g = blockIdx.y;
+  if (!SKV_OK(j < P.NA && g < P.Hkv, pp.hdr, kDbgDraftRow, j)) return;  // CTA-uniform
   const int x = threadIdx.x;
   if (read_status(pp.hdr) != 0) return;  // every thread reads the same word
   for (int idx = x; idx < R * B; idx += blockDim.x) {
@@ -501,6 +510,7 @@ __global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtr
   if (read_status(pp.hdr) != 0) return;
   const int B = P.B, G = P.group, R = B * G;
   const int j = blockIdx.x, g = blockIdx.y;
+  if (!SKV_OK(j < P.NA && g < P.Hkv, pp.hdr, kDbgDraftRow, j)) return;  // CTA-uniform
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = (P.flags & SPLITKV_FLAG_MASK_CAUSAL_BLOCK) != 0;
   for (int i = threadIdx.x; i < B * D; i += blockDim.x) {
@@ -656,9 +666,14 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
   const int r = 64 * blockIdx.z + threadIdx.x % 64, q = threadIdx.x / 64;
   const RowInfo ri = row_info(P, pp.sl_first[sg], pp.sl_nblk[sg], g, r);
   if (ri.n < 0) return;  // padding row of the slab's tile
-  const int nact = (ri.anchor + P.chunk - 1) / P.chunk;
-  const int c_lo = ri.lo >= ri.anchor ? nact : ri.lo / P.chunk;
+  const int na = (ri.anchor + P.chunk - 1) / P.chunk;
+  const int c_lo = ri.lo >= ri.anchor ? na : ri.lo / P.chunk;
   const size_t slot0 = (size_t)pp.sl_slot[sg];
+  // the row reads partial slots slot0 + c, c in [c_lo, nact), of its slab
+  const int nact = SKV_OK(slot0 + (size_t)na <= (size_t)pp.hdr->n_slot_base, pp.hdr, kDbgReduceSlot,
+                          slot0 + na)
+                       ? na
+                       : c_lo;
   const float* prow = wk.part_o + part_off(slot0 * P.Hkv + g, r, 8 * q, D);
   const size_t ostride = (size_t)P.Hkv * kRows * D;  // between chunks of the row
   float acc[kGroups][8];
@@ -677,6 +692,7 @@ __global__ void __launch_bounds__(256) dq_reduce_kernel(ProbDev P, PlanPtrs pp, 
       acc[i][4] += b.x; acc[i][5] += b.y; acc[i][6] += b.z; acc[i][7] += b.w;
     }
   }
+  if (!SKV_OK(ri.n < P.NQ && ri.h >= 0 && ri.h < P.Hq, pp.hdr, kDbgQueryRow, ri.n)) return;
   const size_t row = ((size_t)ri.n * P.Hq + ri.h) * D + 8 * q;
 #pragma unroll
   for (int i = 0; i < kGroups; ++i) {
@@ -719,6 +735,8 @@ __global__ void __launch_bounds__(256) zero_uncovered_kernel(ProbDev P, PlanPtrs
       const int kt = cand - pp.s_bcand_off[s];
       const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
       const int k0 = kt * kKeyTile, k1 = min(L, k0 + kKeyTile);
+      if (!SKV_OK(k0 >= 0 && (int64_t)c0 + k1 <= P.T, pp.hdr, kDbgZeroRow, (int64_t)c0 + k1))
+        continue;  // CTA-uniform
       const size_t lo = (size_t)(c0 + k0) * row16, hi = (size_t)(c0 + k1) * row16;
       for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         ((uint4*)dKc)[i] = z;

@@ -179,6 +179,14 @@ typedef struct splitkv_stats {
   int64_t fwd_tiles;          /* 128x128 (row, key) tiles the forward computes */
   int64_t dense_tiles;        /* tiles of the dense (N_q*group/128) x (L/128) x Hkv grid */
   size_t work_bytes_used;     /* exact bytes of the work workspace this plan needs */
+  /* index checks of the debug build (splitkv_build_flags() & SPLITKV_BUILD_DEBUG):
+   * failed checks since the plan was built (every kernel that read this plan
+   * counts; a failed check skips its access), and the first one's site
+   * (1 .. 10, listed in the source) and index; all zero in the release build */
+  int64_t debug_violations;
+  int32_t debug_site;
+  int32_t pad0;
+  int64_t debug_index;
 } splitkv_stats;
 
 /*
@@ -421,6 +429,15 @@ int splitkv_proj_status(int* status, int clear, splitkv_stream stream);
  * Errors: EINVAL (null status), ECUDA.
  */
 int splitkv_selftest_wait_timeout(int* status, splitkv_stream stream);
+
+/*
+ * splitkv_build_flags — how this library was compiled: SPLITKV_BUILD_DEBUG
+ *   when its kernels check their indices (a debug build, in place of a memory
+ *   checker: out-of-range accesses are counted in the plan header, reported
+ *   by splitkv_plan_stats, and skipped). Host-only.
+ */
+#define SPLITKV_BUILD_DEBUG 1
+int splitkv_build_flags(void);
 
 /* Name of a kernel family id (never NULL). */
 const char* splitkv_kernel_name(int kernel_id);

@@ -35,6 +35,15 @@ def mask_flags(w):
             (S.SPLITKV_FLAG_MASK_CAUSAL_BLOCK if w.mask_causal_block else 0))
 
 
+def assert_no_debug_violations(kv):
+    """Under the index-checking debug build (SPLITKV_DEBUG=1), no kernel that
+    read this plan found an index out of range; a no-op in the release build."""
+    assert S.DEBUG_BUILD == bool(S.splitkv_build_flags() & S.SPLITKV_BUILD_DEBUG)
+    if S.DEBUG_BUILD:
+        st = kv.stats()
+        assert st.debug_violations == 0, (st.debug_violations, st.debug_site, st.debug_index)
+
+
 class Guarded:
     """A device tensor at the start of a poisoned buffer with a guard tail."""
 
@@ -133,6 +142,7 @@ class Case:
         that every element of every output a call has written is finite (no
         poison NaN left)."""
         self.check_guards()
+        assert_no_debug_violations(self.kv)
         out = {"O": self.O.float().cpu().numpy(), "LSE": self.LSE.cpu().numpy()}
         for k, v in self.grads.items():
             out[k] = v.float().cpu().numpy()

@@ -7,6 +7,7 @@ import torch
 import block_sparse_cross_gb300 as S
 import oracle.plan as OP
 import workloads as W
+from gpu_case import assert_no_debug_violations
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +21,8 @@ def planned(w, workers, flags=0):
                    w.Hq, w.Hkv, w.d, w.chunk, w.scale, num_workers=workers, flags=flags,
                    ctx_lo=ctx_lo)
     kv.plan()
+    torch.cuda.synchronize()
+    assert_no_debug_violations(kv)
     return kv
 
 
