@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_free = sfree + 2;         // the epilogue has read O_0, O_1 and the row sums
   uint64_t* lm_ready = o_free + 1;      // the softmax has written the item's (m, l)
   uint64_t* mma_drain = lm_ready + 1;   // [2] one per issuing warp
+  uint64_t* stg_free = mma_drain + 2;   // [2] the epilogue is done with Q buffer b as staging
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -187,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sfree + b, 1);
     }
     mbar_init(o_free, 4);
+    mbar_init(stg_free, 4);
+    mbar_init(stg_free + 1, 4);
     mbar_init(lm_ready, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 1, 1);
@@ -220,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qb = nq & 1;
         // buffer qb is free once the last S of item nq - 2 is done
         if (nq >= 2 && !(ok = warp_wait(q_empty + qb, ((nq >> 1) - 1) & 1, abort_flag))) break;
+        // ... and once the epilogue of that item has used it as staging
+        if (nq >= 2 && !(ok = warp_wait(stg_free + qb, ((nq >> 1) - 1) & 1, abort_flag))) break;
         if (elect_one()) {
           mbar_expect_tx(q_full + qb, Lay::tile);
           for (int i = 0; i < kSub; ++i)
@@ -349,10 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
-    // Waits for the item's last PV and its (m, l) per half, combines the
-    // halves (O = sum_h 2^(m_h - m) O_h, l = sum_h 2^(m_h - m) l_h), releases
-    // the accumulators and writes the chunk partial (O / l, lse): the softmax
-    // warps never wait for it.
+    // Waits for the item's last PV and its (m, l) per half and combines the
+    // halves (O = sum_h 2^(m_h - m) O_h / l, l = sum_h 2^(m_h - m) l_h). The
+    // accumulators are read out of TMEM before anything is written to global
+    // memory, and released at once (the next item's first PV overwrites them
+    // and waits for that): columns [0, D/2) go to a staging row in the item's
+    // Q buffer (free: the item's S are all done, and the next Q load into it
+    // waits for stg_free), columns [D/2, D) stay in registers. Then the chunk
+    // partial (O / l, lse) is written out. The softmax warps never wait for it.
+    constexpr int DH = D / 2;   // staged columns per row
+    constexpr int NC = DH / 4;  // 16-byte chunks per staged row (swizzled by row)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -376,31 +387,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float f0 = w0 * inv, f1 = w1 * inv;
       const bool sok = SKV_OK(I.slot >= 0 && (int64_t)I.slot < (int64_t)pp.hdr->n_slot_base * P.Hkv,
                               pp.hdr, kDbgFwdSlot, I.slot);
+      const uint32_t qb = nit & 1;
+      float* stg = (float*)(smem + Lay::q + qb * Lay::tile) + r * DH;
+      auto chunk = [&](int ch) { return 4 * (ch ^ (r & (NC - 1))); };
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {  // 32 columns of each half at a time (register budget)
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tO + lane_base + 32 * c, v0);
-        tmem_ld32(tO + D + lane_base + 32 * c, v1);
-        tmem_ld_wait(v0);
-        tmem_ld_wait(v1);
-        if (c == D / 32 - 1) {  // O and the row statistics are in registers
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(o_free);
-        }
+      for (int c = 0; c < DH; c += 16) {
+        uint32_t a[16], b[16];
+        tmem_ld16(tO + lane_base + c, a);
+        tmem_ld16(tO + D + lane_base + c, b);
+        tmem_ld_wait16(a);
+        tmem_ld_wait16(b);
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          float o[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            o[k] = fmaf(__uint_as_float(v0[i + k]), f0, __uint_as_float(v1[i + k]) * f1);
-          if (sok)
-            st_global_v8(wk.part_o + part_off(I.slot, r, 32 * c + i, D), o[0], o[1], o[2], o[3],
-                         o[4], o[5], o[6], o[7]);
+        for (int j = 0; j < 16; j += 4) {
+          float4 v;
+          v.x = fmaf(__uint_as_float(a[j]), f0, __uint_as_float(b[j]) * f1);
+          v.y = fmaf(__uint_as_float(a[j + 1]), f0, __uint_as_float(b[j + 1]) * f1);
+          v.z = fmaf(__uint_as_float(a[j + 2]), f0, __uint_as_float(b[j + 2]) * f1);
+          v.w = fmaf(__uint_as_float(a[j + 3]), f0, __uint_as_float(b[j + 3]) * f1);
+          *(float4*)(stg + chunk((c + j) / 4)) = v;
         }
       }
-      if (sok)
+      float oh[DH];
+#pragma unroll
+      for (int c = 0; c < DH; c += 16) {
+        uint32_t a[16], b[16];
+        tmem_ld16(tO + lane_base + DH + c, a);
+        tmem_ld16(tO + D + lane_base + DH + c, b);
+        tmem_ld_wait16(a);
+        tmem_ld_wait16(b);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          oh[c + j] = fmaf(__uint_as_float(a[j]), f0, __uint_as_float(b[j]) * f1);
+      }
+      tc_fence_before();  // O and the row statistics are in registers and staging
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      if (sok) {
+#pragma unroll
+        for (int i = 0; i < DH; i += 8)
+          st_global_v8(wk.part_o + part_off(I.slot, r, DH + i, D), oh[i], oh[i + 1], oh[i + 2],
+                       oh[i + 3], oh[i + 4], oh[i + 5], oh[i + 6], oh[i + 7]);
+#pragma unroll
+        for (int i = 0; i < DH; i += 8) {
+          const float4 x = *(const float4*)(stg + chunk(i / 4));
+          const float4 y = *(const float4*)(stg + chunk(i / 4 + 1));
+          st_global_v8(wk.part_o + part_off(I.slot, r, i, D), x.x, x.y, x.z, x.w, y.x, y.y, y.z,
+                       y.w);
+        }
         wk.part_lse[(size_t)I.slot * kRows + r] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+      }
+      fence_proxy_async_shared();  // the staging reads come before the next TMA load here
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_free + qb);
     }
   } else {
     // ---------------- softmax (warps 2..9) ----------------
