@@ -607,19 +607,6 @@ struct DqLayout {
   static constexpr uint32_t total = bars + 512 + 1024;
 };
 
-// Row r of a [128 rows][64 bf16] sub-tile laid out by a 128-byte-swizzled TMA
-// box: its 16-byte chunk c sits at chunk c ^ (r % 8) of the row.
-__device__ __forceinline__ void lds_row_sw128(const uint8_t* sub, int r, uint32_t (&v)[32]) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 x = *(const uint4*)(sub + r * 128 + ((c ^ (r & 7)) << 4));
-    v[4 * c] = x.x;
-    v[4 * c + 1] = x.y;
-    v[4 * c + 2] = x.z;
-    v[4 * c + 3] = x.w;
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -631,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = (uint64_t*)(smem + Lay::bars);
   uint64_t* q_full = bars + 0;          // Q, dO of the item in shared memory
-  uint64_t* q_empty = bars + 1;         // ... copied to TMEM (4 arrivals)
+  uint64_t* q_empty = bars + 1;         // ... copied to TMEM (the copies are done)
   uint64_t* k_full = bars + 2;          // [kDqNK]
   uint64_t* k_empty = k_full + kDqNK;
   // V is read only by dP: V stage and dp_full of tile t are both t % 2, so
@@ -643,8 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_full = s_read + 1;       // [2] dP of tile t (by tile parity)
   uint64_t* p_ready = dp_full + 2;      // [2] softmax wrote dS (bf16) over dP of tile t
   uint64_t* rfree = p_ready + 2;        // [2] the dQ MMA of tile t has read dS: region free
-  uint64_t* qt_ready = rfree + 2;       // Q, dO of the item are in TMEM (4 arrivals)
-  uint64_t* qt_empty = qt_ready + 1;    // the item's S and dP MMAs are done with them
+  uint64_t* qt_empty = rfree + 2;       // the item's S and dP MMAs are done with Q, dO in TMEM
   uint64_t* dq_done = qt_empty + 1;
   uint64_t* dq_free = dq_done + 1;
   uint64_t* mma_drain = dq_free + 1;    // [2] one per issuing warp
@@ -656,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 4);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kDqNK; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -669,7 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_ready + b, kSoftmaxWarps);
       mbar_init(rfree + b, 1);
     }
-    mbar_init(qt_ready, 4);
     mbar_init(qt_empty, 1);
     mbar_init(dq_done, 1);
     mbar_init(dq_free, 4);
@@ -767,13 +752,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S of tile t lands on the region the dQ MMA of tile t-2 read (rfree);
     // dP of tile t lands on S once the softmax has loaded it (s_read).
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+    const uint64_t qsd0 = desc_kmajor0(smem_u32(smem + Lay::q));
+    const uint64_t dosd0 = desc_kmajor0(smem_u32(smem + Lay::dO));
     uint32_t gt = 0, nit = 0;  // gt: tiles issued (K and V ring index)
     bool ok = true;
     FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = In;
       if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
-      if (!(ok = warp_wait(qt_ready, nit & 1, abort_flag))) break;
+      // Q and dO of the item into TMEM: asynchronous shared-memory -> TMEM
+      // copies, one per 16-element k step, once the previous item's S and dP
+      // are done with the columns; the item's first S follows them in issue
+      // order, which orders it after the copies.
+      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
+      if (nit > 0 && !(ok = warp_wait(qt_empty, (nit - 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          tmem_cp_128x256b(tQ + kk * 8, qsd0 + (kmajor_off(kk) >> 4));
+          tmem_cp_128x256b(tdO + kk * 8, dosd0 + (kmajor_off(kk) >> 4));
+        }
+        mma_commit(q_empty);  // the shared-memory tiles may take the next item
+      }
+      __syncwarp();
       for (int t = 0; t < I.ntiles; ++t, ++gt) {
         const uint32_t ks = gt % kDqNK, vs = gt % kDqNV, b = gt & 1;
         const uint32_t tR = tmem + 128 * b;
@@ -838,11 +840,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait_drain(mma_drain + 1, 0, kDrainNs);
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-    // ---------------- Q/dO copy and epilogue (warps 11..14): one lane quadrant each ----------------
-    // Per item: copy the rows of Q and dO from their swizzled shared-memory
-    // tiles into TMEM (once the previous item's S and dP are done with
-    // them); then write the previous item's dQ partial once its last dQ MMA
-    // is done, releasing the accumulator right after loading it.
+    // ---------------- epilogue (warps 11..14): one lane quadrant each ----------------
+    // Writes each item's dQ partial once its last dQ MMA is done, releasing
+    // the accumulator right after loading it.
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -872,37 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    FwdItem Iprev{};
     uint32_t nit = 0;
     FwdItem In = q0 < q1 ? ld_rec(pp.f_rec + q0) : FwdItem{};
     for (int qi = q0; qi < q1 && ok; ++qi, ++nit) {
       const FwdItem I = In;
       if (qi + 1 < q1) In = ld_rec(pp.f_rec + qi + 1);  // lands during this item
-      if (!(ok = warp_wait(q_full, nit & 1, abort_flag))) break;
-      if (nit > 0 && !(ok = warp_wait(qt_empty, (nit - 1) & 1, abort_flag))) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {  // Q, then dO
-        const uint8_t* tile = smem + (which == 0 ? Lay::q : Lay::dO);
-        const uint32_t tcol = (which == 0 ? tQ : tdO) + lane_base;
-#pragma unroll 1
-        for (int sub = 0; sub < kSub; ++sub) {
-          uint32_t v[32];
-          lds_row_sw128(tile + sub * kSubBytes, r, v);
-          tmem_st32(tcol + 32 * sub, v);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(qt_ready);
-        mbar_arrive(q_empty);  // the shared-memory tiles may take the next item
-      }
-      if (nit > 0 && !(ok = write_dq(Iprev, nit - 1))) break;
-      Iprev = I;
+      ok = write_dq(I, nit);
     }
-    if (ok && nit > 0) write_dq(Iprev, nit - 1);
   } else {
     // softmax (warps 2..9): lane quadrant warp % 4, column half hf
     const int wq = warp & 3;

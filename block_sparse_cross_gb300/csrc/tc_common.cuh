@@ -172,6 +172,16 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
+// Shared memory -> TMEM copy of 128 rows x 32 bytes, the rows described by a
+// shared-memory matrix descriptor exactly as for an MMA operand (one 16-element
+// k step of a K-major tile): lane r receives row r in 8 columns of packed
+// 16-bit pairs, the layout of an A operand in TMEM. Asynchronous; ordered
+// before a later tcgen05.mma of the same thread; completion tracked by
+// tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives on `bar` once every previously issued tcgen05 op of this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
