@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
         H->bwd_total_cost = carry_c;
       }
     }
+    // the rank kernel accumulates each item's rank here (the LPT overwrites it)
+    int32_t* racc = kind == 0 ? pp.f_pos : pp.b_pos;
+    for (int64_t x = tid; x < carry_n; x += blockDim.x) racc[x] = 0;
     __syncthreads();
   }
   if (tid == 0) {
@@ -261,7 +264,12 @@ __global__ void __launch_bounds__(1024) plan_setup_kernel(ProbDev P, PlanPtrs pp
 
 // Rank of item i = #{j : cost_j > cost_i or (cost_j == cost_i and j < i)}.
 // Keys are unique, so the ranks form the permutation of the sort
-// (cost desc, id asc); items are in id order after compaction.
+// (cost desc, id asc); items are in id order after compaction. CTA (x, kind,
+// z) counts for its 256 items over the z-th of kRankSlices slices of j and
+// adds its counts to the items' accumulators (zeroed by the setup kernel):
+// integer sums, so the order of the additions does not matter.
+constexpr int kRankSlices = 8;
+
 __global__ void __launch_bounds__(256) plan_rank_kernel(PlanPtrs pp) {
   __shared__ int64_t tile[1024];
   const PlanHeader* H = pp.hdr;
@@ -272,23 +280,23 @@ __global__ void __launch_bounds__(256) plan_rank_kernel(PlanPtrs pp) {
   const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if ((int)(blockIdx.x * blockDim.x) >= n) return;  // whole CTA idle
+  const int per = (n + (int)gridDim.z - 1) / (int)gridDim.z;
+  const int jb = (int)blockIdx.z * per, je = min(n, jb + per);
+  if (jb >= je) return;  // CTA-uniform
   const int64_t ci = i < n ? cost[item[i]] : 0;
   int rank = 0;
-  for (int j0 = 0; j0 < n; j0 += 1024) {
+  for (int j0 = jb; j0 < je; j0 += 1024) {
     __syncthreads();
     for (int t = threadIdx.x; t < 1024; t += blockDim.x)
-      tile[t] = (j0 + t < n) ? cost[item[j0 + t]] : INT64_MIN;
+      tile[t] = (j0 + t < je) ? cost[item[j0 + t]] : INT64_MIN;
     __syncthreads();
-    const int lim = min(1024, n - j0);
+    const int lim = min(1024, je - j0);
     for (int t = 0; t < lim; ++t) {
       const int64_t cj = tile[t];
       rank += (cj > ci) | ((cj == ci) & (j0 + t < i));
     }
   }
-  if (i < n && SKV_OK(rank < n, H, kDbgPlanScatter, rank)) {
-    (kind == 0 ? pp.f_sorted : pp.b_sorted)[rank] = i;
-    (kind == 0 ? pp.f_scost : pp.b_scost)[rank] = ci;
-  }
+  if (i < n && rank > 0) atomicAdd((kind == 0 ? pp.f_pos : pp.b_pos) + i, rank);
 }
 
 namespace {
@@ -568,6 +576,23 @@ __global__ void __launch_bounds__(1024) plan_assign_kernel(ProbDev P, PlanPtrs p
   const int m = P.workers, Hkv = P.Hkv, G = m / Hkv;
   const bool contiguous = (P.flags & SPLITKV_FLAG_CONTIGUOUS) != 0;
   const int warp = tid >> 5;
+  // the sort order from the ranks the rank kernel accumulated in f_pos / b_pos
+  for (int kind = 0; kind < 2; ++kind) {
+    const int n = kind == 0 ? H->n_fwd_items : H->n_bwd_items;
+    const int32_t* racc = kind == 0 ? pp.f_pos : pp.b_pos;
+    const int64_t* cost = kind == 0 ? pp.f_cost : pp.b_cost;
+    const int32_t* item = kind == 0 ? pp.f_item : pp.b_item;
+    int32_t* sorted = kind == 0 ? pp.f_sorted : pp.b_sorted;
+    int64_t* scost = kind == 0 ? pp.f_scost : pp.b_scost;
+    for (int i = tid; i < n; i += blockDim.x) {
+      const int r = racc[i];
+      if (SKV_OK(r >= 0 && r < n, H, kDbgPlanScatter, r)) {
+        sorted[r] = i;
+        scost[r] = cost[item[i]];
+      }
+    }
+  }
+  __syncthreads();  // the LPT reads the sorted costs and overwrites f_pos / b_pos
   if (warp < 2) {
     const int n = warp == 0 ? H->n_fwd_items : H->n_bwd_items;
     lpt_warp(n, G, warp == 0 ? pp.f_scost : pp.b_scost, warp == 0 ? pp.f_grp : pp.b_grp,
@@ -672,7 +697,7 @@ cudaError_t launch_plan(const ProbDev& P, const PlanPtrs& pp, const PlanCaps& ca
   if (err != cudaSuccess) return err;
   const int64_t maxn = caps.NCF > caps.NCB ? caps.NCF : caps.NCB;
   dim3 grid((unsigned)((maxn + 255) / 256 > 0 ? (maxn + 255) / 256 : 1), 2);
-  plan_rank_kernel<<<grid, 256, 0, st>>>(pp);
+  plan_rank_kernel<<<dim3(grid.x, 2, kRankSlices), 256, 0, st>>>(pp);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   plan_assign_kernel<<<1, 1024, 0, st>>>(P, pp);
