@@ -443,7 +443,13 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   if (work_bytes < work_bytes_for(prob)) return SPLITKV_EWORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
-  if (prob->total_ctx > 0) {
+  const bool tc = use_tensor_cores(c.P);
+  // The tensor-core dK/dV kernel also sums the dQ partials and zeroes the
+  // dK/dV rows of keys no block sees (its reduction warp streams the partials
+  // from HBM while the tensor pipe works); otherwise each is a launch of its
+  // own.
+  const bool fused = tc && any_q && prob->total_ctx > 0 && c.caps.NSL > 0;
+  if (prob->total_ctx > 0 && !fused) {
     e = timed(SPLITKV_K_ZERO, 1, s,
               [&] { return launch_zero_uncovered(c.P, c.pp, c.caps.NCB, dKc, dVc, s); });
     if (e != cudaSuccess) return SPLITKV_ECUDA;
@@ -456,7 +462,6 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
     return launch_bwd_draft(c.P, c.pp, wk, Q, Kd, Vd, O, LSE, dO, dKd, dVd, c.caps.NSL, s);
   });
   if (e != cudaSuccess) return SPLITKV_ECUDA;
-  const bool tc = use_tensor_cores(c.P);
   e = timed(SPLITKV_K_BWD_DQ, 1, s, [&] {
     return tc ? launch_bwd_dq_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s)
               : launch_bwd_dq_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, s);
@@ -464,11 +469,13 @@ int splitkv_bwd(const splitkv_problem* prob, const void* plan_ws, const void* Q,
   if (e != cudaSuccess) return SPLITKV_ECUDA;
   if (prob->total_ctx > 0) {
     e = timed(SPLITKV_K_BWD_DKDV, 1, s, [&] {
-      return tc ? launch_bwd_dkdv_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s)
+      return tc ? launch_bwd_dkdv_tc(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc,
+                                     fused ? dQ : nullptr, s)
                 : launch_bwd_dkdv_simt(c.P, c.pp, wk, Q, Kc, Vc, dO, LSE, dKc, dVc, s);
     });
     if (e != cudaSuccess) return SPLITKV_ECUDA;
   }
+  if (fused) return SPLITKV_OK;
   return cuda_status(
       timed(SPLITKV_K_DQ_REDUCE, 1, s,
             [&] { return launch_dq_reduce(c.P, c.pp, wk, dQ, c.caps.NSL, s); }));

@@ -43,10 +43,26 @@ constexpr int kThreads = 512;    // forward and dQ
 constexpr int kVWarp = 15;
 // dK / dV: warps 2..17 are the softmax (four per TMEM lane quadrant, one
 // 32-row quarter of the slab each; on config 4 at L = 262144 this ran 2 %
-// faster than two half-row warps per quadrant), warp 18 loads dO
+// faster than two half-row warps per quadrant), warp 18 loads dO, warp 19
+// sums the dQ kernel's chunk partials into dQ while the tensor pipe works
+// (the reduction reads HBM, the rest of the kernel hardly does). Twenty
+// warps put five on each SM sub-partition, which leaves 96 registers a
+// thread; a 21st warp would cut that to 80.
 constexpr int kKvSoftmaxWarps = 16;
 constexpr int kKvDoWarp = 2 + kKvSoftmaxWarps;
-constexpr int kThreadsKv = 32 * (kKvDoWarp + 1);
+constexpr int kKvRedWarp = kKvDoWarp + 1;
+constexpr int kThreadsKv = 32 * (kKvRedWarp + 1);
+// the reduction streams [128 rows][8] fp32 pieces (4 KB, one dims group of a
+// partial tile, contiguous) through a ring of shared-memory stages
+constexpr int kRedStages = 6;
+constexpr uint32_t kRedPieceBytes = kRows * 8u * 4u;
+// Stages read before they are refilled together, and the pause between polls
+// of a stage not yet filled. Polling without a pause and refilling every
+// stage at once slowed the dK/dV work beside it by up to 1.7 % on config 4 at
+// L = 262144 (the warp's issue slots are the softmax warps'); these values
+// left it within 0.1 % of the kernel without the reduction.
+constexpr int kRedRefill = 3;
+constexpr uint32_t kRedSleepNs = 200;
 constexpr int kEpiWarp0 = 11;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one column half each
 constexpr uint32_t kSubBytes = 16384; // one [128 rows][64 bf16] swizzled sub-tile
@@ -1005,8 +1021,10 @@ struct KvLayout {
   static constexpr uint32_t info_off = 2 * kSub * kSubBytes;       // inside a stage
   static constexpr uint32_t stage_bytes = 2 * kSub * kSubBytes + 2048;  // Q, dO, row table
   static constexpr uint32_t bars = stage0 + kNS * stage_bytes;
-  static constexpr uint32_t total = bars + 512 + 1024;
+  static constexpr uint32_t red = bars + 512;  // the dQ reduction's ring, then its draft rows
+  static constexpr uint32_t total = red + (kRedStages + 1) * kRedPieceBytes + 1024;
 };
+static_assert(KvLayout<128>::total <= 232448, "dK/dV shared memory above the per-CTA limit");
 
 using KvItem = BwdRec;
 
@@ -1021,12 +1039,223 @@ __device__ __forceinline__ BwdRec ld_brec(const BwdRec* p) {
   return R;
 }
 
+// dQ = scale * (the row's chunk partials summed in ascending chunk order +
+// its draft term), run by the reduction warp of the dK/dV kernel. Tasks are
+// (slab, kv head) pairs, taken from a counter in the work workspace so that
+// the CTAs finish their shares together. For each 8-dim group
+// of the slab's 128 x d partial tiles, the chunks that any of its rows reads
+// are copied one 4 KB piece at a time into a ring of kRedStages
+// shared-memory stages (with an evict-first L2 policy: each partial is read
+// once); lane l sums rows l + 32 i over the chunks of each row's own range
+// only and writes the group's 8 dims of each row, whose draft term was
+// copied into shared memory while the chunks streamed. The warp alone reads the
+// ring, so stages are refilled as soon as the warp has read kRedRefill of
+// them (one proxy fence orders those reads before the copies), and the
+// copies run in ring order across tasks. The sums run in the same order as the standalone
+// dq_reduce kernel, so the result is the same bit for bit.
+// Waits like warp_wait; with kRedSleepNs > 0 the warp pauses between polls,
+// leaving its issue slots to the softmax warps of its SM sub-partition.
+__device__ __forceinline__ bool red_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool mine;
+  if (kRedSleepNs == 0) {
+    mine = mbar_wait(bar, parity, abort);
+  } else {
+    mine = mbar_try_wait(bar, parity);
+    const uint64_t t0 = mine ? 0 : globaltimer();
+    for (uint32_t it = 1; !mine; ++it) {
+      __nanosleep(kRedSleepNs);
+      if ((mine = mbar_try_wait(bar, parity))) break;
+      if ((it & 15) == 0) {
+        if (*abort) break;
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+          *abort = 1;
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, mine);
+}
+
+template <int D>
+__device__ __forceinline__ void kv_dq_reduce(const ProbDev& P, const PlanPtrs& pp,
+                                             const WorkPtrs& wk, __nv_bfloat16* __restrict__ dQ,
+                                             float* ring, uint64_t* full, volatile int* abort_flag,
+                                             int lane) {
+  constexpr int kPieces = D / 8;
+  constexpr uint32_t kPieceFloats = kRedPieceBytes / 4;
+  const int ntask = pp.hdr->n_slabs * P.Hkv;
+  const size_t cstride = (size_t)P.Hkv * kRows * D;  // floats between chunk tiles
+  const uint64_t policy = l2_evict_first_policy();
+  float* dbuf = ring + kRedStages * kPieceFloats;  // [128 rows][8] draft term of one piece
+  uint32_t cs = 0, cpar = 0;  // ring stage of the next copy to read, and its phase parity
+  uint32_t is = 0;            // ring stage of the next copy to issue
+  int pend = 0;               // stages read since the last proxy fence
+  bool ok = true;
+  int t = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(wk.red_next, 1) : 0, 0);
+  while (t < ntask && ok) {
+    // the next task is claimed now; the answer is needed only at the end
+    const int tn = lane == 0 ? atomicAdd(wk.red_next, 1) : 0;
+    const int sg = t / P.Hkv, g = t - sg * P.Hkv;
+    const int first = pp.sl_first[sg], nblk = pp.sl_nblk[sg];
+    const size_t slot0 = (size_t)pp.sl_slot[sg];
+    // chunk range [clo, cend) and output row of rows lane + 32 i
+    int clo[4], cend[4], qrow[4];
+    int cmin = 0x7fffffff, cmax = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const RowInfo ri = row_info(P, first, nblk, g, lane + 32 * i);
+      clo[i] = cend[i] = 0;
+      qrow[i] = -1;
+      if (ri.n >= 0) {
+        const int na = (ri.anchor + P.chunk - 1) / P.chunk;
+        clo[i] = ri.lo >= ri.anchor ? na : ri.lo / P.chunk;
+        cend[i] = SKV_OK(slot0 + (size_t)na <= (size_t)pp.hdr->n_slot_base, pp.hdr,
+                         kDbgReduceSlot, slot0 + na)
+                      ? na
+                      : clo[i];
+        if (cend[i] > clo[i]) {
+          cmin = min(cmin, clo[i]);
+          cmax = max(cmax, cend[i]);
+        }
+        if (SKV_OK(ri.n < P.NQ && ri.h >= 0 && ri.h < P.Hq, pp.hdr, kDbgQueryRow, ri.n))
+          qrow[i] = ri.n * P.Hq + ri.h;
+      }
+    }
+    cmin = (int)__reduce_min_sync(0xffffffffu, (uint32_t)cmin);
+    cmax = (int)__reduce_max_sync(0xffffffffu, (uint32_t)cmax);
+    const int nch = cmax > cmin ? cmax - cmin : 0;
+    if (nch == 0) cmin = 0;       // no row reads a partial: only the draft term
+    const int K = kPieces * nch;  // copies of this task: dims group-major, then chunk
+    // the next copy to issue: dims group ip of chunk cmin + ic, into stage is
+    const float* tile0 = wk.part_o + part_off((slot0 + cmin) * P.Hkv + g, 0, 0, D);
+    int ip = 0, ic = 0, issued = 0;
+    auto issue = [&]() {
+      if (elect_one()) {
+        mbar_expect_tx(full + is, kRedPieceBytes);
+        bulk_load_hint(ring + is * kPieceFloats, tile0 + (size_t)ic * cstride + ip * kPieceFloats,
+                       kRedPieceBytes, full + is, policy);
+      }
+      __syncwarp();
+      ++issued;
+      if (++is == (uint32_t)kRedStages) is = 0;
+      if (++ic == nch) {
+        ic = 0;
+        ++ip;
+      }
+    };
+    if (K > 0 && pend > 0) {  // stages read by the previous task are refilled now
+      fence_proxy_async_shared();
+      __syncwarp();
+      pend = 0;
+    }
+    for (int k = 0; k < K && k < kRedStages; ++k) issue();
+    int k = 0;  // copies read
+    for (int p = 0; p < kPieces && ok; ++p) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (qrow[i] < 0) continue;
+        const float* src = wk.dq_draft + (size_t)qrow[i] * D + 8 * p;
+        cp_async16(dbuf + (lane + 32 * i) * 8, src);
+        cp_async16(dbuf + (lane + 32 * i) * 8 + 4, src + 4);
+      }
+      float acc[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+      for (int c = cmin; c < cmin + nch; ++c) {
+        if (!(ok = red_wait(full + cs, cpar, abort_flag))) break;
+        const float* sp = ring + cs * kPieceFloats;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (c >= clo[i] && c < cend[i]) {
+            const int r = lane + 32 * i;
+            const float4 a = *(const float4*)(sp + r * 8);
+            const float4 b = *(const float4*)(sp + r * 8 + 4);
+            float* o = acc[i];
+            o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
+            o[4] += b.x; o[5] += b.y; o[6] += b.z; o[7] += b.w;
+          }
+        }
+        ++k;
+        if (++pend >= kRedRefill && issued < K) {  // refill the stages just read
+          fence_proxy_async_shared();
+          __syncwarp();
+          for (; pend > 0 && issued < K; --pend) issue();
+          pend = 0;
+        }
+        if (++cs == (uint32_t)kRedStages) {
+          cs = 0;
+          cpar ^= 1u;
+        }
+      }
+      cp_async_wait_all();
+      if (!ok) break;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (qrow[i] < 0) continue;
+        const size_t row = (size_t)qrow[i] * D + 8 * p;
+        const float4 a = *(const float4*)(dbuf + (lane + 32 * i) * 8);
+        const float4 b = *(const float4*)(dbuf + (lane + 32 * i) * 8 + 4);
+        uint4 w;
+        w.x = pack_bf16((acc[i][0] + a.x) * P.scale, (acc[i][1] + a.y) * P.scale);
+        w.y = pack_bf16((acc[i][2] + a.z) * P.scale, (acc[i][3] + a.w) * P.scale);
+        w.z = pack_bf16((acc[i][4] + b.x) * P.scale, (acc[i][5] + b.y) * P.scale);
+        w.w = pack_bf16((acc[i][6] + b.z) * P.scale, (acc[i][7] + b.w) * P.scale);
+        *(uint4*)(dQ + row) = w;
+      }
+    }
+    if (!ok) {
+      // copies issued and not read land before the CTA exits: the one the
+      // warp gave up on (stage cs) and those after it in ring order
+      uint32_t st = cs, par = cpar;
+      for (int i = k; i < issued; ++i) {
+        mbar_wait_drain(full + st, par, kDrainNs);
+        if (++st == (uint32_t)kRedStages) {
+          st = 0;
+          par ^= 1u;
+        }
+      }
+    }
+    t = __shfl_sync(0xffffffffu, tn, 0);
+  }
+}
+
+// Key tiles that no block sees (backward candidates of cost 0) are in no
+// backward item; their dK and dV rows are zero. Run by the reduction warp of
+// the dK/dV kernel after its dQ tasks: candidate c on CTA c mod the grid,
+// 16-byte stores.
+template <int D>
+__device__ __forceinline__ void kv_zero_unseen(const ProbDev& P, const PlanPtrs& pp,
+                                               __nv_bfloat16* __restrict__ dKc,
+                                               __nv_bfloat16* __restrict__ dVc, int lane) {
+  const int ncand = pp.hdr->n_bwd_cand;
+  const size_t row16 = (size_t)P.Hkv * D * 2 / 16;  // 16-byte units of a key row
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int cand = blockIdx.x; cand < ncand; cand += gridDim.x) {
+    if (pp.b_cost[cand] != 0) continue;  // warp-uniform
+    const int s = seg_of(pp.s_bcand_off, P.S, cand);
+    const int kt = cand - pp.s_bcand_off[s];
+    const int c0 = P.cu_ctx[s], L = P.cu_ctx[s + 1] - c0;
+    const int k0 = kt * kKeyTile, k1 = min(L, k0 + kKeyTile);
+    if (!SKV_OK(k0 >= 0 && (int64_t)c0 + k1 <= P.T, pp.hdr, kDbgZeroRow, (int64_t)c0 + k1))
+      continue;
+    const size_t lo = (size_t)(c0 + k0) * row16, hi = (size_t)(c0 + k1) * row16;
+    for (size_t i = lo + lane; i < hi; i += 32) {
+      ((uint4*)dKc)[i] = z;
+      ((uint4*)dVc)[i] = z;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsKv, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        ProbDev P, PlanPtrs pp, WorkPtrs wk, const float* __restrict__ LSE,
-                       __nv_bfloat16* __restrict__ dKc, __nv_bfloat16* __restrict__ dVc) {
+                       __nv_bfloat16* __restrict__ dKc, __nv_bfloat16* __restrict__ dVc,
+                       __nv_bfloat16* __restrict__ dQ) {
   using Lay = KvLayout<D>;
   constexpr int kSub = Lay::kSub;
   extern __shared__ uint8_t smem_raw[];
@@ -1043,6 +1272,8 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   uint64_t* acc_done = ds_ready + 1;
   uint64_t* acc_free = acc_done + 1;
   uint64_t* mma_drain = acc_free + 1;
+  uint64_t* red_full = bars + 16;   // [kRedStages] a partial piece is in its stage
+  static_assert(16 + kRedStages <= 32, "reduction barriers below the TMEM slot");
   uint32_t* tmem_slot = (uint32_t*)(bars + 32);
   volatile int* abort_flag = (volatile int*)(bars + 33);
 
@@ -1064,6 +1295,7 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
     mbar_init(acc_done, 1);
     mbar_init(acc_free, kKvSoftmaxWarps);
     mbar_init(mma_drain, 1);
+    for (int s = 0; s < kRedStages; ++s) mbar_init(red_full + s, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1079,7 +1311,14 @@ __global__ void __launch_bounds__(kThreadsKv, 1)
   const int q0 = pp.b_qoff[blockIdx.x];
   const int q1 = queue_end(pp.b_qoff, blockIdx.x, (int64_t)pp.hdr->n_bwd_items * P.Hkv, pp.hdr);
 
-  if (warp == 0) {
+  if (warp == kKvRedWarp) {
+    // ---------------- dQ reduction and the zero rows (independent of the
+    // items) ----------------
+    if (dQ != nullptr) {
+      kv_dq_reduce<D>(P, pp, wk, dQ, (float*)(smem + Lay::red), red_full, abort_flag, lane);
+      kv_zero_unseen<D>(P, pp, dKc, dVc, lane);
+    }
+  } else if (warp == 0) {
     // ---------------- producer: K/V per item, then Q and the slab's row table
     // (one bulk copy of the precomputed record) per slab; dO comes from
     // warp 10 ----------------
@@ -1469,7 +1708,8 @@ cudaError_t launch_bwd_dq_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtr
 
 cudaError_t launch_bwd_dkdv_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                                const void* Q, const void* Kc, const void* Vc, const void* dO,
-                               const float* LSE, void* dKc, void* dVc, cudaStream_t st) {
+                               const float* LSE, void* dKc, void* dVc, void* dQ,
+                               cudaStream_t st) {
   Maps m;
   cudaError_t e = make_maps(P, Q, dO, Kc, Vc, &m);
   if (e != cudaSuccess) return e;
@@ -1477,12 +1717,14 @@ cudaError_t launch_bwd_dkdv_tc(const ProbDev& P, const PlanPtrs& pp, const WorkP
     auto k = bwd_dkdv_tc_kernel<128>;
     if ((e = prep(k, KvLayout<128>::total)) != cudaSuccess) return e;
     k<<<P.workers, kThreadsKv, KvLayout<128>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
-                                                          (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
+                                                          (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc,
+                                                          (__nv_bfloat16*)dQ);
   } else {
     auto k = bwd_dkdv_tc_kernel<64>;
     if ((e = prep(k, KvLayout<64>::total)) != cudaSuccess) return e;
     k<<<P.workers, kThreadsKv, KvLayout<64>::total, st>>>(m.q, m.dO, m.k, m.v, P, pp, wk, LSE,
-                                                         (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc);
+                                                         (__nv_bfloat16*)dKc, (__nv_bfloat16*)dVc,
+                                                         (__nv_bfloat16*)dQ);
   }
   return cudaGetLastError();
 }

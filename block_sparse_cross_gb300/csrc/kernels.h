@@ -26,9 +26,12 @@ cudaError_t launch_fwd_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& 
 cudaError_t launch_bwd_dq_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                              const void* Q, const void* Kc, const void* Vc, const void* dO,
                              const float* LSE, cudaStream_t st);
+// dQ != nullptr: the kernel also reduces the dQ partials into dQ (bf16) and
+// zeroes the dK/dV rows of key tiles no block sees
 cudaError_t launch_bwd_dkdv_tc(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,
                                const void* Q, const void* Kc, const void* Vc, const void* dO,
-                               const float* LSE, void* dKc, void* dVc, cudaStream_t st);
+                               const float* LSE, void* dKc, void* dVc, void* dQ,
+                               cudaStream_t st);
 
 // rows.cu — HBM-bound row kernels
 cudaError_t launch_merge(const ProbDev& P, const PlanPtrs& pp, const WorkPtrs& wk,

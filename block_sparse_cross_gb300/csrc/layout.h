@@ -188,7 +188,8 @@ inline size_t plan_layout(const PlanCaps& c, char* base, PlanPtrs* p) {
 // Work workspace: partial O (or dQ) [slots][d/8][128][8] fp32 (part_off),
 // partial lse [slots][128] fp32, dQ of the draft blocks [N_q][Hq][d] fp32, the
 // backward row term D [Hq][N_q] fp32, the draft-key P / dS [N_q][Hq][B] and
-// the per-(slab, kv head) row table the dK/dV kernel streams with each slab.
+// the per-(slab, kv head) row table the dK/dV kernel streams with each slab,
+// and the task counter of the dK/dV kernel's dQ reduction.
 struct WorkPtrs {
   float* part_o;
   float* part_lse;
@@ -198,6 +199,8 @@ struct WorkPtrs {
   float* draft_ds;   // [N_q][Hq][B] dS of each draft key
   float* rowinfo;    // [slab][Hkv][4][128]: -LSE*log2(e) (-inf on padding rows), D, and the
                      // row's visible context [lo, end) as int bits
+  int* red_next;     // next (slab, kv head) task of the dQ reduction; zeroed by the row-table
+                     // kernel before each backward's dQ and dK/dV kernels
 };
 
 constexpr int kRowInfoFloats = 4 * kRows;  // one (slab, kv head) record: 2048 bytes
@@ -227,6 +230,7 @@ inline size_t work_layout(int64_t slots, int64_t nq, int64_t Hq, int64_t d, int6
   q.draft_p = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
   q.draft_ds = (float*)take(sizeof(float) * (size_t)nq * Hq * B);
   q.rowinfo = (float*)take(sizeof(float) * (size_t)slabs_x_hkv * kRowInfoFloats);
+  q.red_next = (int*)take(sizeof(int));
   if (p) *p = q;
   return align_up(off, 256);
 }

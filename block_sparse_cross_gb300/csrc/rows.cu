@@ -637,6 +637,7 @@ __global__ void __launch_bounds__(256) bwd_draft_block_kernel(ProbDev P, PlanPtr
 __global__ void __launch_bounds__(128) slab_rowinfo_kernel(ProbDev P, PlanPtrs pp, WorkPtrs wk,
                                                            const float* __restrict__ LSE) {
   const int sg = blockIdx.x, g = blockIdx.y, r = threadIdx.x;
+  if (sg == 0 && g == 0 && r == 0) *wk.red_next = 0;  // the dK/dV kernel's task counter
   if (sg >= pp.hdr->n_slabs || read_status(pp.hdr) != 0) return;
   const RowInfo ri = row_info(P, pp.sl_first[sg], pp.sl_nblk[sg], g, r);
   float* rec = wk.rowinfo + ((size_t)sg * P.Hkv + g) * kRowInfoFloats;

@@ -194,7 +194,8 @@ typedef struct splitkv_stats {
  *   plan_bytes: holds the plan (costs, LPT queues, slab tables, status word);
  *               built by splitkv_plan, read by splitkv_fwd / splitkv_bwd.
  *   work_bytes: fp32 partials of the split (per chunk (lse, O) in the forward,
- *               per chunk dQ and the draft-block terms in the backward). This
+ *               per chunk dQ and the draft-block terms in the backward) and
+ *               the backward's row tables and task counter. This
  *               is an upper bound computed from host scalars; the exact need
  *               of a built plan is splitkv_stats.work_bytes_used.
  * Host-only; no device work. Errors: EINVAL (null), EUNSUPPORTED.
@@ -331,14 +332,20 @@ int splitkv_fwd_noalloc(const splitkv_problem* prob, const void* Q, const void* 
  * most SPLITKV_NUM_KERNELS entries are written). Errors: EINVAL, ECUDA.
  */
 enum {
-  SPLITKV_K_PLAN = 0,        /* planner: setup, rank, assign (3 launches) */
+  SPLITKV_K_PLAN = 0,        /* planner: setup, rank, assign, queues (4 launches) */
   SPLITKV_K_FWD_ATTN = 1,    /* forward partial attention (persistent) */
   SPLITKV_K_MERGE = 2,       /* draft partial + log-sum-exp merge */
   SPLITKV_K_BWD_DRAFT = 3,   /* D = rowsum(dO*O) + draft-block backward */
   SPLITKV_K_BWD_DQ = 4,      /* dQ chunk partials (persistent) */
-  SPLITKV_K_BWD_DKDV = 5,    /* dK/dV of 128-key tiles (persistent) */
-  SPLITKV_K_DQ_REDUCE = 6,   /* dQ = scale * sum of partials */
-  SPLITKV_K_ZERO = 7,        /* zero dK/dV rows no block sees */
+  SPLITKV_K_BWD_DKDV = 5,    /* dK/dV of 128-key tiles (persistent); on the
+                                tensor-core path it also sums dQ and zeroes
+                                the rows of keys no block sees */
+  SPLITKV_K_DQ_REDUCE = 6,   /* dQ = scale * sum of partials: a launch of its
+                                own on the CUDA-core path or without context
+                                keys only */
+  SPLITKV_K_ZERO = 7,        /* zero dK/dV rows no block sees: a launch of
+                                its own on the CUDA-core path or without
+                                anchors only */
   SPLITKV_K_PROJ = 8,        /* projection GEMMs (splitkv_proj_*) */
   SPLITKV_NUM_KERNELS = 9
 };
