@@ -1039,20 +1039,6 @@ __device__ __forceinline__ BwdRec ld_brec(const BwdRec* p) {
   return R;
 }
 
-// dQ = scale * (the row's chunk partials summed in ascending chunk order +
-// its draft term), run by the reduction warp of the dK/dV kernel. Tasks are
-// (slab, kv head) pairs, taken from a counter in the work workspace so that
-// the CTAs finish their shares together. For each 8-dim group
-// of the slab's 128 x d partial tiles, the chunks that any of its rows reads
-// are copied one 4 KB piece at a time into a ring of kRedStages
-// shared-memory stages (with an evict-first L2 policy: each partial is read
-// once); lane l sums rows l + 32 i over the chunks of each row's own range
-// only and writes the group's 8 dims of each row, whose draft term was
-// copied into shared memory while the chunks streamed. The warp alone reads the
-// ring, so stages are refilled as soon as the warp has read kRedRefill of
-// them (one proxy fence orders those reads before the copies), and the
-// copies run in ring order across tasks. The sums run in the same order as the standalone
-// dq_reduce kernel, so the result is the same bit for bit.
 // Waits like warp_wait; with kRedSleepNs > 0 the warp pauses between polls,
 // leaving its issue slots to the softmax warps of its SM sub-partition.
 __device__ __forceinline__ bool red_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -1077,6 +1063,20 @@ __device__ __forceinline__ bool red_wait(uint64_t* bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, mine);
 }
 
+// dQ = scale * (the row's chunk partials summed in ascending chunk order +
+// its draft term), run by the reduction warp of the dK/dV kernel. Tasks are
+// (slab, kv head) pairs, taken from a counter in the work workspace so that
+// the CTAs finish their shares together. For each 8-dim group of the slab's
+// 128 x d partial tiles, the chunks that any of its rows reads are copied one
+// 4 KB piece at a time into a ring of kRedStages shared-memory stages (with
+// an evict-first L2 policy: each partial is read once); lane l sums rows
+// l + 32 i over the chunks of each row's own range only and writes the
+// group's 8 dims of each row, whose draft term was copied into shared memory
+// while the chunks streamed. The warp alone reads the ring, so stages are
+// refilled as soon as the warp has read kRedRefill of them (one proxy fence
+// orders those reads before the copies), and the copies run in ring order
+// across tasks. The sums run in the same order as the standalone dq_reduce
+// kernel, so the result is the same bit for bit.
 template <int D>
 __device__ __forceinline__ void kv_dq_reduce(const ProbDev& P, const PlanPtrs& pp,
                                              const WorkPtrs& wk, __nv_bfloat16* __restrict__ dQ,
