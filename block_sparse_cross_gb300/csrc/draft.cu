@@ -579,7 +579,10 @@ cudaError_t launch_bwd_draft_mma(const ProbDev& P, const PlanPtrs& pp, const Wor
     auto k = bwd_draft_mma_kernel<D, NT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int threads = 32 * (R / 16 > 4 ? R / 16 : 4);
+    // eight warps whatever R: shared memory holds four CTAs per SM, so the
+    // extra warps double the loads in flight during staging (the kernel is
+    // latency-bound: 4 warps per CTA left 16 warps per SM, 24 % occupancy)
+    const int threads = 256;
     k<<<dim3((unsigned)P.NA, (unsigned)P.Hkv), threads, smem, st>>>(
         P, pp, wk, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)Kd, (const __nv_bfloat16*)Vd,
         (const __nv_bfloat16*)O, LSE, (const __nv_bfloat16*)dO, (__nv_bfloat16*)dKd,
