@@ -57,10 +57,9 @@ constexpr int kThreadsKv = 32 * (kKvRedWarp + 1);
 constexpr int kRedStages = 6;
 constexpr uint32_t kRedPieceBytes = kRows * 8u * 4u;
 // Stages read before they are refilled together, and the pause between polls
-// of a stage not yet filled. Polling without a pause and refilling every
-// stage at once slowed the dK/dV work beside it by up to 1.7 % on config 4 at
-// L = 262144 (the warp's issue slots are the softmax warps'); these values
-// left it within 0.1 % of the kernel without the reduction.
+// of a stage not yet filled. On one box, at config 4 L = 262144, polling
+// without a pause and refilling every stage at once ran the kernel 1.7 %
+// slower than these values (the warp's issue slots are the softmax warps').
 constexpr int kRedRefill = 3;
 constexpr uint32_t kRedSleepNs = 200;
 constexpr int kEpiWarp0 = 11;
